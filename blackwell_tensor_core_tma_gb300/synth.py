@@ -1,0 +1,221 @@
+"""Seeded synthetic inputs for D = A·B + C.
+
+This module is shared by the CUDA path and the CPU oracle: it produces the
+operand *bit patterns* (bf16 / fp16 / e4m3 codes, UE8M0 scale codes, fp32 C)
+and nothing else.  It contains none of the multiply-accumulate arithmetic.
+
+Random numbers
+    A counter-based splitmix64 stream (Steele, Lea & Flood, "Fast splittable
+    pseudorandom number generators", OOPSLA 2014; the finaliser constants are
+    Vigna's published splitmix64).  Output i of stream (seed, tensor) is
+    ``mix64(base + (i + 1) * GAMMA)`` with ``base = mix64(seed << 32 | tensor)``.
+
+Distributions
+    uniform[-1, 1): the top 24 bits of an output, ``u * 2**-23 - 1`` (exact
+    in fp32).
+    N(0, sigma): Box & Muller (1958), two stream outputs per sample, evaluated
+    in fp64 and rounded to fp32 (sigma is the standard deviation).
+    UE8M0 scale 2**e with e uniform over {-4, ..., 4}: code = e + 127.
+
+Rounding of operands (round to nearest, ties to even, from an fp32 sample)
+    bf16 : the upper half of the binary32 pattern after RNE on bit 16.
+    fp16 : IEEE binary16 (numpy's correctly rounded conversion).
+    e4m3 : OCP 8-bit floating point (E4M3: bias 7, no infinities, max 448,
+           S.1111.111 is NaN), saturating to +-448.
+"""
+
+from __future__ import annotations
+
+import dataclasses
+import numpy as np
+
+GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+# stream ids of the tensors of one problem
+T_A, T_B, T_C, T_SFA, T_SFB = 0, 1, 2, 3, 4
+
+_CHUNK = 1 << 22
+
+
+def mix64(z: np.ndarray) -> np.ndarray:
+    """splitmix64 finaliser on a uint64 array (wrapping arithmetic)."""
+    z = z.astype(np.uint64, copy=True)
+    z ^= z >> np.uint64(30)
+    z *= _M1
+    z ^= z >> np.uint64(27)
+    z *= _M2
+    z ^= z >> np.uint64(31)
+    return z
+
+
+def _base(seed: int, tensor: int) -> np.uint64:
+    key = np.array([((seed & 0xFFFFFFFF) << 32) | (tensor & 0xFFFFFFFF)], dtype=np.uint64)
+    return mix64(key)[0]
+
+
+def stream(seed: int, tensor: int, start: int, count: int) -> np.ndarray:
+    """Outputs start .. start+count-1 of the (seed, tensor) stream."""
+    with np.errstate(over="ignore"):
+        i = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+        return mix64(_base(seed, tensor) + i * GAMMA)
+
+
+def uniform_pm1(seed: int, tensor: int, n: int) -> np.ndarray:
+    """n fp32 samples of uniform[-1, 1) on a 2**-23 grid."""
+    out = np.empty(n, dtype=np.float32)
+    for s in range(0, n, _CHUNK):
+        c = min(_CHUNK, n - s)
+        x = stream(seed, tensor, s, c) >> np.uint64(40)
+        out[s:s + c] = (x.astype(np.float64) * 2.0 ** -23 - 1.0).astype(np.float32)
+    return out
+
+
+def normal(seed: int, tensor: int, n: int, sigma: float = 1.0) -> np.ndarray:
+    """n fp32 samples of N(0, sigma**2) by Box-Muller (outputs 2i and 2i+1)."""
+    out = np.empty(n, dtype=np.float32)
+    for s in range(0, n, _CHUNK):
+        c = min(_CHUNK, n - s)
+        x = stream(seed, tensor, 2 * s, 2 * c)
+        u1 = ((x[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0 ** -53
+        u2 = (x[1::2] >> np.uint64(11)).astype(np.float64) * 2.0 ** -53
+        z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+        out[s:s + c] = (sigma * z).astype(np.float32)
+    return out
+
+
+def ue8m0_codes(seed: int, tensor: int, n: int, lo: int = -4, hi: int = 4) -> np.ndarray:
+    """n UE8M0 codes (biased exponents) of 2**e, e uniform over {lo..hi}."""
+    span = np.uint64(hi - lo + 1)
+    out = np.empty(n, dtype=np.uint8)
+    for s in range(0, n, _CHUNK):
+        c = min(_CHUNK, n - s)
+        x = stream(seed, tensor, s, c) >> np.uint64(32)
+        e = ((x * span) >> np.uint64(32)).astype(np.int64) + lo
+        out[s:s + c] = (e + 127).astype(np.uint8)
+    return out
+
+
+# ---------------------------------------------------------------- rounding
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """RNE fp32 -> bf16 codes (finite inputs)."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (b >> np.uint32(16)) & np.uint32(1)
+    with np.errstate(over="ignore"):
+        r = (b + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """RNE fp32 -> IEEE binary16 codes."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """RNE fp32 -> OCP E4M3 codes, saturating finite values to +-448."""
+    x = np.ascontiguousarray(x, dtype=np.float32).astype(np.float64)
+    sign = (np.signbit(x)).astype(np.uint8) << np.uint8(7)
+    a = np.abs(x)
+    _, e2 = np.frexp(np.where(a > 0, a, 1.0))        # a = m * 2**e2, m in [0.5, 1)
+    ex = np.maximum(e2 - 1, -6)                        # unbiased exponent, subnormals share -6
+    q = np.ldexp(1.0, ex - 3)                          # spacing of the 3-bit mantissa grid
+    r = np.rint(a / q) * q                             # ties to even (a/q is exact)
+    r = np.minimum(r, 448.0)                           # satfinite
+    _, er = np.frexp(np.where(r > 0, r, 1.0))
+    er = er - 1
+    normal_ = r >= 2.0 ** -6
+    e_field = np.where(normal_, er + 7, 0)
+    m_field = np.where(normal_, r / np.ldexp(1.0, er - 3) - 8.0, r / 2.0 ** -9)
+    code = (e_field.astype(np.int64) << 3) | m_field.astype(np.int64)
+    code = np.where(r == 0, 0, code)
+    return (code.astype(np.uint8) | sign).astype(np.uint8)
+
+
+# ---------------------------------------------------------------- workloads
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    """One GEMM problem D = A·B + C and the recipe of its inputs.
+
+    A is M x K, row-major when ``a_row_major`` (else column-major); B is K x N,
+    column-major unless ``b_row_major`` (column-major K x N = N rows of K).
+    ``ab`` is "bf16", "f16" or "e4m3"; ``dist`` "uniform" or "normal" with
+    ``sigma``; ``c`` "zero" or "normal"; ``d`` "f32" or "bf16".
+    """
+    name: str
+    M: int
+    N: int
+    K: int
+    ab: str
+    dist: str
+    sigma: float
+    c: str
+    d: str
+    seed: int
+    block_scaled: bool = False
+    a_row_major: bool = True
+    b_row_major: bool = False
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def sfk(self) -> int:
+        return (self.K + 31) // 32
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("bf16_256x256x256_c0_f32out", 256, 256, 256, "bf16", "uniform", 1.0, "zero", "f32", 0),
+        Workload("bf16_4096x4096x4096_f32out", 4096, 4096, 4096, "bf16", "uniform", 1.0, "normal", "f32", 1),
+        Workload("f16_4000x3000x2056_f32out", 4000, 3000, 2056, "f16", "normal", 0.5, "normal", "f32", 2),
+        Workload("bf16_8192x8192x8192_bf16out", 8192, 8192, 8192, "bf16", "uniform", 1.0, "normal", "bf16", 3),
+        Workload("mxf8e4m3_8192x8192x8192_c0_f32out", 8192, 8192, 8192, "e4m3", "normal", 1.0, "zero", "f32", 4,
+                 block_scaled=True),
+    ]
+}
+
+HEADLINE = "bf16_8192x8192x8192_bf16out"
+
+
+def scaled(w: Workload, M: int, N: int, K: int, name: str | None = None, **kw) -> Workload:
+    """The same recipe at other sizes (parity cases the oracle finishes quickly)."""
+    return dataclasses.replace(w, name=name or f"{w.name}@{M}x{N}x{K}", M=M, N=N, K=K, **kw)
+
+
+def _operand(w: Workload, tensor: int, n: int) -> np.ndarray:
+    if w.dist == "uniform":
+        x = uniform_pm1(w.seed, tensor, n)
+    else:
+        x = normal(w.seed, tensor, n, w.sigma)
+    if w.ab == "bf16":
+        return f32_to_bf16_bits(x)
+    if w.ab == "f16":
+        return f32_to_f16_bits(x)
+    if w.ab == "e4m3":
+        return f32_to_e4m3_bits(np.clip(x, -448.0, 448.0))
+    raise ValueError(w.ab)
+
+
+def make_inputs(w: Workload) -> dict:
+    """Bit patterns of A, B, C (and SFA, SFB) for workload w.
+
+    Shapes follow the memory layout: A is (M, K) when row-major, else (K, M);
+    B is (N, K) when column-major, else (K, N); C is (M, N) fp32 row-major;
+    SFA is (M, ceil(K/32)) and SFB is (N, ceil(K/32)), both row-major u8.
+    """
+    M, N, K = w.M, w.N, w.K
+    A = _operand(w, T_A, M * K).reshape((M, K) if w.a_row_major else (K, M))
+    B = _operand(w, T_B, K * N).reshape((K, N) if w.b_row_major else (N, K))
+    if w.c == "zero":
+        C = np.zeros((M, N), dtype=np.float32)
+    else:
+        C = normal(w.seed, T_C, M * N, 1.0).reshape(M, N)
+    out = {"A": A, "B": B, "C": C}
+    if w.block_scaled:
+        out["SFA"] = ue8m0_codes(w.seed, T_SFA, M * w.sfk).reshape(M, w.sfk)
+        out["SFB"] = ue8m0_codes(w.seed, T_SFB, N * w.sfk).reshape(N, w.sfk)
+    return out

@@ -1,0 +1,156 @@
+"""CPU oracle for D = A·B + C — TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` import this package.  The CUDA library never links, loads or
+calls it, and it imports nothing from the CUDA package.
+
+``gemm`` / ``gemm_entries`` wrap the plain fp64 triple loop in
+``gemm_oracle.c`` (the definition D[i][j] = C[i][j] + sum_k a[i][k] b[k][j]
+from "Tensor Core 数据布局的演进", overview, with the block-scaling rule of its
+section "Block-Scaled MMA 的 Scale Factors").  ``layouts`` holds the pages'
+register-fragment and TMEM layout maps.
+
+Parity pins (tests/test_oracle_*.py): exhaustive format decodes against
+torch/numpy conversions and the OCP/IEEE tables; A = I, rank-1, all-ones and
+sign-alternating closed forms; brute force in exact integer arithmetic on
+small problems in every storage order; block scales against a per-block
+exact evaluation; the pages' printed fragment and TMEM examples.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gemm_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+DTYPES = {"f16": 0, "bf16": 1, "e4m3": 2}
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile gemm_oracle.c with gcc (OpenMP, no fp contraction)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+    os.close(fd)
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
+           "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        i64, vp, dp = ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p
+        L.oracle_gemm.argtypes = [i64, i64, i64, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
+                                  vp, vp, vp, ctypes.c_int, i64, i64, dp, dp, ctypes.c_int]
+        L.oracle_gemm.restype = ctypes.c_int
+        L.oracle_gemm_entries.argtypes = [i64, i64, i64, ctypes.c_int, vp, ctypes.c_int, vp, ctypes.c_int,
+                                          vp, vp, vp, ctypes.c_int, i64, vp, vp, dp, dp, ctypes.c_int]
+        L.oracle_gemm_entries.restype = ctypes.c_int
+        for name, arg in [("oracle_decode_bf16", ctypes.c_uint16), ("oracle_decode_f16", ctypes.c_uint16),
+                          ("oracle_decode_e4m3", ctypes.c_uint8), ("oracle_decode_ue8m0", ctypes.c_uint8)]:
+            f = getattr(L, name)
+            f.argtypes = [arg]
+            f.restype = ctypes.c_double
+        L.oracle_threads.argtypes = [ctypes.c_int]
+        L.oracle_threads.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def threads(nthreads: int = 0) -> int:
+    return lib().oracle_threads(nthreads)
+
+
+def decode(codes, dtype: str) -> np.ndarray:
+    """fp64 values of bf16 / f16 / e4m3 / ue8m0 codes (element by element)."""
+    f = getattr(lib(), "oracle_decode_" + dtype)
+    flat = np.asarray(codes).ravel()
+    return np.array([f(int(c)) for c in flat], dtype=np.float64).reshape(np.shape(codes))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _check_operands(A, B, C, SFA, SFB, M, N, K, dtype, block_scaled):
+    width = np.uint8 if dtype == "e4m3" else np.uint16
+    A = np.ascontiguousarray(A, dtype=width)
+    B = np.ascontiguousarray(B, dtype=width)
+    if A.size != M * K or B.size != K * N:
+        raise ValueError("operand sizes do not match M, N, K")
+    if C is not None:
+        C = np.ascontiguousarray(C, dtype=np.float32)
+        if C.size != M * N:
+            raise ValueError("C size does not match M, N")
+    sfk = (K + 31) // 32
+    if block_scaled:
+        SFA = np.ascontiguousarray(SFA, dtype=np.uint8)
+        SFB = np.ascontiguousarray(SFB, dtype=np.uint8)
+        if SFA.size != M * sfk or SFB.size != N * sfk:
+            raise ValueError("scale-factor sizes do not match M, N, ceil(K/32)")
+    else:
+        SFA = SFB = None
+    return A, B, C, SFA, SFB
+
+
+def gemm(A, B, C, M: int, N: int, K: int, dtype: str, a_row_major: bool = True,
+         b_row_major: bool = False, SFA=None, SFB=None, block_scaled: bool = False,
+         rows: tuple | None = None, nthreads: int = 0):
+    """(D, S) as fp64 arrays of shape (rows, N): D = C + sum_k a b, S = sum_k |a b|.
+
+    ``rows`` = (row0, row1) restricts the work to a row slab (default: all).
+    """
+    A, B, C, SFA, SFB = _check_operands(A, B, C, SFA, SFB, M, N, K, dtype, block_scaled)
+    r0, r1 = rows if rows is not None else (0, M)
+    D = np.empty((r1 - r0, N), dtype=np.float64)
+    S = np.empty((r1 - r0, N), dtype=np.float64)
+    rc = lib().oracle_gemm(M, N, K, DTYPES[dtype], _ptr(A), int(a_row_major), _ptr(B), int(b_row_major),
+                           _ptr(C), _ptr(SFA), _ptr(SFB), int(block_scaled), r0, r1,
+                           D.ctypes.data, S.ctypes.data, nthreads)
+    if rc != 0:
+        raise ValueError("oracle_gemm rejected its arguments")
+    return D, S
+
+
+def gemm_entries(A, B, C, M: int, N: int, K: int, dtype: str, rows, cols, a_row_major: bool = True,
+                 b_row_major: bool = False, SFA=None, SFB=None, block_scaled: bool = False,
+                 nthreads: int = 0):
+    """(D, S) at the listed (row, col) entries, each computed on its own."""
+    A, B, C, SFA, SFB = _check_operands(A, B, C, SFA, SFB, M, N, K, dtype, block_scaled)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    cols = np.ascontiguousarray(cols, dtype=np.int64)
+    n = rows.size
+    D = np.empty(n, dtype=np.float64)
+    S = np.empty(n, dtype=np.float64)
+    rc = lib().oracle_gemm_entries(M, N, K, DTYPES[dtype], _ptr(A), int(a_row_major), _ptr(B),
+                                   int(b_row_major), _ptr(C), _ptr(SFA), _ptr(SFB), int(block_scaled),
+                                   n, rows.ctypes.data, cols.ctypes.data, D.ctypes.data, S.ctypes.data,
+                                   nthreads)
+    if rc != 0:
+        raise ValueError("oracle_gemm_entries rejected its arguments")
+    return D, S
+
+
+def bf16_ulp(x) -> np.ndarray:
+    """Spacing of the bf16 grid (8 significant bits) at |x|: 2**(floor(log2|x|) - 7).
+
+    Below the smallest normal (2**-126) the spacing is the subnormal one, 2**-133.
+    """
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    _, e = np.frexp(a)                              # a = m * 2**e, m in [0.5, 1); e = 0 at 0
+    ex = np.where(a > 0, np.maximum(e - 1, -126), -126)
+    return np.ldexp(1.0, ex - 7)

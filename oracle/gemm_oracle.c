@@ -1,0 +1,205 @@
+/*
+ * CPU oracle for the tensor-core multiply-accumulate D = A·B + C.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do.  It shares no code, header or table with the CUDA library.
+ *
+ * What it computes (the plain definition, "Tensor Core 数据布局的演进",
+ * overview: the three tensor-core generations all compute D = AB + C):
+ *
+ *     D[i][j] = C[i][j] + sum_{k=0}^{K-1} a[i][k] * b[k][j]
+ *     S[i][j] =           sum_{k=0}^{K-1} |a[i][k] * b[k][j]|
+ *
+ * in fp64 over the already rounded operands.  bf16, fp16 and e4m3 values are
+ * exact in fp64, and so are their products, so the only rounding is the
+ * fp64 summation (error far below any tolerance applied to the result).
+ *
+ * Block scaling ("Tensor Core 数据布局的演进", section "Block-Scaled MMA 的
+ * Scale Factors"): SFA[m][sfk] scales the elements of row m of A inside the
+ * sfk-th K block, SFB[n][sfk] the elements of column n of B.  The K block is
+ * 32 elements (one UE8M0 scale per 32 contiguous K elements), so
+ *     a[i][k] = e4m3(A[i][k]) * 2^(SFA[i][k/32] - 127)
+ *     b[k][j] = e4m3(B[k][j]) * 2^(SFB[j][k/32] - 127)
+ * SFA is stored M x ceil(K/32) row-major, SFB N x ceil(K/32) row-major.
+ *
+ * Operand storage: A is M x K, row-major (A[i*K+k]) when a_row_major, else
+ * column-major (A[k*M+i]).  B is K x N, row-major (B[k*N+j]) when b_row_major,
+ * else column-major (B[j*K+k]).  C is M x N fp32 row-major, or NULL for 0.
+ *
+ * Operand formats, decoded from their definitions:
+ *   bf16  the upper 16 bits of an IEEE-754 binary32 pattern;
+ *   fp16  IEEE-754 binary16 (1/5/10, bias 15, subnormals, inf/NaN at 31);
+ *   e4m3  OCP 8-bit floating point E4M3 (1/4/3, bias 7, subnormals,
+ *         no infinities, S.1111.111 is NaN, max normal 448);
+ *   ue8m0 OCP microscaling scale: 2^(code-127), code 255 is NaN.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 2 };
+
+double oracle_decode_bf16(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+double oracle_decode_f16(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int m = h & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);                 /* subnormal: m * 2^-14 * 2^-10 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);     /* (1 + m/2^10) * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+double oracle_decode_e4m3(uint8_t c) {
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int m = c & 0x7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)m, -9);                  /* m/8 * 2^(1-7) */
+    else
+        v = ldexp((double)(8 + m), e - 10);        /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+double oracle_decode_ue8m0(uint8_t c) {
+    return c == 255 ? NAN : ldexp(1.0, (int)c - 127);
+}
+
+static double decode(int dtype, const void *p, int64_t idx) {
+    switch (dtype) {
+    case ORACLE_F16: return oracle_decode_f16(((const uint16_t *)p)[idx]);
+    case ORACLE_BF16: return oracle_decode_bf16(((const uint16_t *)p)[idx]);
+    default: return oracle_decode_e4m3(((const uint8_t *)p)[idx]);
+    }
+}
+
+typedef struct {
+    int64_t M, N, K, sfk;
+    int dtype, a_row_major, b_row_major, block_scaled;
+    const void *A, *B;
+    const uint8_t *SFA, *SFB;
+} problem;
+
+/* a[i][k] with its block scale applied */
+static double a_elem(const problem *p, int64_t i, int64_t k) {
+    int64_t idx = p->a_row_major ? i * p->K + k : k * p->M + i;
+    double v = decode(p->dtype, p->A, idx);
+    if (p->block_scaled) v *= oracle_decode_ue8m0(p->SFA[i * p->sfk + k / 32]);
+    return v;
+}
+
+/* b[k][j] with its block scale applied */
+static double b_elem(const problem *p, int64_t k, int64_t j) {
+    int64_t idx = p->b_row_major ? k * p->N + j : j * p->K + k;
+    double v = decode(p->dtype, p->B, idx);
+    if (p->block_scaled) v *= oracle_decode_ue8m0(p->SFB[j * p->sfk + k / 32]);
+    return v;
+}
+
+static int set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) return nthreads;
+    return omp_get_max_threads();
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}
+
+/* Number of threads an oracle call with this request would use. */
+int oracle_threads(int nthreads) { return set_threads(nthreads); }
+
+/*
+ * Rows [row0, row1) of the product (pass 0, M for all of it): D and S are
+ * (row1 - row0) x N fp64 row-major outputs, row r holding row row0 + r.
+ * Returns 0, or -1 on a bad argument or allocation failure.
+ */
+int oracle_gemm(int64_t M, int64_t N, int64_t K, int dtype,
+                const void *A, int a_row_major, const void *B, int b_row_major,
+                const float *C, const uint8_t *SFA, const uint8_t *SFB, int block_scaled,
+                int64_t row0, int64_t row1, double *D, double *S, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || row0 < 0 || row1 > M || row0 > row1) return -1;
+    if (block_scaled && (dtype != ORACLE_E4M3 || !SFA || !SFB)) return -1;
+    problem p = {M, N, K, (K + 31) / 32, dtype, a_row_major, b_row_major, block_scaled, A, B, SFA, SFB};
+    int64_t rows = row1 - row0;
+    /* decode the operands once into plain fp64 matrices: ad (rows x K), bd (K x N) */
+    double *ad = (double *)malloc(sizeof(double) * (size_t)(rows * K > 0 ? rows * K : 1));
+    double *bd = (double *)malloc(sizeof(double) * (size_t)(K * N > 0 ? K * N : 1));
+    if (!ad || !bd) { free(ad); free(bd); return -1; }
+    int nt = set_threads(nthreads);
+    #pragma omp parallel for num_threads(nt) schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t k = 0; k < K; ++k) ad[r * K + k] = a_elem(&p, row0 + r, k);
+    #pragma omp parallel for num_threads(nt) schedule(static)
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t j = 0; j < N; ++j) bd[k * N + j] = b_elem(&p, k, j);
+
+    #pragma omp parallel for num_threads(nt) schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t i = row0 + r;
+        double *d = D + r * N, *s = S + r * N;
+        for (int64_t j = 0; j < N; ++j) { d[j] = 0.0; s[j] = 0.0; }
+        for (int64_t k = 0; k < K; ++k) {
+            double a = ad[r * K + k];
+            const double *b = bd + k * N;
+            for (int64_t j = 0; j < N; ++j) {
+                double prod = a * b[j];
+                d[j] += prod;
+                s[j] += fabs(prod);
+            }
+        }
+        for (int64_t j = 0; j < N; ++j) d[j] += C ? (double)C[i * N + j] : 0.0;
+    }
+    free(ad);
+    free(bd);
+    return 0;
+}
+
+/*
+ * Selected entries: for each (rows[e], cols[e]) the same sums as oracle_gemm,
+ * evaluated one entry at a time straight from the operand codes.
+ */
+int oracle_gemm_entries(int64_t M, int64_t N, int64_t K, int dtype,
+                        const void *A, int a_row_major, const void *B, int b_row_major,
+                        const float *C, const uint8_t *SFA, const uint8_t *SFB, int block_scaled,
+                        int64_t n, const int64_t *rows, const int64_t *cols,
+                        double *D, double *S, int nthreads) {
+    if (M < 0 || N < 0 || K < 0 || n < 0) return -1;
+    if (block_scaled && (dtype != ORACLE_E4M3 || !SFA || !SFB)) return -1;
+    for (int64_t e = 0; e < n; ++e)
+        if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;
+    problem p = {M, N, K, (K + 31) / 32, dtype, a_row_major, b_row_major, block_scaled, A, B, SFA, SFB};
+    int nt = set_threads(nthreads);
+    #pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
+    for (int64_t e = 0; e < n; ++e) {
+        int64_t i = rows[e], j = cols[e];
+        double d = 0.0, s = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double prod = a_elem(&p, i, k) * b_elem(&p, k, j);
+            d += prod;
+            s += fabs(prod);
+        }
+        D[e] = d + (C ? (double)C[i * N + j] : 0.0);
+        S[e] = s;
+    }
+    return 0;
+}
