@@ -1,0 +1,375 @@
+"""Benchmark of the tensor-core GEMM D = A·B + C on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one D = A·B + C over the workload's synthetic inputs (default: bf16
+8192^3, C ~ N(0,1) fp32, D bf16).  ``value`` is TFLOP/s (2*M*N*K per step)
+over K back-to-back steps with the inputs resident in HBM, timed with CUDA
+events between a barrier + synchronize on both sides (max over ranks).  The
+inputs (A+B+C = 512 MiB at the default size) are larger than L2, so no L2
+flush runs between steps.  ``e2e`` times the same product through the C ABI
+with host buffers (gemm_run_host: H2D of A, B, C, the kernel, D2H of D).
+
+With N > 1 (launched by torch.distributed.run) every rank runs its own
+replica of the workload on its own GPU: the GEMM has no exchange step, so
+there is no collective on the data path (weak scaling).
+
+``--impl reference`` times the CPU oracle instead (rank 0 only), on bounded
+samples of the same workload; it is the deliberately slow fp64 definition,
+not a competing GPU implementation.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# dense tensor-core rate of e4m3 relative to bf16 (nominal 4.5 vs 2.25 PFLOP/s)
+FP8_OVER_BF16 = 2.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def aggregate(local_ms: float, units_per_rank: float, world: int, group=None):
+    """Whole-job throughput: all ranks' units over the slowest rank's time.
+
+    Returns (max_ms, total units / max seconds).  With world > 1 the max is an
+    all-reduce over the default process group (or ``group``).
+    """
+    max_ms = local_ms
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([local_ms], dtype=torch.float64)
+        if dist.get_backend(group) == "nccl":
+            t = t.cuda()
+        dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+        max_ms = float(t.item())
+    return max_ms, units_per_rank * world / (max_ms / 1e3)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.gpu, self.period, self.proc, self.lines = gpu_index, period_ms, None, []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(self.period), "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._t:
+                self._t.join(timeout=5)
+
+    def summary(self):
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxes.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+# --------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    from blackwell_tensor_core_tma_gb300 import gemm, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w)
+
+    def dev_tensor(a):
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    A, B, C = dev_tensor(x["A"]), dev_tensor(x["B"]), dev_tensor(x["C"])
+    SFA = dev_tensor(x["SFA"]) if w.block_scaled else None
+    SFB = dev_tensor(x["SFB"]) if w.block_scaled else None
+    d_t = torch.bfloat16 if w.d == "bf16" else torch.float32
+    D = torch.empty((w.M, w.N), dtype=d_t, device=dev)
+    plan = gemm.Plan(w.M, w.N, w.K, w.ab, w.d, w.block_scaled)
+    info = plan.info
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        plan.run(A, B, C, D, SFA, SFB, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    if plan.last_status() != gemm.GEMM_OK:
+        raise RuntimeError("kernel reported a timeout during warm-up")
+
+    # per-launch events on the launching stream give the kernel's duration
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    if plan.last_status() != gemm.GEMM_OK:
+        raise RuntimeError("kernel reported a timeout in the timed region")
+    local_ms = t0.elapsed_time(t1) / args.steps
+    kernel_ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
+    max_ms, flops_per_s = aggregate(local_ms, w.flops, world)
+    value = flops_per_s / 1e12
+
+    # end to end through the C ABI with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hA = torch.from_numpy(x["A"].view(np.int16) if x["A"].dtype == np.uint16 else x["A"]).pin_memory()
+        hB = torch.from_numpy(x["B"].view(np.int16) if x["B"].dtype == np.uint16 else x["B"]).pin_memory()
+        hC = torch.from_numpy(x["C"]).pin_memory()
+        hSFA = torch.from_numpy(x["SFA"]).pin_memory() if w.block_scaled else None
+        hSFB = torch.from_numpy(x["SFB"]).pin_memory() if w.block_scaled else None
+        hD = torch.empty((w.M, w.N), dtype=d_t).pin_memory()
+        e_steps = max(3, min(args.steps, args.e2e_steps))
+        for _ in range(2):
+            plan.run_host(hA, hB, hC, hD, hSFA, hSFB, stream)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            plan.run_host(hA, hB, hC, hD, hSFA, hSFB, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        _, e2e_flops = aggregate(e0.elapsed_time(e1) / e_steps, w.flops, world)
+        h2d = x["A"].nbytes + x["B"].nbytes + x["C"].nbytes + \
+            (x["SFA"].nbytes + x["SFB"].nbytes if w.block_scaled else 0)
+        e2e = {"value": round(e2e_flops / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(hD.numel() * hD.element_size()), "steps": e_steps}
+
+    peaks, source = load_peaks()
+    peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if w.ab == "e4m3" else 1.0)
+    achieved = w.flops / (kernel_ms / 1e3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": args.traffic,
+                "peak_source": f"{source} bf16 burst (cuBLAS bf16 8192^3)" +
+                               (" x2 nominal fp8/bf16" if w.ab == "e4m3" else ""),
+                "frac_of_sustained": round(achieved / (peaks.get("bf16_tflops_sustained", peak) *
+                                                      (FP8_OVER_BF16 if w.ab == "e4m3" else 1.0)), 4),
+                "kernel": "gemm_f16_kernel" if w.ab != "e4m3" else "gemm_mxf8_kernel",
+                "kernel_ms": round(kernel_ms, 5)}
+
+    out = {
+        "metric": "GEMM TFLOP/s and % of GB300 dense tensor peak (bf16 8192^3), vs CPU oracle",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(max_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.ab == "bf16" else w.ab,
+        "data": "synthetic (seeded splitmix64; recipe of the workload)",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "ab": w.ab, "c": "fp32",
+                   "d": w.d, "cta_group": info["cta_group"], "tile": [info["tile_m"], info["tile_n"],
+                                                                      info["tile_k"]],
+                   "stages": info["stages"], "grid": info["grid"], "replicas": world,
+                   "l2": "no flush: inputs (A+B+C) larger than the 129 MB L2"},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": args.steps * info["launches_per_run"],
+        "clocks": clocks.summary(),
+    }
+    plan.close()
+    if rank == 0 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(w, x, args.cpu_seconds)
+    return out
+
+
+def cpu_baseline(w, x, seconds: float):
+    """The oracle's triple loop on a row slab of the same workload (bounded CPU time)."""
+    import oracle
+    t = time.perf_counter()
+    oracle.gemm(x["A"], x["B"], x["C"], w.M, w.N, w.K, w.ab, SFA=x.get("SFA"), SFB=x.get("SFB"),
+                block_scaled=w.block_scaled, rows=(0, 1))
+    one = time.perf_counter() - t                    # includes decoding all of B once
+    rows = 2
+    t = time.perf_counter()
+    oracle.gemm(x["A"], x["B"], x["C"], w.M, w.N, w.K, w.ab, SFA=x.get("SFA"), SFB=x.get("SFB"),
+                block_scaled=w.block_scaled, rows=(0, rows))
+    two = time.perf_counter() - t
+    per_row = max((two - one) / (rows - 1), 1e-6)
+    fixed = max(one - per_row, 0.0)
+    R = int(max(1, min(w.M, (seconds - fixed) / per_row)))
+    t = time.perf_counter()
+    oracle.gemm(x["A"], x["B"], x["C"], w.M, w.N, w.K, w.ab, SFA=x.get("SFA"), SFB=x.get("SFB"),
+                block_scaled=w.block_scaled, rows=(0, R))
+    dt = time.perf_counter() - t
+    return {"value": round(2.0 * R * w.N * w.K / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"rows 0..{R - 1} of {w.name} (all N and K, fp64 triple loop incl. operand decode), "
+                      f"{dt:.1f} s"}
+
+
+# --------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    import numpy as np
+
+    import oracle
+    from blackwell_tensor_core_tma_gb300 import synth
+
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w)
+    rng = np.random.default_rng(0)
+    total_budget = args.reference_seconds
+    per_step = total_budget / (args.steps + args.warmup)
+
+    def sample(n):
+        r = rng.integers(0, w.M, n)
+        c = rng.integers(0, w.N, n)
+        t = time.perf_counter()
+        oracle.gemm_entries(x["A"], x["B"], x["C"], w.M, w.N, w.K, w.ab, r, c, SFA=x.get("SFA"),
+                            SFB=x.get("SFB"), block_scaled=w.block_scaled)
+        return time.perf_counter() - t
+
+    probe = 256
+    rate = probe / max(sample(probe), 1e-6)          # entries per second
+    n = int(max(16, rate * per_step))
+    for _ in range(args.warmup):
+        sample(n)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        sample(n)
+    dt = (time.perf_counter() - t) / args.steps
+    flops = 2.0 * n * w.K
+    value = flops / dt / 1e12
+    desc = f"{n} random entries of {w.name} per step (each a fp64 sum over K = {w.K})"
+    return {
+        "impl": "reference",
+        "metric": "GEMM TFLOP/s and % of GB300 dense tensor peak (bf16 8192^3), vs CPU oracle",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded splitmix64)",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "ab": w.ab, "d": w.d},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    from blackwell_tensor_core_tma_gb300 import synth
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-seconds", type=float, default=120.0)
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        out = run_ours(args, rank, world, local_rank)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

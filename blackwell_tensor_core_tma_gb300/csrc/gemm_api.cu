@@ -1,0 +1,325 @@
+// C ABI of the GEMM library (include/gb300gemm.h): plan validation, kernel
+// choice, tensor-map encoding and launch.
+//
+// Tensor maps ("(二) CUTLASS —— 掌握 Tensor Memory Accelerator（TMA）", host
+// code: a copy descriptor built on the host from the global tensor and the
+// shared-memory tile, passed to the kernel as a __grid_constant__ parameter)
+// are encoded with the driver's cuTensorMapEncodeTiled, fetched through the
+// runtime's entry-point query so that the library does not link libcuda.
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include <cudaTypedefs.h>
+
+#include "gemm_internal.h"
+#include "ptx.cuh"
+
+using namespace gb300;
+
+struct gemm_plan {
+    int64_t M, N, K;
+    gemm_dtype ab, c, d;
+    int block_scaled;
+    unsigned flags;
+    int device;
+    int sm_count;
+    int cta_group;
+    int stages;
+    int tiles_m, tiles_n, tiles;
+    int grid;
+    int smem;
+    int group_m;
+    uint64_t timeout_ns;
+    int fault;
+    int *status;              // device word
+    // device buffers of gemm_run_host (allocated on first use)
+    void *hA, *hB, *hC, *hD;
+    uint8_t *hSFA, *hSFB;
+    // tensor maps of the last run, reused while the pointers repeat
+    const void *lastA, *lastB, *lastC, *lastD;
+    CUtensorMap maps[4];
+    bool maps_valid;
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+int elem_bytes(gemm_dtype t) { return t == GEMM_E4M3 ? 1 : (t == GEMM_F32 ? 4 : 2); }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D row-major tensor [outer][inner] with a box of box_outer x box_inner elements
+bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, int ebytes, const void *ptr, uint64_t inner, uint64_t outer,
+               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * (uint64_t)ebytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+CUtensorMapDataType tma_dtype(gemm_dtype t) {
+    switch (t) {
+    case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    case GEMM_F32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    }
+}
+
+gemm_status encode_maps(gemm_plan *p, const void *A, const void *B, const void *C, void *D) {
+    if (p->maps_valid && A == p->lastA && B == p->lastB && C == p->lastC && D == p->lastD) return GEMM_OK;
+    if (!encoder()) return GEMM_ERR_CUDA;
+    std::memset(p->maps, 0, sizeof p->maps);
+    const int eb = elem_bytes(p->ab);
+    const uint32_t bk = 128u / (uint32_t)eb;                       // K elements in a 128-byte row
+    const uint32_t b_rows = (uint32_t)(TILE_N / p->cta_group);
+    bool ok = encode_2d(&p->maps[0], tma_dtype(p->ab), eb, A, p->K, p->M, bk, TILE_M, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode_2d(&p->maps[1], tma_dtype(p->ab), eb, B, p->K, p->N, bk, b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (ok && C)
+        ok = encode_2d(&p->maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, p->N, p->M, EPI_COLS, 32,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+    if (ok) {
+        if (p->d == GEMM_BF16)
+            ok = encode_2d(&p->maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, p->N, p->M, EPI_COLS, 32,
+                           CU_TENSOR_MAP_SWIZZLE_64B);
+        else
+            ok = encode_2d(&p->maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, p->N, p->M, EPI_COLS, 32,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    if (!ok) {
+        p->maps_valid = false;
+        return GEMM_ERR_CUDA;
+    }
+    p->lastA = A;
+    p->lastB = B;
+    p->lastC = C;
+    p->lastD = D;
+    p->maps_valid = true;
+    return GEMM_OK;
+}
+
+gemm_status configure_f16(gemm_plan *p) {
+    const bool pair_fits = p->M >= 2 * TILE_M;
+    int cg = (p->M >= 1024 && p->N >= 1024) ? 2 : 1;
+    if (p->flags & GEMM_FLAG_FORCE_1CTA) cg = 1;
+    if (p->flags & GEMM_FLAG_FORCE_2CTA) cg = 2;
+    (void)pair_fits;
+    F16Config cfg{cg, p->d == GEMM_BF16};
+    if (f16_prepare(cfg) != cudaSuccess) return GEMM_ERR_CUDA;
+    p->cta_group = cg;
+    p->stages = f16_stages(cg);
+    p->smem = f16_smem_bytes(cg);
+    p->tiles_m = (int)((p->M + TILE_M * cg - 1) / (TILE_M * cg));
+    p->tiles_n = (int)((p->N + TILE_N - 1) / TILE_N);
+    p->tiles = p->tiles_m * p->tiles_n;
+    int units = p->sm_count / cg;
+    if (cg == 2) {
+        int clusters = 0;
+        if (f16_max_active_clusters(cfg, &clusters) == cudaSuccess && clusters > 0) units = clusters;
+    }
+    p->grid = cg * (p->tiles < units ? p->tiles : units);
+    p->group_m = cg == 2 ? 8 : 16;
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gemm_status_string(gemm_status s) {
+    switch (s) {
+    case GEMM_OK: return "ok";
+    case GEMM_ERR_INVALID_ARG: return "invalid argument";
+    case GEMM_ERR_UNSUPPORTED: return "unsupported dtype, layout or device";
+    case GEMM_ERR_ALIGNMENT: return "pointer or row stride not a multiple of 16 bytes";
+    case GEMM_ERR_CUDA: return "CUDA call failed";
+    case GEMM_ERR_TIMEOUT: return "a bounded wait inside the kernel ran out";
+    default: return "unknown status";
+    }
+}
+
+gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K, gemm_dtype ab, gemm_dtype c,
+                             gemm_dtype d, int a_row_major, int b_row_major, int block_scaled, unsigned flags) {
+    if (!out || M <= 0 || N <= 0 || K <= 0) return GEMM_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_ARG;
+    if ((unsigned)ab > GEMM_F32 || (unsigned)c > GEMM_F32 || (unsigned)d > GEMM_F32) return GEMM_ERR_INVALID_ARG;
+    if ((flags & GEMM_FLAG_FORCE_1CTA) && (flags & GEMM_FLAG_FORCE_2CTA)) return GEMM_ERR_INVALID_ARG;
+    if (c != GEMM_F32 || (d != GEMM_F32 && d != GEMM_BF16)) return GEMM_ERR_UNSUPPORTED;
+    if (block_scaled ? ab != GEMM_E4M3 : (ab != GEMM_F16 && ab != GEMM_BF16)) return GEMM_ERR_UNSUPPORTED;
+    if (!a_row_major || b_row_major) return GEMM_ERR_UNSUPPORTED;
+    if (block_scaled) return GEMM_ERR_UNSUPPORTED;
+    // 16-byte row strides (the copy engine's stride rule)
+    if ((K * elem_bytes(ab)) % 16 != 0 || (N * 4) % 16 != 0 || (N * elem_bytes(d)) % 16 != 0)
+        return GEMM_ERR_ALIGNMENT;
+
+    int dev = 0;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return GEMM_ERR_UNSUPPORTED;
+
+    gemm_plan *p = new (std::nothrow) gemm_plan();
+    if (!p) return GEMM_ERR_CUDA;
+    p->M = M;
+    p->N = N;
+    p->K = K;
+    p->ab = ab;
+    p->c = c;
+    p->d = d;
+    p->block_scaled = block_scaled;
+    p->flags = flags;
+    p->device = dev;
+    p->sm_count = prop.multiProcessorCount;
+    p->timeout_ns = 1000000000ull;
+    gemm_status st = configure_f16(p);
+    if (st != GEMM_OK) {
+        delete p;
+        return st;
+    }
+    if (cudaMalloc(&p->status, sizeof(int)) != cudaSuccess) {
+        delete p;
+        return GEMM_ERR_CUDA;
+    }
+    if (cudaMemset(p->status, 0, sizeof(int)) != cudaSuccess) {
+        cudaFree(p->status);
+        delete p;
+        return GEMM_ERR_CUDA;
+    }
+    *out = p;
+    return GEMM_OK;
+}
+
+gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C, void *D, const uint8_t *SFA,
+                     const uint8_t *SFB, void *cuda_stream) {
+    (void)SFA;
+    (void)SFB;
+    if (!p || !A || !B || !D) return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (C && !aligned16(C))) return GEMM_ERR_ALIGNMENT;
+    gemm_status st = encode_maps(p, A, B, C, D);
+    if (st != GEMM_OK) return st;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
+    KParams kp{};
+    kp.M = (int)p->M;
+    kp.N = (int)p->N;
+    kp.K = (int)p->K;
+    kp.tiles_m = p->tiles_m;
+    kp.tiles_n = p->tiles_n;
+    kp.num_tiles = p->tiles;
+    kp.num_kb = (int)((p->K + TILE_K16 - 1) / TILE_K16);
+    kp.group_m = p->group_m;
+    kp.has_c = C != nullptr;
+    kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * p->cta_group), (uint32_t)TILE_N);
+    kp.status = p->status;
+    kp.timeout_ns = p->timeout_ns;
+    kp.fault = p->fault;
+    F16Config cfg{p->cta_group, p->d == GEMM_BF16};
+    LaunchShape shape{p->grid, p->cta_group, p->smem};
+    if (f16_launch(cfg, shape, p->maps, kp, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (p->flags & GEMM_FLAG_SYNC) {
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
+        return gemm_plan_last_status(p);
+    }
+    return GEMM_OK;
+}
+
+gemm_status gemm_run_host(gemm_plan_t p, const void *A, const void *B, const void *C, void *D, const uint8_t *SFA,
+                          const uint8_t *SFB, void *cuda_stream) {
+    if (!p || !A || !B || !D) return GEMM_ERR_INVALID_ARG;
+    const size_t a_bytes = (size_t)p->M * p->K * elem_bytes(p->ab);
+    const size_t b_bytes = (size_t)p->K * p->N * elem_bytes(p->ab);
+    const size_t c_bytes = (size_t)p->M * p->N * 4;
+    const size_t d_bytes = (size_t)p->M * p->N * elem_bytes(p->d);
+    if (!p->hA) {
+        if (cudaMalloc(&p->hA, a_bytes) != cudaSuccess || cudaMalloc(&p->hB, b_bytes) != cudaSuccess ||
+            cudaMalloc(&p->hC, c_bytes) != cudaSuccess || cudaMalloc(&p->hD, d_bytes) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
+    if (cudaMemcpyAsync(p->hA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(p->hB, B, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (C && cudaMemcpyAsync(p->hC, C, c_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    (void)SFA;
+    (void)SFB;
+    const unsigned saved = p->flags;
+    p->flags &= ~GEMM_FLAG_SYNC;
+    gemm_status st = gemm_run(p, p->hA, p->hB, C ? p->hC : nullptr, p->hD, nullptr, nullptr, cuda_stream);
+    p->flags = saved;
+    if (st != GEMM_OK) return st;
+    if (cudaMemcpyAsync(D, p->hD, d_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    return gemm_plan_last_status(p);
+}
+
+gemm_status gemm_plan_last_status(gemm_plan_t p) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return GEMM_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, p->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (v != 0 && cudaMemset(p->status, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+    return (gemm_status)v;
+}
+
+gemm_status gemm_plan_get_info(gemm_plan_t p, gemm_plan_info *info) {
+    if (!p || !info) return GEMM_ERR_INVALID_ARG;
+    info->cta_group = p->cta_group;
+    info->tile_m = TILE_M * p->cta_group;
+    info->tile_n = TILE_N;
+    info->tile_k = 128 / elem_bytes(p->ab);
+    info->stages = p->stages;
+    info->grid = p->grid;
+    info->tiles = p->tiles;
+    info->smem_bytes = p->smem;
+    info->launches_per_run = 1;
+    info->sm_count = p->sm_count;
+    return GEMM_OK;
+}
+
+gemm_status gemm_plan_set_timeout(gemm_plan_t p, uint64_t ns) {
+    if (!p || ns == 0) return GEMM_ERR_INVALID_ARG;
+    p->timeout_ns = ns;
+    return GEMM_OK;
+}
+
+gemm_status gemm_plan_destroy(gemm_plan_t p) {
+    if (!p) return GEMM_OK;
+    cudaFree(p->status);
+    cudaFree(p->hA);
+    cudaFree(p->hB);
+    cudaFree(p->hC);
+    cudaFree(p->hD);
+    cudaFree(p->hSFA);
+    cudaFree(p->hSFB);
+    delete p;
+    return GEMM_OK;
+}
+
+// Test hook (declared in include/gb300gemm_testing.h): make the next runs'
+// producer withhold one arrival so that a bounded wait runs out.
+gemm_status gemm_testing_set_fault(gemm_plan_t p, int fault) {
+    if (!p || fault < 0 || fault > 1) return GEMM_ERR_INVALID_ARG;
+    p->fault = fault;
+    return GEMM_OK;
+}
+
+}  // extern "C"

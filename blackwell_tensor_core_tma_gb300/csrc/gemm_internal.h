@@ -1,0 +1,51 @@
+// Host/device shared declarations of the GEMM library (not part of the C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/gb300gemm.h"
+
+namespace gb300 {
+
+// Kernel parameters common to every GEMM kernel (passed by value).
+struct KParams {
+    int M, N, K;
+    int tiles_m, tiles_n, num_tiles;
+    int num_kb;          // K blocks (pipeline stages consumed per tile)
+    int group_m;         // tile rasterisation: M tiles per group
+    int has_c;
+    uint32_t idesc;      // tcgen05 instruction descriptor
+    int *status;         // device status word (sticky error code)
+    uint64_t timeout_ns; // limit of every wait
+    int fault;           // test hook: 1 = producer withholds its first arrival
+    const uint8_t *sfa;  // block-scaled: packed scale factors (device)
+    const uint8_t *sfb;
+};
+
+// A launch: grid, cluster width and dynamic shared memory.
+struct LaunchShape {
+    int grid;
+    int cluster;
+    int smem;
+};
+
+// bf16/fp16 kernel family (gemm_f16.cu)
+struct F16Config {
+    int cta_group;   // 1 or 2
+    int out_bf16;    // D is bf16 (else fp32)
+};
+int f16_stages(int cta_group);
+int f16_smem_bytes(int cta_group);
+cudaError_t f16_prepare(const F16Config &cfg);   // set the kernel's shared-memory limit
+cudaError_t f16_max_active_clusters(const F16Config &cfg, int *clusters);
+cudaError_t f16_launch(const F16Config &cfg, const LaunchShape &shape, const CUtensorMap *maps,
+                       const KParams &p, cudaStream_t stream);
+
+constexpr int TILE_M = 128;   // rows of D per CTA
+constexpr int TILE_N = 256;   // columns of D per CTA (and per CTA pair)
+constexpr int TILE_K16 = 64;  // 16-bit K elements per stage (one 128-byte swizzle row)
+constexpr int EPI_COLS = 32;  // epilogue chunk width (columns)
+
+}  // namespace gb300

@@ -1,0 +1,187 @@
+"""ctypes binding of libgb300gemm.so (include/gb300gemm.h), same entry-point names.
+
+Argument marshalling only: every step of D = A·B + C runs in the CUDA
+library.  Pointers may be passed as ints or as torch tensors (their
+``data_ptr()``); streams as ints or torch streams (their ``cuda_stream``).
+There is no fallback: if the library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ALIGNMENT, GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT = range(6)
+GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_F32 = range(4)
+GEMM_FLAG_SYNC, GEMM_FLAG_FORCE_1CTA, GEMM_FLAG_FORCE_2CTA = 0x1, 0x2, 0x4
+
+DTYPE = {"f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM_E4M3, "f32": GEMM_F32}
+
+# every symbol include/gb300gemm.h and include/gb300gemm_testing.h declare
+EXPORTS = ["gemm_plan_create", "gemm_run", "gemm_run_host", "gemm_plan_last_status", "gemm_plan_get_info",
+           "gemm_plan_set_timeout", "gemm_plan_destroy", "gemm_status_string", "gemm_testing_set_fault"]
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gemm_status_string(status)} (status {status})")
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "grid", "tiles",
+                                            "smem_bytes", "launches_per_run", "sm_count")]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"{_build.LIB} is missing: build it first (python -m "
+                               "blackwell_tensor_core_tma_gb300.build); there is no CPU path")
+        L = ctypes.CDLL(_build.LIB)
+        vp, i64, st = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.gemm_plan_create.argtypes = [ctypes.POINTER(vp), i64, i64, i64, st, st, st, st, st, st, ctypes.c_uint]
+        L.gemm_plan_create.restype = st
+        for name in ("gemm_run", "gemm_run_host"):
+            f = getattr(L, name)
+            f.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+            f.restype = st
+        L.gemm_plan_last_status.argtypes = [vp]
+        L.gemm_plan_last_status.restype = st
+        L.gemm_plan_get_info.argtypes = [vp, ctypes.POINTER(PlanInfo)]
+        L.gemm_plan_get_info.restype = st
+        L.gemm_plan_set_timeout.argtypes = [vp, ctypes.c_uint64]
+        L.gemm_plan_set_timeout.restype = st
+        L.gemm_plan_destroy.argtypes = [vp]
+        L.gemm_plan_destroy.restype = st
+        L.gemm_status_string.argtypes = [st]
+        L.gemm_status_string.restype = ctypes.c_char_p
+        L.gemm_testing_set_fault.argtypes = [vp, st]
+        L.gemm_testing_set_fault.restype = st
+        _lib = L
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):                       # numpy array (host buffers)
+        return x.ctypes.data
+    raise TypeError(f"cannot pass {type(x)} as a pointer")
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, where: str):
+    if status != GEMM_OK:
+        raise GemmError(status, where)
+
+
+def gemm_status_string(status: int) -> str:
+    return lib().gemm_status_string(status).decode()
+
+
+def gemm_plan_create(M: int, N: int, K: int, ab="bf16", c="f32", d="f32", a_row_major: int = 1,
+                     b_row_major: int = 0, block_scaled: int = 0, flags: int = 0) -> int:
+    out = ctypes.c_void_p()
+    st = lib().gemm_plan_create(ctypes.byref(out), M, N, K, DTYPE.get(ab, ab), DTYPE.get(c, c), DTYPE.get(d, d),
+                                int(a_row_major), int(b_row_major), int(block_scaled), flags)
+    _check(st, "gemm_plan_create")
+    return out.value
+
+
+def gemm_run(plan: int, A, B, C, D, SFA=None, SFB=None, stream=None) -> int:
+    st = lib().gemm_run(plan, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(SFA), _ptr(SFB), _stream(stream))
+    _check(st, "gemm_run")
+    return st
+
+
+def gemm_run_host(plan: int, A, B, C, D, SFA=None, SFB=None, stream=None) -> int:
+    st = lib().gemm_run_host(plan, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(SFA), _ptr(SFB), _stream(stream))
+    _check(st, "gemm_run_host")
+    return st
+
+
+def gemm_plan_last_status(plan: int) -> int:
+    return lib().gemm_plan_last_status(plan)
+
+
+def gemm_plan_get_info(plan: int) -> dict:
+    info = PlanInfo()
+    _check(lib().gemm_plan_get_info(plan, ctypes.byref(info)), "gemm_plan_get_info")
+    return {n: getattr(info, n) for n, _ in PlanInfo._fields_}
+
+
+def gemm_plan_set_timeout(plan: int, ns: int):
+    _check(lib().gemm_plan_set_timeout(plan, ns), "gemm_plan_set_timeout")
+
+
+def gemm_plan_destroy(plan: int):
+    _check(lib().gemm_plan_destroy(plan), "gemm_plan_destroy")
+
+
+def gemm_testing_set_fault(plan: int, fault: int):
+    _check(lib().gemm_testing_set_fault(plan, fault), "gemm_testing_set_fault")
+
+
+class Plan:
+    """Owning wrapper of a gemm_plan_t (destroyed on close / context exit)."""
+
+    def __init__(self, M, N, K, ab="bf16", d="f32", block_scaled=False, flags=0, c="f32"):
+        self.M, self.N, self.K, self.ab, self.d = M, N, K, ab, d
+        self.block_scaled = bool(block_scaled)
+        self.handle = gemm_plan_create(M, N, K, ab, c, d, 1, 0, int(block_scaled), flags)
+
+    @property
+    def info(self) -> dict:
+        return gemm_plan_get_info(self.handle)
+
+    def run(self, A, B, C, D, SFA=None, SFB=None, stream=None):
+        return gemm_run(self.handle, A, B, C, D, SFA, SFB, stream)
+
+    def run_host(self, A, B, C, D, SFA=None, SFB=None, stream=None):
+        return gemm_run_host(self.handle, A, B, C, D, SFA, SFB, stream)
+
+    def last_status(self) -> int:
+        return gemm_plan_last_status(self.handle)
+
+    def set_timeout(self, ns: int):
+        gemm_plan_set_timeout(self.handle, ns)
+
+    def close(self):
+        if self.handle:
+            gemm_plan_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

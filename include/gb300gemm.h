@@ -1,0 +1,152 @@
+/*
+ * gb300gemm — tensor-core matrix multiply-accumulate D = A·B + C on one
+ * NVIDIA GB300 (sm_103a), behind a plain C ABI.
+ *
+ * The operation is the one the three tensor-core generations share
+ * ("Tensor Core 数据布局的演进", overview: D = AB + C, A and B the multiplied
+ * matrices, C the addend, D the result), computed with fp32 accumulation:
+ *
+ *     D[i][j] = C[i][j] + sum_k a[i][k] * b[k][j]          (0 <= i < M, 0 <= j < N)
+ *
+ * Operands a and b are fp16 or bf16 values, or — block scaled — OCP e4m3
+ * values each multiplied by a UE8M0 power-of-two scale shared by 32
+ * consecutive K elements ("Tensor Core 数据布局的演进", section
+ * "Block-Scaled MMA 的 Scale Factors": SFA[m][sfk] scales row m of A in K
+ * block sfk, SFB[n][sfk] scales column n of B):
+ *
+ *     a[i][k] = e4m3(A[i][k]) * 2^(SFA[i][k/32] - 127)
+ *     b[k][j] = e4m3(B[k][j]) * 2^(SFB[j][k/32] - 127)
+ *
+ * Memory layout (all buffers packed; no leading-dimension arguments):
+ *   A    M x K, row-major (element (i,k) at A[i*K + k]).
+ *   B    K x N, column-major (element (k,j) at B[j*K + k]); both operands
+ *        are thus K-major, the layout the tensor core reads natively.
+ *   C    M x N fp32 row-major, or NULL for C = 0.
+ *   D    M x N row-major, fp32 or bf16 (round to nearest even).
+ *   SFA  M x ceil(K/32) UE8M0 codes, row-major (block-scaled plans only).
+ *   SFB  N x ceil(K/32) UE8M0 codes, row-major (block-scaled plans only).
+ *
+ * Every global row stride and every base pointer must be a multiple of
+ * 16 bytes: the tensor-memory-accelerator copy engine needs one dimension of
+ * stride 1 and 16-byte aligned strides for the others ("(二) CUTLASS —— 掌握
+ * Tensor Memory Accelerator（TMA）", section "使用 TMA 处理 remainder tiles
+ * 以及 stride 要求": pad the tensor before calling otherwise).  For 16-bit
+ * operands that means K % 8 == 0, for e4m3 K % 16 == 0; for C and fp32 D
+ * N % 4 == 0, for bf16 D N % 8 == 0.  M, N and K need not be multiples of
+ * any tile size: the copy engine predicates the remainder tiles.
+ *
+ * Ownership: the caller owns every device buffer.  A plan owns host state and
+ * one small device status word.  Calls on one plan are not thread-safe; calls
+ * on different plans are.  No entry point aborts the process: each returns a
+ * gemm_status.
+ */
+#ifndef GB300GEMM_H
+#define GB300GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,   /* null plan/pointer, dimension <= 0, bad enum value */
+    GEMM_ERR_UNSUPPORTED = 2,   /* dtype / layout combination or device not handled */
+    GEMM_ERR_ALIGNMENT = 3,     /* a base pointer or row stride is not a multiple of 16 bytes */
+    GEMM_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed */
+    GEMM_ERR_TIMEOUT = 5        /* a bounded wait inside a kernel ran out; the kernel gave up */
+} gemm_status;
+
+typedef enum {
+    GEMM_F16 = 0,
+    GEMM_BF16 = 1,
+    GEMM_E4M3 = 2,
+    GEMM_F32 = 3
+} gemm_dtype;
+
+/* gemm_plan_create flags */
+#define GEMM_FLAG_SYNC        0x1u  /* gemm_run synchronises its stream and returns the kernel status */
+#define GEMM_FLAG_FORCE_1CTA  0x2u  /* use single-CTA tiles (cta_group::1) even where pairs would be chosen */
+#define GEMM_FLAG_FORCE_2CTA  0x4u  /* use CTA-pair tiles (cta_group::2) even where single CTAs would be chosen */
+
+typedef struct gemm_plan *gemm_plan_t;
+
+/* What a plan will launch (for tests, benchmarks and logs). */
+typedef struct {
+    int cta_group;          /* 1: one CTA per tile, 2: CTA pairs (cta_group::2) share a tile */
+    int tile_m, tile_n;     /* output tile of one CTA (group) */
+    int tile_k;             /* K elements per pipeline stage */
+    int stages;             /* shared-memory ring depth */
+    int grid;               /* CTAs launched (persistent) */
+    int tiles;              /* output tiles */
+    int smem_bytes;         /* dynamic shared memory per CTA */
+    int launches_per_run;   /* kernels one gemm_run enqueues */
+    int sm_count;           /* SMs of the device the plan was made for */
+} gemm_plan_info;
+
+/*
+ * Validate a problem and choose its kernel.  M, N, K > 0.  ab is GEMM_F16 or
+ * GEMM_BF16 (block_scaled = 0) or GEMM_E4M3 (block_scaled = 1).  c must be
+ * GEMM_F32; d is GEMM_F32 or GEMM_BF16.  a_row_major = 1 and b_row_major = 0
+ * (both operands K-major) are the supported layout; other combinations return
+ * GEMM_ERR_UNSUPPORTED.  Row-stride alignment (see above) is checked here and
+ * returns GEMM_ERR_ALIGNMENT.  The plan is bound to the CUDA device current
+ * at creation, which must be compute capability 10.3.  *out is set only on
+ * GEMM_OK.
+ */
+gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K,
+                             gemm_dtype ab, gemm_dtype c, gemm_dtype d,
+                             int a_row_major, int b_row_major, int block_scaled,
+                             unsigned flags);
+
+/*
+ * Enqueue D = A·B + C on cuda_stream (a cudaStream_t; NULL = legacy default
+ * stream).  A, B, D: device pointers, non-NULL, 16-byte aligned; C: device
+ * pointer or NULL (C = 0); SFA, SFB: device pointers for block-scaled plans,
+ * ignored otherwise.  D must not overlap A, B, C, SFA or SFB.  Returns after
+ * enqueueing (asynchronous) unless the plan has GEMM_FLAG_SYNC, in which case
+ * it waits for the stream and returns the kernel's status.
+ */
+gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C, void *D,
+                     const uint8_t *SFA, const uint8_t *SFB, void *cuda_stream);
+
+/*
+ * The same product with HOST buffers (any host memory; page-locked memory
+ * copies fastest): copies A, B, C (and SFA, SFB) to device buffers the plan
+ * owns (allocated on first use, freed by gemm_plan_destroy), runs the kernel,
+ * copies D back and waits for the stream.  Returns the kernel's status.
+ */
+gemm_status gemm_run_host(gemm_plan_t p, const void *A, const void *B, const void *C, void *D,
+                          const uint8_t *SFA, const uint8_t *SFB, void *cuda_stream);
+
+/*
+ * Wait for the stream of the plan's last run, read the plan's device status
+ * word (GEMM_OK, or GEMM_ERR_TIMEOUT if a kernel gave up on a wait) and
+ * reset it to GEMM_OK.
+ */
+gemm_status gemm_plan_last_status(gemm_plan_t p);
+
+/* Fill *info with the plan's launch configuration. */
+gemm_status gemm_plan_get_info(gemm_plan_t p, gemm_plan_info *info);
+
+/*
+ * Set the limit, in nanoseconds, of every wait inside the plan's kernels
+ * (default 1e9).  When a wait runs out the kernel records GEMM_ERR_TIMEOUT in
+ * the status word, its other roles stop, it frees its tensor memory and it
+ * returns; the CUDA context stays usable.
+ */
+gemm_status gemm_plan_set_timeout(gemm_plan_t p, uint64_t ns);
+
+/* Release the plan (its status word and any host-run buffers).  NULL is a no-op. */
+gemm_status gemm_plan_destroy(gemm_plan_t p);
+
+/* Static description of a status code. */
+const char *gemm_status_string(gemm_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB300GEMM_H */

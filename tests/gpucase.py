@@ -1,0 +1,116 @@
+"""Shared helpers of the GPU parity tests: run one workload through the C ABI
+and compare it with the oracle under the accept rule
+
+    |D_gpu - D_ref| <= 1e-5 * sum_k |a b| + 1e-6 * |c|   (+ 1 bf16 ulp of D_ref for bf16 D)
+
+The operands are the seeded synthetic inputs both sides share; the reference
+values come from the oracle only."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from blackwell_tensor_core_tma_gb300 import gemm, synth
+
+REL_S = 1e-5
+REL_C = 1e-6
+
+
+def to_device(x: np.ndarray):
+    import torch
+    if x.dtype == np.uint16:
+        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16))
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(x))
+    return t.cuda()
+
+
+def decode_d(t, d: str) -> np.ndarray:
+    """fp64 values of a device D (fp32, or bf16 codes widened exactly)."""
+    import torch
+    if d == "bf16":
+        bits = t.view(torch.int16).cpu().numpy().view(np.uint16)
+        return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return t.cpu().numpy().astype(np.float64)
+
+
+def run(w: synth.Workload, flags: int = 0, c_none: bool = False, guard: int = 0, inputs=None, reps: int = 1):
+    """Run w through gemm_run; returns (inputs, D as fp64, plan info, status, guard intact)."""
+    import torch
+    x = inputs if inputs is not None else synth.make_inputs(w)
+    A, B = to_device(x["A"]), to_device(x["B"])
+    C = None if c_none else to_device(x["C"])
+    SFA = to_device(x["SFA"]) if w.block_scaled else None
+    SFB = to_device(x["SFB"]) if w.block_scaled else None
+    tdt = torch.bfloat16 if w.d == "bf16" else torch.float32
+    n = w.M * w.N
+    g = guard
+    buf = torch.full((n + 2 * g,), float("nan"), dtype=tdt, device="cuda")
+    D = buf[g:g + n].view(w.M, w.N)
+    with gemm.Plan(w.M, w.N, w.K, w.ab, w.d, w.block_scaled, flags) as plan:
+        for _ in range(reps):
+            plan.run(A, B, C, D, SFA, SFB, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        status = plan.last_status()
+        info = plan.info
+    intact = True
+    if g:
+        intact = bool(torch.isnan(buf[:g]).all().item()) and bool(torch.isnan(buf[g + n:]).all().item())
+    return x, decode_d(D, w.d), info, status, intact
+
+
+def tolerance(w, D_ref, S, c):
+    tol = REL_S * S + REL_C * np.abs(c)
+    if w.d == "bf16":
+        tol = tol + oracle.bf16_ulp(D_ref)
+    return tol
+
+
+def check_full(w, x, D, c_none=False):
+    C = None if c_none else x["C"]
+    D_ref, S = oracle.gemm(x["A"], x["B"], C, w.M, w.N, w.K, w.ab, a_row_major=w.a_row_major,
+                           b_row_major=w.b_row_major, SFA=x.get("SFA"), SFB=x.get("SFB"),
+                           block_scaled=w.block_scaled)
+    c = np.zeros_like(D_ref) if c_none else x["C"].astype(np.float64)
+    _assert_within(w, D, D_ref, S, c, "full")
+
+
+def sample_entries(M: int, N: int, tile_m: int, tile_n: int, n_random: int = 4096, seed: int = 0):
+    """Tile corners and edges, one full row and column, and random entries."""
+    rng = np.random.default_rng(seed)
+    rows, cols = [], []
+    rm = sorted({r for t in range(0, M, tile_m) for r in (t, t + 31, t + 32, t + tile_m // 2, t + tile_m - 1)
+                 if r < M} | {M - 1})
+    cn = sorted({c for t in range(0, N, tile_n) for c in (t, t + 31, t + 32, t + tile_n // 2, t + tile_n - 1)
+                 if c < N} | {N - 1})
+    for r in rm[:: max(1, len(rm) // 64)]:
+        for c in cn[:: max(1, len(cn) // 64)]:
+            rows.append(r)
+            cols.append(c)
+    r0 = int(rng.integers(0, M))
+    c0 = int(rng.integers(0, N))
+    rows += [r0] * N + list(range(M))
+    cols += list(range(N)) + [c0] * M
+    rows += list(rng.integers(0, M, n_random))
+    cols += list(rng.integers(0, N, n_random))
+    return np.array(rows, np.int64), np.array(cols, np.int64)
+
+
+def check_entries(w, x, D, rows, cols):
+    D_ref, S = oracle.gemm_entries(x["A"], x["B"], x["C"], w.M, w.N, w.K, w.ab, rows, cols,
+                                   a_row_major=w.a_row_major, b_row_major=w.b_row_major,
+                                   SFA=x.get("SFA"), SFB=x.get("SFB"), block_scaled=w.block_scaled)
+    c = x["C"][rows, cols].astype(np.float64)
+    _assert_within(w, D[rows, cols], D_ref, S, c, f"{rows.size} sampled entries")
+
+
+def _assert_within(w, D, D_ref, S, c, what):
+    tol = tolerance(w, D_ref, S, c)
+    err = np.abs(D - D_ref)
+    bad = ~(err <= tol)
+    if bad.any():
+        idx = np.flatnonzero(bad.ravel())
+        k = idx[np.argmax((err.ravel()[idx]) / np.maximum(tol.ravel()[idx], 1e-300))] if idx.size else 0
+        raise AssertionError(
+            f"{w.name} ({what}): {idx.size} of {err.size} entries outside tolerance; worst flat index {k}: "
+            f"gpu {D.ravel()[k]!r} ref {D_ref.ravel()[k]!r} tol {tol.ravel()[k]!r}")

@@ -1,0 +1,79 @@
+"""The C-ABI library builds, loads without a GPU, exports every symbol the
+headers declare, and rejects bad plans before touching a device."""
+import os
+import re
+
+import pytest
+
+from blackwell_tensor_core_tma_gb300 import build, gemm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in ("gb300gemm.h", "gb300gemm_testing.h"):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        names |= set(re.findall(r"^\s*(?:gemm_status|const char \*)\s*\**(gemm_\w+)\s*\(", text, re.M))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return gemm.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert declared == set(gemm.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert gemm.gemm_status_string(s)
+    assert "unknown" in gemm.gemm_status_string(99)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, 256, 256), gemm.GEMM_ERR_INVALID_ARG),
+    ((256, -1, 256), gemm.GEMM_ERR_INVALID_ARG),
+    ((256, 256, 0), gemm.GEMM_ERR_INVALID_ARG),
+    ((256, 256, 2057), gemm.GEMM_ERR_ALIGNMENT),     # 16-bit K-major rows of 4114 bytes
+    ((256, 258, 256), gemm.GEMM_ERR_ALIGNMENT),      # fp32 C rows of 1032 bytes
+])
+def test_plan_rejects_before_device(lib, args, status):
+    with pytest.raises(gemm.GemmError) as e:
+        gemm.gemm_plan_create(*args)
+    assert e.value.status == status
+
+
+def test_plan_rejects_unsupported_combinations(lib):
+    cases = [
+        dict(ab="f32"), dict(c="bf16"), dict(d="f16"), dict(a_row_major=0), dict(b_row_major=1),
+        dict(ab="e4m3", block_scaled=0), dict(ab="bf16", block_scaled=1),
+    ]
+    for kw in cases:
+        with pytest.raises(gemm.GemmError) as e:
+            gemm.gemm_plan_create(256, 256, 256, **kw)
+        assert e.value.status == gemm.GEMM_ERR_UNSUPPORTED, kw
+    with pytest.raises(gemm.GemmError) as e:
+        gemm.gemm_plan_create(256, 256, 256, flags=gemm.GEMM_FLAG_FORCE_1CTA | gemm.GEMM_FLAG_FORCE_2CTA)
+    assert e.value.status == gemm.GEMM_ERR_INVALID_ARG
+
+
+def test_null_plan_calls(lib):
+    assert lib.gemm_run(None, None, None, None, None, None, None, None) == gemm.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_plan_last_status(None) == gemm.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_plan_destroy(None) == gemm.GEMM_OK
+    assert lib.gemm_plan_set_timeout(None, 10) == gemm.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_testing_set_fault(None, 1) == gemm.GEMM_ERR_INVALID_ARG
+
+
+def test_no_cpu_fallback_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(gemm, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU path"):
+        gemm.lib()

@@ -1,0 +1,99 @@
+"""GPU parity of the tensor-core GEMM against the fp64 oracle, through the C ABI.
+
+Small cases compare every element; the full-size workloads (in the launch
+configuration the benchmark times, i.e. the default plan) compare tile
+corners and edges, a full row and column, and random entries."""
+import numpy as np
+import pytest
+
+from blackwell_tensor_core_tma_gb300 import gemm, synth
+from tests import gpucase
+
+pytestmark = pytest.mark.gpu
+
+W = synth.WORKLOADS
+BF16_UNI = W["bf16_4096x4096x4096_f32out"]
+F16_NORM = W["f16_4000x3000x2056_f32out"]
+BF16_OUT = W["bf16_8192x8192x8192_bf16out"]
+
+FORCE = {"1cta": gemm.GEMM_FLAG_FORCE_1CTA, "2cta": gemm.GEMM_FLAG_FORCE_2CTA}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gemm.lib()
+
+
+def test_first_workload_full():
+    """bf16 256^3, C = 0 passed as a zero buffer, fp32 D: every element."""
+    w = W["bf16_256x256x256_c0_f32out"]
+    x, D, info, st, intact = gpucase.run(w, guard=4096)
+    assert st == gemm.GEMM_OK and intact
+    gpucase.check_full(w, x, D)
+
+
+@pytest.mark.parametrize("variant", ["1cta", "2cta"])
+@pytest.mark.parametrize("base,M,N,K", [
+    (BF16_UNI, 640, 768, 512),        # several whole tiles
+    (F16_NORM, 1000, 600, 520),       # ragged M, N and K (K % 64 == 8)
+    (BF16_OUT, 1100, 1048, 1032),     # bf16 D, ragged
+    (F16_NORM, 129, 260, 72),         # one row and a few columns past a tile
+])
+def test_parity_small(variant, base, M, N, K):
+    w = synth.scaled(base, M, N, K)
+    x, D, info, st, intact = gpucase.run(w, flags=FORCE[variant], guard=1024)
+    assert st == gemm.GEMM_OK and intact
+    assert info["cta_group"] == (1 if variant == "1cta" else 2)
+    gpucase.check_full(w, x, D)
+
+
+@pytest.mark.parametrize("variant", ["1cta", "2cta"])
+def test_c_null_means_zero(variant):
+    w = synth.scaled(F16_NORM, 300, 520, 264)
+    x, D, info, st, intact = gpucase.run(w, flags=FORCE[variant], c_none=True, guard=512)
+    assert st == gemm.GEMM_OK and intact
+    gpucase.check_full(w, x, D, c_none=True)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4, 8), (1, 8, 8), (7, 12, 24), (128, 256, 64), (257, 264, 8)])
+def test_degenerate_shapes(M, N, K):
+    base = BF16_OUT if N % 8 == 0 else BF16_UNI
+    w = synth.scaled(base, M, N, K)
+    x, D, info, st, intact = gpucase.run(w, guard=256)
+    assert st == gemm.GEMM_OK and intact
+    gpucase.check_full(w, x, D)
+
+
+def test_long_k_and_many_tiles_per_cta():
+    """K = 16384 stresses the ring over many wraps; 2 x 32 tiles per CTA for the scheduler."""
+    w = synth.scaled(BF16_UNI, 256, 512, 16384)
+    x, D, info, st, _ = gpucase.run(w, flags=gemm.GEMM_FLAG_FORCE_1CTA)
+    assert st == gemm.GEMM_OK
+    gpucase.check_full(w, x, D)
+    for M, N, K, flags in [(4096, 4096, 64, gemm.GEMM_FLAG_FORCE_1CTA), (8192, 4096, 64, 0)]:
+        w2 = synth.scaled(BF16_UNI, M, N, K)
+        x, D, info, st, _ = gpucase.run(w2, flags=flags)
+        assert st == gemm.GEMM_OK and info["tiles"] > 2 * info["grid"] // info["cta_group"]
+        gpucase.check_full(w2, x, D)
+
+
+def test_repeated_runs_identical():
+    w = synth.scaled(BF16_UNI, 512, 512, 640)
+    x, D1, _, st1, _ = gpucase.run(w, reps=1)
+    _, D3, _, st3, _ = gpucase.run(w, inputs=x, reps=3)
+    assert st1 == st3 == gemm.GEMM_OK
+    assert np.array_equal(D1, D3)
+
+
+@pytest.mark.parametrize("name", ["bf16_4096x4096x4096_f32out", "f16_4000x3000x2056_f32out",
+                                  "bf16_8192x8192x8192_bf16out"])
+def test_full_size_sampled(name):
+    w = W[name]
+    x, D, info, st, intact = gpucase.run(w, guard=4096)
+    assert st == gemm.GEMM_OK and intact
+    rows, cols = gpucase.sample_entries(w.M, w.N, info["tile_m"], info["tile_n"])
+    gpucase.check_entries(w, x, D, rows, cols)
+    assert np.isfinite(D).all()
