@@ -139,6 +139,24 @@ class ClockSampler:
                 "samples": len(sms)}
 
 
+def smi_index(local_rank: int) -> int:
+    """nvidia-smi index of CUDA device local_rank (through CUDA_VISIBLE_DEVICES)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [v.strip() for v in vis.split(",") if v.strip()]
+    if local_rank < len(ids) and ids[local_rank].isdigit():
+        return int(ids[local_rank])
+    return local_rank
+
+
+def workload(args):
+    from blackwell_tensor_core_tma_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    if args.shape:
+        M, N, K = (int(v) for v in args.shape.lower().split("x"))
+        w = synth.scaled(w, M, N, K)
+    return w
+
+
 # --------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local_rank):
@@ -149,7 +167,7 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = synth.WORKLOADS[args.workload]
+    w = workload(args)
     x = synth.make_inputs(w)
 
     def dev_tensor(a):
@@ -181,7 +199,7 @@ def run_ours(args, rank, world, local_rank):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
-    with ClockSampler(local_rank) as clocks:
+    with ClockSampler(smi_index(local_rank)) as clocks:
         t0.record(stream)
         for i in range(args.steps):
             ev[i][0].record(stream)
@@ -291,7 +309,7 @@ def run_reference(args, rank, world):
     import oracle
     from blackwell_tensor_core_tma_gb300 import synth
 
-    w = synth.WORKLOADS[args.workload]
+    w = workload(args)
     x = synth.make_inputs(w)
     rng = np.random.default_rng(0)
     total_budget = args.reference_seconds
@@ -339,6 +357,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--shape", default=None, help="MxNxK: the workload's recipe at other sizes (profiling)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
