@@ -21,7 +21,8 @@ DTYPE = {"f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM_E4M3, "f32": GEMM_F32}
 
 # every symbol include/gb300gemm.h and include/gb300gemm_testing.h declare
 EXPORTS = ["gemm_plan_create", "gemm_run", "gemm_run_host", "gemm_plan_last_status", "gemm_plan_get_info",
-           "gemm_plan_set_timeout", "gemm_plan_destroy", "gemm_status_string", "gemm_testing_set_fault"]
+           "gemm_plan_set_timeout", "gemm_plan_destroy", "gemm_status_string", "gemm_testing_set_fault",
+           "gemm_run_noalloc"]
 
 
 class GemmError(RuntimeError):
@@ -69,6 +70,8 @@ def lib():
         L.gemm_status_string.restype = ctypes.c_char_p
         L.gemm_testing_set_fault.argtypes = [vp, st]
         L.gemm_testing_set_fault.restype = st
+        L.gemm_run_noalloc.argtypes = [i64, i64, i64, st, st, vp, vp, vp, vp, vp, st]
+        L.gemm_run_noalloc.restype = st
         _lib = L
     return _lib
 
@@ -143,6 +146,14 @@ def gemm_plan_destroy(plan: int):
 
 def gemm_testing_set_fault(plan: int, fault: int):
     _check(lib().gemm_testing_set_fault(plan, fault), "gemm_testing_set_fault")
+
+
+def gemm_run_noalloc(M: int, N: int, K: int, ab, d, A, B, C, D, stream=None, wait: int = 0) -> int:
+    """Allocation-free run (no plan): the kernel's status word lives in a static device array."""
+    st = lib().gemm_run_noalloc(M, N, K, DTYPE.get(ab, ab), DTYPE.get(d, d), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                _stream(stream), int(wait))
+    _check(st, "gemm_run_noalloc")
+    return st
 
 
 class Plan:

@@ -142,6 +142,40 @@ gemm_status gemm_plan_set_timeout(gemm_plan_t p, uint64_t ns);
 /* Release the plan (its status word and any host-run buffers).  NULL is a no-op. */
 gemm_status gemm_plan_destroy(gemm_plan_t p);
 
+/*
+ * Allocation-free variant of gemm_run for the fp16/bf16 kernel (the pages
+ * have no counterpart to this entry point; it is a property of this library).
+ *
+ * Some callers cannot call cudaMalloc: a host program whose device memory is
+ * all owned by its own allocator and that forbids allocations behind its
+ * back, a latency-critical loop that cannot afford the device-wide
+ * synchronisation cudaMalloc and cudaFree imply, or a plug-in held to a fixed
+ * memory budget.  The plan API does allocate (each plan's device status
+ * word), so this entry point takes no plan and allocates nothing: the
+ * kernel's only memory beyond A, B, C and D — its 4-byte status word — lives
+ * in a file-scope __device__ array of 256 bytes that every GPU which loads
+ * the library holds until the process exits.  A kernel needing more scratch
+ * than the array holds would be rejected with GEMM_ERR_INVALID_ARG.
+ *
+ * Arguments mean what they mean for gemm_plan_create + gemm_run with
+ * a_row_major = 1, b_row_major = 0, c = GEMM_F32, no flags (the same kernel
+ * is chosen): ab is GEMM_F16 or GEMM_BF16, d is GEMM_F32 or GEMM_BF16, C may
+ * be NULL.  The caller owns and passes every input and output.  With
+ * wait = 0 the call returns after enqueueing; with wait != 0 it synchronises
+ * cuda_stream and returns the kernel's status (GEMM_ERR_TIMEOUT if a bounded
+ * wait ran out).
+ *
+ * The first call on a device does a one-time set-up there (it looks up the
+ * array's device address with cudaGetSymbolAddress and sets the kernel's
+ * shared-memory limit); make that first call before any stream capture.  All
+ * calls on a device share the one array, and each call clears the status word
+ * before its kernel runs, so calls whose kernels overlap on the GPU (for
+ * example on two streams at once) race on it; serialise them.
+ */
+gemm_status gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype ab, gemm_dtype d,
+                             const void *A, const void *B, const void *C, void *D,
+                             void *cuda_stream, int wait);
+
 /* Static description of a status code. */
 const char *gemm_status_string(gemm_status s);
 
