@@ -180,7 +180,8 @@ def run_ours(args, rank, world, local_rank):
     SFB = dev_tensor(x["SFB"]) if w.block_scaled else None
     d_t = torch.bfloat16 if w.d == "bf16" else torch.float32
     D = torch.empty((w.M, w.N), dtype=d_t, device=dev)
-    plan = gemm.Plan(w.M, w.N, w.K, w.ab, w.d, w.block_scaled)
+    flags = {0: 0, 1: gemm.GEMM_FLAG_FORCE_1CTA, 2: gemm.GEMM_FLAG_FORCE_2CTA}[args.cta_group]
+    plan = gemm.Plan(w.M, w.N, w.K, w.ab, w.d, w.block_scaled, flags)
     info = plan.info
     stream = torch.cuda.Stream(device=dev)
 
@@ -358,6 +359,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--shape", default=None, help="MxNxK: the workload's recipe at other sizes (profiling)")
+    ap.add_argument("--cta-group", type=int, choices=[0, 1, 2], default=0,
+                    help="force single CTAs (1) or CTA pairs (2); 0 = the plan's choice")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")

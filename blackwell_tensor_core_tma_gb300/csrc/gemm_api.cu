@@ -35,6 +35,10 @@ struct gemm_plan {
     uint64_t timeout_ns;
     int fault;
     int *status;              // device word
+    int family;               // 0: fp16/bf16 kernel, 1: block-scaled e4m3 kernel
+    int tile_n;
+    int num_kb;
+    uint8_t *ws_a, *ws_b;     // block-scaled: packed scale factors (workspace)
     // device buffers of gemm_run_host (allocated on first use)
     void *hA, *hB, *hC, *hD;
     uint8_t *hSFA, *hSFB;
@@ -92,7 +96,7 @@ gemm_status encode_maps(gemm_plan *p, const void *A, const void *B, const void *
     std::memset(p->maps, 0, sizeof p->maps);
     const int eb = elem_bytes(p->ab);
     const uint32_t bk = 128u / (uint32_t)eb;                       // K elements in a 128-byte row
-    const uint32_t b_rows = (uint32_t)(TILE_N / p->cta_group);
+    const uint32_t b_rows = (uint32_t)(p->tile_n / p->cta_group);
     bool ok = encode_2d(&p->maps[0], tma_dtype(p->ab), eb, A, p->K, p->M, bk, TILE_M, CU_TENSOR_MAP_SWIZZLE_128B) &&
               encode_2d(&p->maps[1], tma_dtype(p->ab), eb, B, p->K, p->N, bk, b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (ok && C)
@@ -129,6 +133,9 @@ gemm_status configure_f16(gemm_plan *p) {
     p->cta_group = cg;
     p->stages = f16_stages(cg);
     p->smem = f16_smem_bytes(cg);
+    p->family = 0;
+    p->tile_n = TILE_N;
+    p->num_kb = (int)((p->K + TILE_K16 - 1) / TILE_K16);
     p->tiles_m = (int)((p->M + TILE_M * cg - 1) / (TILE_M * cg));
     p->tiles_n = (int)((p->N + TILE_N - 1) / TILE_N);
     p->tiles = p->tiles_m * p->tiles_n;
@@ -139,6 +146,30 @@ gemm_status configure_f16(gemm_plan *p) {
     }
     p->grid = cg * (p->tiles < units ? p->tiles : units);
     p->group_m = cg == 2 ? 8 : 16;
+    return GEMM_OK;
+}
+
+gemm_status configure_mxf8(gemm_plan *p) {
+    if (p->flags & GEMM_FLAG_FORCE_2CTA) return GEMM_ERR_UNSUPPORTED;
+    if (mxf8_prepare(p->d == GEMM_BF16) != cudaSuccess) return GEMM_ERR_CUDA;
+    p->family = 1;
+    p->cta_group = 1;
+    p->tile_n = MXF8_TILE_N;
+    p->stages = mxf8_stages();
+    p->smem = mxf8_smem_bytes();
+    p->num_kb = (int)((p->K + 127) / 128);
+    p->tiles_m = (int)((p->M + TILE_M - 1) / TILE_M);
+    p->tiles_n = (int)((p->N + MXF8_TILE_N - 1) / MXF8_TILE_N);
+    p->tiles = p->tiles_m * p->tiles_n;
+    p->grid = p->tiles < p->sm_count ? p->tiles : p->sm_count;
+    p->group_m = 16;
+    if (cudaMalloc(&p->ws_a, mxf8_workspace_a(p->tiles_m, p->num_kb)) != cudaSuccess ||
+        cudaMalloc(&p->ws_b, mxf8_workspace_b(p->tiles_n, p->num_kb)) != cudaSuccess) {
+        cudaFree(p->ws_a);
+        cudaFree(p->ws_b);
+        p->ws_a = p->ws_b = nullptr;
+        return GEMM_ERR_CUDA;
+    }
     return GEMM_OK;
 }
 
@@ -167,7 +198,6 @@ gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K, 
     if (c != GEMM_F32 || (d != GEMM_F32 && d != GEMM_BF16)) return GEMM_ERR_UNSUPPORTED;
     if (block_scaled ? ab != GEMM_E4M3 : (ab != GEMM_F16 && ab != GEMM_BF16)) return GEMM_ERR_UNSUPPORTED;
     if (!a_row_major || b_row_major) return GEMM_ERR_UNSUPPORTED;
-    if (block_scaled) return GEMM_ERR_UNSUPPORTED;
     // 16-byte row strides (the copy engine's stride rule)
     if ((K * elem_bytes(ab)) % 16 != 0 || (N * 4) % 16 != 0 || (N * elem_bytes(d)) % 16 != 0)
         return GEMM_ERR_ALIGNMENT;
@@ -191,7 +221,7 @@ gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K, 
     p->device = dev;
     p->sm_count = prop.multiProcessorCount;
     p->timeout_ns = 1000000000ull;
-    gemm_status st = configure_f16(p);
+    gemm_status st = block_scaled ? configure_mxf8(p) : configure_f16(p);
     if (st != GEMM_OK) {
         delete p;
         return st;
@@ -211,9 +241,8 @@ gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K, 
 
 gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C, void *D, const uint8_t *SFA,
                      const uint8_t *SFB, void *cuda_stream) {
-    (void)SFA;
-    (void)SFB;
     if (!p || !A || !B || !D) return GEMM_ERR_INVALID_ARG;
+    if (p->family == 1 && (!SFA || !SFB)) return GEMM_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (C && !aligned16(C))) return GEMM_ERR_ALIGNMENT;
     gemm_status st = encode_maps(p, A, B, C, D);
     if (st != GEMM_OK) return st;
@@ -225,16 +254,26 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
     kp.tiles_m = p->tiles_m;
     kp.tiles_n = p->tiles_n;
     kp.num_tiles = p->tiles;
-    kp.num_kb = (int)((p->K + TILE_K16 - 1) / TILE_K16);
+    kp.num_kb = p->num_kb;
     kp.group_m = p->group_m;
     kp.has_c = C != nullptr;
-    kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * p->cta_group), (uint32_t)TILE_N);
     kp.status = p->status;
     kp.timeout_ns = p->timeout_ns;
     kp.fault = p->fault;
-    F16Config cfg{p->cta_group, p->d == GEMM_BF16};
     LaunchShape shape{p->grid, p->cta_group, p->smem};
-    if (f16_launch(cfg, shape, p->maps, kp, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (p->family == 1) {
+        kp.idesc = idesc_mxf8((uint32_t)TILE_M, (uint32_t)MXF8_TILE_N, 0, 0);
+        kp.sfa = p->ws_a;
+        kp.sfb = p->ws_b;
+        if (mxf8_pack(SFA, SFB, p->ws_a, p->ws_b, kp.M, kp.N, kp.K, p->tiles_m, p->tiles_n, p->num_kb, p->sm_count,
+                      stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (mxf8_launch(p->d == GEMM_BF16, shape, p->maps, kp, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    } else {
+        kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * p->cta_group), (uint32_t)TILE_N);
+        F16Config cfg{p->cta_group, p->d == GEMM_BF16};
+        if (f16_launch(cfg, shape, p->maps, kp, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    }
     if (p->flags & GEMM_FLAG_SYNC) {
         if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
         return gemm_plan_last_status(p);
@@ -259,11 +298,19 @@ gemm_status gemm_run_host(gemm_plan_t p, const void *A, const void *B, const voi
         cudaMemcpyAsync(p->hB, B, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     if (C && cudaMemcpyAsync(p->hC, C, c_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GEMM_ERR_CUDA;
-    (void)SFA;
-    (void)SFB;
+    if (p->family == 1) {
+        if (!SFA || !SFB) return GEMM_ERR_INVALID_ARG;
+        const size_t sfk = (size_t)((p->K + 31) / 32);
+        if (!p->hSFA && (cudaMalloc(&p->hSFA, (size_t)p->M * sfk) != cudaSuccess ||
+                         cudaMalloc(&p->hSFB, (size_t)p->N * sfk) != cudaSuccess))
+            return GEMM_ERR_CUDA;
+        if (cudaMemcpyAsync(p->hSFA, SFA, (size_t)p->M * sfk, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+            cudaMemcpyAsync(p->hSFB, SFB, (size_t)p->N * sfk, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
     const unsigned saved = p->flags;
     p->flags &= ~GEMM_FLAG_SYNC;
-    gemm_status st = gemm_run(p, p->hA, p->hB, C ? p->hC : nullptr, p->hD, nullptr, nullptr, cuda_stream);
+    gemm_status st = gemm_run(p, p->hA, p->hB, C ? p->hC : nullptr, p->hD, p->hSFA, p->hSFB, cuda_stream);
     p->flags = saved;
     if (st != GEMM_OK) return st;
     if (cudaMemcpyAsync(D, p->hD, d_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return GEMM_ERR_CUDA;
@@ -284,13 +331,13 @@ gemm_status gemm_plan_get_info(gemm_plan_t p, gemm_plan_info *info) {
     if (!p || !info) return GEMM_ERR_INVALID_ARG;
     info->cta_group = p->cta_group;
     info->tile_m = TILE_M * p->cta_group;
-    info->tile_n = TILE_N;
+    info->tile_n = p->tile_n;
     info->tile_k = 128 / elem_bytes(p->ab);
     info->stages = p->stages;
     info->grid = p->grid;
     info->tiles = p->tiles;
     info->smem_bytes = p->smem;
-    info->launches_per_run = 1;
+    info->launches_per_run = p->family == 1 ? 2 : 1;
     info->sm_count = p->sm_count;
     return GEMM_OK;
 }
@@ -310,6 +357,8 @@ gemm_status gemm_plan_destroy(gemm_plan_t p) {
     cudaFree(p->hD);
     cudaFree(p->hSFA);
     cudaFree(p->hSFB);
+    cudaFree(p->ws_a);
+    cudaFree(p->ws_b);
     delete p;
     return GEMM_OK;
 }

@@ -43,6 +43,18 @@ cudaError_t f16_max_active_clusters(const F16Config &cfg, int *clusters);
 cudaError_t f16_launch(const F16Config &cfg, const LaunchShape &shape, const CUtensorMap *maps,
                        const KParams &p, cudaStream_t stream);
 
+// block-scaled e4m3 kernel family (gemm_mxf8.cu): single CTAs, 128 x MXF8_TILE_N tiles
+constexpr int MXF8_TILE_N = 224;
+int mxf8_stages();
+int mxf8_smem_bytes();
+size_t mxf8_workspace_a(int tiles_m, int num_kb);
+size_t mxf8_workspace_b(int tiles_n, int num_kb);
+cudaError_t mxf8_prepare(int out_bf16);
+cudaError_t mxf8_pack(const uint8_t *sfa, const uint8_t *sfb, uint8_t *out_a, uint8_t *out_b, int M, int N, int K,
+                      int tiles_m, int tiles_n, int num_kb, int sm_count, cudaStream_t stream);
+cudaError_t mxf8_launch(int out_bf16, const LaunchShape &shape, const CUtensorMap *maps, const KParams &p,
+                        cudaStream_t stream);
+
 constexpr int TILE_M = 128;   // rows of D per CTA
 constexpr int TILE_N = 256;   // columns of D per CTA (and per CTA pair)
 constexpr int TILE_K16 = 64;  // 16-bit K elements per stage (one 128-byte swizzle row)

@@ -1,0 +1,430 @@
+// Persistent, warp-specialised tensor-core GEMM for sm_103a (shared by the
+// fp16/bf16 and the block-scaled e4m3 kernels):
+//   D = A·B + C, A (M x K) and B (K x N) K-major, fp32 accumulation in tensor
+//   memory, C fp32, D fp32 or bf16.
+//
+// One CTA (cta_group::1) or one CTA pair (cta_group::2) owns a 128 x BN or
+// 256 x BN output tile at a time and walks the tile list persistently.
+// Warp roles (192 threads):
+//   warp 0      TMA producer: fills a STAGES-deep shared-memory ring of
+//               A (128 rows) and B (BN/CG rows) boxes of 128-byte K rows,
+//               128-byte swizzled, running STAGES k-blocks ahead of the MMA
+//               ("(二) CUTLASS —— 掌握 Tensor Memory Accelerator（TMA）":
+//               prefetch distance fetch_batch = compute_batch + num_stages;
+//               one thread issues each copy, completion is an mbarrier
+//               transaction count).  Block-scaled kernels also copy the
+//               stage's packed scale factors.
+//   warp 1      allocates 512 TMEM columns (two BN-column fp32 accumulators,
+//               plus scale-factor slots when block-scaled) and, in lane 0 of
+//               the pair's leader CTA, issues tcgen05.mma from shared-memory
+//               descriptors into TMEM ("Tensor Core 数据布局的演进",
+//               Blackwell: A/B in SMEM --tcgen05.mma--> C/D in TMEM); for
+//               block scaling it first moves the stage's scales SMEM -> TMEM
+//               with tcgen05.cp (same page: SFA, SFB: GMEM --TMA--> SMEM
+//               --tcgen05.cp--> TMEM --tcgen05.mma-->).
+//   warps 2..5  epilogue warpgroup: warp w reads TMEM lanes 32*(w%4)..+31
+//               ("Tensor Memory（TMEM）": each warp of a warpgroup reaches its
+//               own 32-lane window) with tcgen05.ld + tcgen05.wait::ld, adds C
+//               (TMA-loaded, 128-byte swizzled), converts, stages D in shared
+//               memory and writes it with a TMA store (proxy fence before the
+//               store, bulk-group wait before the buffer is reused).
+// Every wait is bounded: when one runs out the kernel records
+// GEMM_ERR_TIMEOUT, its roles stop, and it still frees its tensor memory.
+#pragma once
+
+#include <cstdint>
+
+#include "gemm_internal.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+
+// Compile-time shape of one kernel instance.
+//   CG      1 = single CTA per tile, 2 = CTA pair (cta_group::2)
+//   OUT_BF16  D is bf16 (else fp32)
+//   SCALED  block-scaled e4m3 operands (kind::mxf8f6f4, scale_vec::1X)
+//   BN      tile columns (MMA N)
+template <int CG_, bool OUT_BF16_, bool SCALED_, int BN_, int STAGES_>
+struct TileCfg {
+    static constexpr int CG = CG_;
+    static constexpr bool OUT_BF16 = OUT_BF16_;
+    static constexpr bool SCALED = SCALED_;
+    static constexpr int BN = BN_;
+    static constexpr int STAGES = STAGES_;
+    static constexpr int ELEM = SCALED ? 1 : 2;                 // operand bytes
+    static constexpr int BK = 128 / ELEM;                       // K elements per stage: one 128-byte row
+    static constexpr int MMA_K = 32 / ELEM;                     // K per instruction: 32 bytes
+    static constexpr int A_BYTES = TILE_M * 128;                // 16 KiB
+    static constexpr int B_ROWS = BN / CG;                      // B rows held by one CTA
+    static constexpr int B_BYTES = B_ROWS * 128;
+    static constexpr int SFA_BYTES = SCALED ? 512 : 0;          // 128 rows x 4 K-blocks of 32
+    static constexpr int SFB_BYTES = SCALED ? 512 * ((BN + 127) / 128) : 0;
+    static constexpr int TX_BYTES = CG * (A_BYTES + B_BYTES) + SFA_BYTES + SFB_BYTES;
+    static constexpr int EPI_BUF = 32 * EPI_COLS * 4;           // one 32 x 32 fp32 box
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+    static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
+    static constexpr int OFF_EPI = OFF_SF + STAGES * (SFA_BYTES + SFB_BYTES);
+    static constexpr int OFF_BAR = OFF_EPI + 4 * 2 * EPI_BUF;
+    // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], cload[4 warps][2], drain
+    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 8 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base slot, abort flag
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
+    // TMEM columns: accumulators [0, 2*BN), then one SFB slot (4 columns per
+    // 128 rows of B) and one SFA slot (4 columns, padded to 8) per stage; every
+    // slot starts on a multiple of 8 columns
+    static constexpr int SFB_COLS = SCALED ? 4 * ((BN + 127) / 128) : 0;
+    static constexpr int SFA_COLS = SCALED ? 8 : 0;
+    static constexpr int SFB_COL0 = 2 * BN;
+    static constexpr int SFA_COL0 = SFB_COL0 + STAGES * SFB_COLS;
+    static_assert(2 * BN + STAGES * (SFB_COLS + SFA_COLS) <= 512, "TMEM budget");
+    static_assert(!SCALED || (SFB_COL0 % 8 == 0 && SFB_COLS % 8 == 0), "scale slots on 8-column boundaries");
+    static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
+    static_assert(BN % EPI_COLS == 0 && BN % 16 == 0 && BN <= 256, "tile N");
+    static_assert(!SCALED || CG == 1, "block-scaled tiles use single CTAs");
+};
+
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int group_m, int &tm, int &tn, int tiles_n) {
+    // groups of group_m M-tiles walk N together so that a wave of CTAs shares
+    // A rows and B columns in L2
+    const int per_group = group_m * tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * group_m;
+    const int gsize = min(tiles_m - first_m, group_m);
+    const int r = t - g * per_group;
+    tm = first_m + r % gsize;
+    tn = r / gsize;
+}
+
+struct Waiter {
+    volatile int *abort_flag;
+    int *status;
+    uint64_t timeout_ns;
+
+    // wait for phase `parity` of `bar`; false if the kernel is giving up
+    // (another role aborted, unless honor_abort is false, or the limit ran out)
+    __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, bool honor_abort = true) const {
+        const uint32_t a = smem_addr(bar);
+        if (mbar_try_wait(a, parity)) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 1;; ++it) {
+            if (mbar_try_wait(a, parity)) return true;
+            if ((it & 15) == 0) {
+                if (honor_abort && *abort_flag) return false;
+                if (globaltimer_ns() - t0 > timeout_ns) {
+                    *abort_flag = 1;
+                    atomicExch(status, (int)GEMM_ERR_TIMEOUT);
+                    return false;
+                }
+            }
+        }
+    }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                   const KParams p) {
+    constexpr int CG = Cfg::CG;
+    constexpr int STAGES = Cfg::STAGES;
+    constexpr int BN = Cfg::BN;
+    constexpr int CHUNKS = BN / EPI_COLS;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *tfull = bars + 2 * STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *cload = tempty + 2;
+    uint64_t *drain = cload + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 4);
+    const Waiter W{abort_flag, p.status, p.timeout_ns};
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        if (p.has_c) prefetch_tensormap(&tmC);
+        prefetch_tensormap(&tmD);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4 * CG);   // every epilogue warp of the pair
+        }
+        for (int i = 0; i < 8; ++i) mbar_init(&cload[i], 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc<CG>(smem_addr(tmem_slot), 512);
+        tmem_relinquish<CG>();
+    }
+    tc_fence_before_sync();
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int tile0 = blockIdx.x / CG;
+    const int tile_step = gridDim.x / CG;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
+                int tm, tn;
+                tile_coords(t, p.tiles_m, p.group_m, tm, tn, p.tiles_n);
+                const int m0 = tm * TILE_M * CG + (int)rank * TILE_M;
+                const int n0 = tn * BN + (int)rank * Cfg::B_ROWS;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!W.wait(&empty[s], ph ^ 1u)) { ok = false; break; }
+                    const bool withhold = p.fault == 1 && t == tile0 && kb == 0;
+                    if (rank == 0 && !withhold) mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
+                    const uint32_t a_dst = smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES);
+                    const uint32_t b_dst = smem_addr(smem + Cfg::OFF_B + s * Cfg::B_BYTES);
+                    const uint32_t fb = smem_addr(&full[s]);
+                    if constexpr (CG == 1) {
+                        tma_load_2d(a_dst, &tmA, fb, kb * Cfg::BK, m0);
+                        tma_load_2d(b_dst, &tmB, fb, kb * Cfg::BK, n0);
+                    } else {
+                        const uint32_t leader_fb = mapa_shared(fb, 0);
+                        tma_load_2d_pair(a_dst, &tmA, leader_fb, kb * Cfg::BK, m0);
+                        tma_load_2d_pair(b_dst, &tmB, leader_fb, kb * Cfg::BK, n0);
+                    }
+                    if constexpr (Cfg::SCALED) {
+                        // packed scale factors of this (tile, k-block): 512 bytes of SFA, 512 per
+                        // 128 B rows of SFB, contiguous in the workspace
+                        const uint32_t sf_dst = smem_addr(smem + Cfg::OFF_SF + s * (Cfg::SFA_BYTES + Cfg::SFB_BYTES));
+                        bulk_load(sf_dst, p.sfa + ((size_t)tm * p.num_kb + kb) * Cfg::SFA_BYTES, Cfg::SFA_BYTES, fb);
+                        bulk_load(sf_dst + Cfg::SFA_BYTES, p.sfb + ((size_t)tn * p.num_kb + kb) * Cfg::SFB_BYTES,
+                                  Cfg::SFB_BYTES, fb);
+                    }
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMA issue
+        if (rank == 0 && lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, acc_it = 0;
+            bool ok = true;
+            for (int t = tile0; ok && t < p.num_tiles; t += tile_step, ++acc_it) {
+                const uint32_t b = acc_it & 1u, aph = (acc_it >> 1) & 1u;
+                if (!W.wait(&tempty[b], aph ^ 1u)) { ok = false; break; }
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + b * BN;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!W.wait(&full[s], ph)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    const uint64_t ad = smem_desc(smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES), 16, 1024, SWZ_128B);
+                    const uint64_t bd = smem_desc(smem_addr(smem + Cfg::OFF_B + s * Cfg::B_BYTES), 16, 1024, SWZ_128B);
+                    if constexpr (Cfg::SCALED) {
+                        // stage s's scales: SFA in 4 columns, SFB in 4 per 128 rows of B,
+                        // each a 32-lane x 16-byte SMEM block replicated to the 4 lane windows
+                        const uint32_t sfa_t = tmem_base + Cfg::SFA_COL0 + s * Cfg::SFA_COLS;
+                        const uint32_t sfb_t = tmem_base + Cfg::SFB_COL0 + s * Cfg::SFB_COLS;
+                        const uint32_t sf_src = smem_addr(smem + Cfg::OFF_SF + s * (Cfg::SFA_BYTES + Cfg::SFB_BYTES));
+                        tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc(sf_src, 512, 128, SWZ_NONE));
+#pragma unroll
+                        for (int h = 0; h < Cfg::SFB_BYTES / 512; ++h)
+                            tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * h,
+                                                       smem_desc(sf_src + Cfg::SFA_BYTES + 512 * h, 512, 128, SWZ_NONE));
+#pragma unroll
+                        for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k)   // K block k of 32 uses scale byte k
+                            mma_mxf8<CG>(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc | (k << 4) | (k << 29), sfa_t, sfb_t,
+                                         (kb | k) != 0);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k)   // 32 bytes of K = 2 descriptor units
+                            mma_f16<CG>(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, (kb | k) != 0);
+                    }
+                    if constexpr (CG == 1) tc_commit<1>(smem_addr(&empty[s]));
+                    else tc_commit_pair(smem_addr(&empty[s]), 0x3);
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                if constexpr (CG == 1) tc_commit<1>(smem_addr(&tfull[b]));
+                else tc_commit_pair(smem_addr(&tfull[b]), 0x3);
+            }
+            // every MMA this thread issued has finished before teardown (also
+            // after an abort: this wait is bounded by time only)
+            tc_commit<CG>(smem_addr(drain));
+            W.wait(drain, 0, false);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                           // TMEM lane window of this warp
+        uint8_t *ebuf = smem + Cfg::OFF_EPI + q * 2 * Cfg::EPI_BUF;
+        uint64_t *cb = cload + 2 * q;
+        // ec counts the 32 x 32 boxes this warp has stored; box ec uses staging
+        // buffer ec % 2, and its C load is that buffer's (ec / 2)-th
+        uint32_t acc_it = 0, ec = 0;
+        for (int t = tile0; t < p.num_tiles; t += tile_step, ++acc_it) {
+            int tm, tn;
+            tile_coords(t, p.tiles_m, p.group_m, tm, tn, p.tiles_n);
+            const uint32_t b = acc_it & 1u, aph = (acc_it >> 1) & 1u;
+            if (!__all_sync(0xffffffffu, W.wait(&tfull[b], aph))) break;
+            tc_fence_after_sync();
+            const int m_warp = tm * TILE_M * CG + (int)rank * TILE_M + 32 * q;
+            const int n_tile = tn * BN;
+            // 32 x 32 boxes that lie wholly outside D are neither loaded nor stored
+            const bool rows_in = m_warp < p.M;
+            const int chunks_in = rows_in ? min(CHUNKS, (p.N - n_tile + EPI_COLS - 1) / EPI_COLS) : 0;
+            const bool use_c = p.has_c && chunks_in > 0;
+            if (use_c && lane == 0) {
+                bulk_wait_group_read0();
+                mbar_arrive_expect_tx(&cb[ec & 1u], Cfg::EPI_BUF);
+                tma_load_2d(smem_addr(ebuf + (ec & 1u) * Cfg::EPI_BUF), &tmC, smem_addr(&cb[ec & 1u]), n_tile, m_warp);
+            }
+            bool ok = true;
+            for (int j = 0; j < CHUNKS; ++j) {
+                const uint32_t cur = ec & 1u;
+                uint8_t *buf = ebuf + cur * Cfg::EPI_BUF;
+                const bool in = j < chunks_in;
+                if (use_c && j + 1 < chunks_in && lane == 0) {
+                    const uint32_t nx = cur ^ 1u;
+                    bulk_wait_group_read0();              // the store from buffer nx has read it
+                    mbar_arrive_expect_tx(&cb[nx], Cfg::EPI_BUF);
+                    tma_load_2d(smem_addr(ebuf + nx * Cfg::EPI_BUF), &tmC, smem_addr(&cb[nx]),
+                                n_tile + EPI_COLS * (j + 1), m_warp);
+                }
+                uint32_t acc[32];
+                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(32 * q) << 16) + b * BN + EPI_COLS * j, acc);
+                tmem_ld_wait(acc);
+                if (j == CHUNKS - 1) {
+                    // the accumulator buffer is free once all 32 lanes have read it
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (CG == 1) mbar_arrive(&tempty[b]);
+                        else mbar_arrive_remote(mapa_shared(smem_addr(&tempty[b]), 0));
+                    }
+                }
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
+                if (!in) continue;
+                if (use_c) {
+                    ok = __all_sync(0xffffffffu, W.wait(&cb[cur], (ec >> 1) & 1u));
+                    if (!ok) break;
+                    // row `lane` of the 128-byte-swizzled fp32 box: 16-byte chunk c at (c ^ (row % 8))
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float4 cv = *reinterpret_cast<const float4 *>(buf + lane * 128 + ((c ^ (lane & 7)) << 4));
+                        v[4 * c + 0] += cv.x;
+                        v[4 * c + 1] += cv.y;
+                        v[4 * c + 2] += cv.z;
+                        v[4 * c + 3] += cv.w;
+                    }
+                } else if (lane == 0) {
+                    bulk_wait_group_read1();              // the store two boxes back has read this buffer
+                }
+                __syncwarp();
+                if constexpr (Cfg::OUT_BF16) {
+                    // 64-byte rows, 64-byte swizzle: chunk c at (c ^ ((row / 2) % 4))
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 w;
+                        w.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+                        w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+                        w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+                        w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+                        *reinterpret_cast<uint4 *>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = w;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<float4 *>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                            make_float4(v[4 * c + 0], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&tmD, smem_addr(buf), n_tile + EPI_COLS * j, m_warp);
+                    bulk_commit_group();
+                }
+                ++ec;
+            }
+            if (!ok) break;
+        }
+        if (lane == 0) bulk_wait_group0();
+    }
+
+    // ----------------------------------------------------------------- teardown
+    __syncwarp();
+    if (*abort_flag) {
+        // give copies that were already in flight time to land before the
+        // shared memory they target is released
+        for (int i = 0; i < 64; ++i) __nanosleep(1000);
+    }
+    tc_fence_before_sync();
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc<CG>(tmem_base, 512);
+    }
+}
+
+// Launch with a cluster of Cfg::CG CTAs.
+template <class Cfg>
+cudaError_t launch_tc(const LaunchShape &shape, const CUtensorMap *maps, const KParams &p, cudaStream_t stream) {
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute attr[1];
+    lc.gridDim = dim3(shape.grid, 1, 1);
+    lc.blockDim = dim3(192, 1, 1);
+    lc.dynamicSmemBytes = shape.smem;
+    lc.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = shape.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    void *args[5] = {(void *)&maps[0], (void *)&maps[1], (void *)&maps[2], (void *)&maps[3], (void *)&p};
+    return cudaLaunchKernelExC(&lc, reinterpret_cast<const void *>(&gemm_tc_kernel<Cfg>), args);
+}
+
+template <class Cfg>
+cudaError_t prepare_tc() {
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(&gemm_tc_kernel<Cfg>),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+}
+
+template <class Cfg>
+cudaError_t max_active_clusters_tc(int *clusters) {
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute attr[1];
+    lc.gridDim = dim3(2 * 1024, 1, 1);
+    lc.blockDim = dim3(192, 1, 1);
+    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = Cfg::CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters, reinterpret_cast<const void *>(&gemm_tc_kernel<Cfg>), &lc);
+}
+
+}  // namespace gb300

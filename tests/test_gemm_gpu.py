@@ -15,6 +15,7 @@ W = synth.WORKLOADS
 BF16_UNI = W["bf16_4096x4096x4096_f32out"]
 F16_NORM = W["f16_4000x3000x2056_f32out"]
 BF16_OUT = W["bf16_8192x8192x8192_bf16out"]
+MXF8 = W["mxf8e4m3_8192x8192x8192_c0_f32out"]
 
 FORCE = {"1cta": gemm.GEMM_FLAG_FORCE_1CTA, "2cta": gemm.GEMM_FLAG_FORCE_2CTA}
 
@@ -88,8 +89,31 @@ def test_repeated_runs_identical():
     assert np.array_equal(D1, D3)
 
 
+@pytest.mark.parametrize("M,N,K,d,c", [
+    (640, 448, 512, "f32", "zero"),      # two whole 128 x 224 tiles across, 4 k-blocks
+    (1000, 600, 528, "f32", "normal"),   # ragged M, N; K = 4 k-blocks + 16 (last scale block partial)
+    (300, 232, 96, "bf16", "normal"),    # bf16 D; one k-block, 3 scale blocks
+    (129, 8, 32, "f32", "zero"),         # one scale block
+])
+def test_block_scaled_small(M, N, K, d, c):
+    """e4m3 x e4m3 with one UE8M0 scale per 32 K, distinct per (row, block): a wrong
+    scale byte or block shows as errors of up to 2^8."""
+    w = synth.scaled(MXF8, M, N, K, d=d, c=c)
+    x, D, info, st, intact = gpucase.run(w, guard=512)
+    assert st == gemm.GEMM_OK and intact
+    assert info["tile_n"] == 224 and info["launches_per_run"] == 2
+    gpucase.check_full(w, x, D)
+
+
+def test_block_scaled_c_null():
+    w = synth.scaled(MXF8, 384, 480, 256, c="normal")
+    x, D, info, st, intact = gpucase.run(w, c_none=True, guard=512)
+    assert st == gemm.GEMM_OK and intact
+    gpucase.check_full(w, x, D, c_none=True)
+
+
 @pytest.mark.parametrize("name", ["bf16_4096x4096x4096_f32out", "f16_4000x3000x2056_f32out",
-                                  "bf16_8192x8192x8192_bf16out"])
+                                  "bf16_8192x8192x8192_bf16out", "mxf8e4m3_8192x8192x8192_c0_f32out"])
 def test_full_size_sampled(name):
     w = W[name]
     x, D, info, st, intact = gpucase.run(w, guard=4096)
