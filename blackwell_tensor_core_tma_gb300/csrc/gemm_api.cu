@@ -19,6 +19,14 @@
 
 using namespace gb300;
 
+// M tiles per rasterisation group (tuning knobs)
+#ifndef GB300_GROUP_M_PAIRS
+#define GB300_GROUP_M_PAIRS 8
+#endif
+#ifndef GB300_GROUP_M_SINGLE
+#define GB300_GROUP_M_SINGLE 16
+#endif
+
 struct gemm_plan {
     int64_t M, N, K;
     gemm_dtype ab, c, d;
@@ -44,7 +52,7 @@ struct gemm_plan {
     uint8_t *hSFA, *hSFB;
     // tensor maps of the last run, reused while the pointers repeat
     const void *lastA, *lastB, *lastC, *lastD;
-    CUtensorMap maps[4];
+    CUtensorMap maps[NUM_MAPS];   // A, B, C, D, packed SFA, packed SFB
     bool maps_valid;
 };
 
@@ -93,7 +101,7 @@ CUtensorMapDataType tma_dtype(gemm_dtype t) {
 gemm_status encode_maps(gemm_plan *p, const void *A, const void *B, const void *C, void *D) {
     if (p->maps_valid && A == p->lastA && B == p->lastB && C == p->lastC && D == p->lastD) return GEMM_OK;
     if (!encoder()) return GEMM_ERR_CUDA;
-    std::memset(p->maps, 0, sizeof p->maps);
+    std::memset(p->maps, 0, 4 * sizeof(CUtensorMap));     // the scale-factor maps stay
     const int eb = elem_bytes(p->ab);
     const uint32_t bk = 128u / (uint32_t)eb;                       // K elements in a 128-byte row
     const uint32_t b_rows = (uint32_t)(p->tile_n / p->cta_group);
@@ -145,31 +153,49 @@ gemm_status configure_f16(gemm_plan *p) {
         if (f16_max_active_clusters(cfg, &clusters) == cudaSuccess && clusters > 0) units = clusters;
     }
     p->grid = cg * (p->tiles < units ? p->tiles : units);
-    p->group_m = cg == 2 ? 8 : 16;
+    p->group_m = cg == 2 ? GB300_GROUP_M_PAIRS : GB300_GROUP_M_SINGLE;
     return GEMM_OK;
 }
 
 gemm_status configure_mxf8(gemm_plan *p) {
-    if (p->flags & GEMM_FLAG_FORCE_2CTA) return GEMM_ERR_UNSUPPORTED;
-    if (mxf8_prepare(p->d == GEMM_BF16) != cudaSuccess) return GEMM_ERR_CUDA;
+    int cg = (p->M >= 1024 && p->N >= 1024) ? 2 : 1;
+    if (p->flags & GEMM_FLAG_FORCE_1CTA) cg = 1;
+    if (p->flags & GEMM_FLAG_FORCE_2CTA) cg = 2;
+    const int bf = p->d == GEMM_BF16;
+    if (mxf8_prepare(cg, bf) != cudaSuccess) return GEMM_ERR_CUDA;
     p->family = 1;
-    p->cta_group = 1;
+    p->cta_group = cg;
     p->tile_n = MXF8_TILE_N;
-    p->stages = mxf8_stages();
-    p->smem = mxf8_smem_bytes();
+    p->stages = mxf8_stages(cg);
+    p->smem = mxf8_smem_bytes(cg);
     p->num_kb = (int)((p->K + 127) / 128);
-    p->tiles_m = (int)((p->M + TILE_M - 1) / TILE_M);
+    p->tiles_m = (int)((p->M + TILE_M * cg - 1) / (TILE_M * cg));
     p->tiles_n = (int)((p->N + MXF8_TILE_N - 1) / MXF8_TILE_N);
     p->tiles = p->tiles_m * p->tiles_n;
-    p->grid = p->tiles < p->sm_count ? p->tiles : p->sm_count;
-    p->group_m = 16;
-    if (cudaMalloc(&p->ws_a, mxf8_workspace_a(p->tiles_m, p->num_kb)) != cudaSuccess ||
-        cudaMalloc(&p->ws_b, mxf8_workspace_b(p->tiles_n, p->num_kb)) != cudaSuccess) {
+    int units = p->sm_count / cg;
+    if (cg == 2) {
+        int clusters = 0;
+        if (mxf8_max_active_clusters(cg, bf, &clusters) == cudaSuccess && clusters > 0) units = clusters;
+    }
+    p->grid = cg * (p->tiles < units ? p->tiles : units);
+    p->group_m = cg == 2 ? GB300_GROUP_M_PAIRS : GB300_GROUP_M_SINGLE;
+    // workspace: one 512-byte SFA block per (128 rows, 128 K), one SFB block per (tile column, 128 K)
+    const int row_blocks = p->tiles_m * cg;
+    const size_t a_bytes = mxf8_workspace_a(row_blocks, p->num_kb);
+    const size_t b_bytes = mxf8_workspace_b(p->tiles_n, p->num_kb);
+    if (cudaMalloc(&p->ws_a, a_bytes) != cudaSuccess || cudaMalloc(&p->ws_b, b_bytes) != cudaSuccess) {
         cudaFree(p->ws_a);
         cudaFree(p->ws_b);
         p->ws_a = p->ws_b = nullptr;
         return GEMM_ERR_CUDA;
     }
+    if (!encoder()) return GEMM_ERR_CUDA;
+    const uint32_t b_block_rows = (uint32_t)(mxf8_sfb_block_bytes() / 128);
+    if (!encode_2d(&p->maps[4], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p->ws_a, 128, a_bytes / 128, 128, 4,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&p->maps[5], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p->ws_b, 128, b_bytes / 128, 128, b_block_rows,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+        return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
 
@@ -262,13 +288,14 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
     kp.fault = p->fault;
     LaunchShape shape{p->grid, p->cta_group, p->smem};
     if (p->family == 1) {
-        kp.idesc = idesc_mxf8((uint32_t)TILE_M, (uint32_t)MXF8_TILE_N, 0, 0);
+        kp.idesc = idesc_mxf8((uint32_t)(TILE_M * p->cta_group), (uint32_t)MXF8_TILE_N, 0, 0);
         kp.sfa = p->ws_a;
         kp.sfb = p->ws_b;
-        if (mxf8_pack(SFA, SFB, p->ws_a, p->ws_b, kp.M, kp.N, kp.K, p->tiles_m, p->tiles_n, p->num_kb, p->sm_count,
-                      stream) != cudaSuccess)
+        if (mxf8_pack(SFA, SFB, p->ws_a, p->ws_b, kp.M, kp.N, kp.K, p->tiles_m * p->cta_group, p->tiles_n, p->num_kb,
+                      p->sm_count, stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
-        if (mxf8_launch(p->d == GEMM_BF16, shape, p->maps, kp, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (mxf8_launch(p->cta_group, p->d == GEMM_BF16, shape, p->maps, kp, stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
     } else {
         kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * p->cta_group), (uint32_t)TILE_N);
         F16Config cfg{p->cta_group, p->d == GEMM_BF16};

@@ -4,11 +4,19 @@
 // each with fp32 or bf16 D.
 #include "gemm_kernel.cuh"
 
+// ring depths (tuning knobs; the defaults fill shared memory)
+#ifndef GB300_F16_CG1_STAGES
+#define GB300_F16_CG1_STAGES 4
+#endif
+#ifndef GB300_F16_CG2_STAGES
+#define GB300_F16_CG2_STAGES 6
+#endif
+
 namespace gb300 {
 namespace {
 
 template <int CG, bool OUT_BF16>
-using F16Cfg = TileCfg<CG, OUT_BF16, false, TILE_N, CG == 1 ? 4 : 6>;
+using F16Cfg = TileCfg<CG, OUT_BF16, false, TILE_N, CG == 1 ? GB300_F16_CG1_STAGES : GB300_F16_CG2_STAGES>;
 
 }  // namespace
 

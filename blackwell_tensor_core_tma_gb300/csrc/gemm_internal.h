@@ -5,7 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "../../include/gb300gemm.h"
+#include "gb300gemm.h"
 
 namespace gb300 {
 
@@ -23,6 +23,9 @@ struct KParams {
     const uint8_t *sfa;  // block-scaled: packed scale factors (device)
     const uint8_t *sfb;
 };
+
+// Tensor maps a kernel takes: A, B, C, D, and the packed scale factors (block-scaled only).
+constexpr int NUM_MAPS = 6;
 
 // A launch: grid, cluster width and dynamic shared memory.
 struct LaunchShape {
@@ -43,17 +46,19 @@ cudaError_t f16_max_active_clusters(const F16Config &cfg, int *clusters);
 cudaError_t f16_launch(const F16Config &cfg, const LaunchShape &shape, const CUtensorMap *maps,
                        const KParams &p, cudaStream_t stream);
 
-// block-scaled e4m3 kernel family (gemm_mxf8.cu): single CTAs, 128 x MXF8_TILE_N tiles
+// block-scaled e4m3 kernel family (gemm_mxf8.cu): 128 x MXF8_TILE_N tiles per CTA
 constexpr int MXF8_TILE_N = 224;
-int mxf8_stages();
-int mxf8_smem_bytes();
-size_t mxf8_workspace_a(int tiles_m, int num_kb);
+int mxf8_stages(int cta_group);
+int mxf8_smem_bytes(int cta_group);
+size_t mxf8_workspace_a(int row_blocks, int num_kb);
 size_t mxf8_workspace_b(int tiles_n, int num_kb);
-cudaError_t mxf8_prepare(int out_bf16);
+int mxf8_sfb_block_bytes();
+cudaError_t mxf8_prepare(int cta_group, int out_bf16);
+cudaError_t mxf8_max_active_clusters(int cta_group, int out_bf16, int *clusters);
 cudaError_t mxf8_pack(const uint8_t *sfa, const uint8_t *sfb, uint8_t *out_a, uint8_t *out_b, int M, int N, int K,
                       int tiles_m, int tiles_n, int num_kb, int sm_count, cudaStream_t stream);
-cudaError_t mxf8_launch(int out_bf16, const LaunchShape &shape, const CUtensorMap *maps, const KParams &p,
-                        cudaStream_t stream);
+cudaError_t mxf8_launch(int cta_group, int out_bf16, const LaunchShape &shape, const CUtensorMap *maps,
+                        const KParams &p, cudaStream_t stream);
 
 constexpr int TILE_M = 128;   // rows of D per CTA
 constexpr int TILE_N = 256;   // columns of D per CTA (and per CTA pair)

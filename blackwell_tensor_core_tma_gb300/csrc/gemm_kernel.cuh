@@ -57,31 +57,35 @@ struct TileCfg {
     static constexpr int A_BYTES = TILE_M * 128;                // 16 KiB
     static constexpr int B_ROWS = BN / CG;                      // B rows held by one CTA
     static constexpr int B_BYTES = B_ROWS * 128;
+    // scales of one stage in one CTA: SFA of its 128 rows, SFB of all BN columns of the
+    // tile (each CTA of a pair computes every column of its rows); 512 bytes per 128 rows
     static constexpr int SFA_BYTES = SCALED ? 512 : 0;          // 128 rows x 4 K-blocks of 32
     static constexpr int SFB_BYTES = SCALED ? 512 * ((BN + 127) / 128) : 0;
-    static constexpr int TX_BYTES = CG * (A_BYTES + B_BYTES) + SFA_BYTES + SFB_BYTES;
+    static constexpr int TX_BYTES = CG * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES);
     static constexpr int EPI_BUF = 32 * EPI_COLS * 4;           // one 32 x 32 fp32 box
+    // Every region a swizzled TMA copy or a swizzled MMA descriptor addresses
+    // starts on a 1024-byte boundary: the 128-byte swizzle permutes 16-byte
+    // chunks by address bits 7..9, so an offset of 512 would shift the row phase.
+    static constexpr int align1k(int x) { return (x + 1023) / 1024 * 1024; }
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_EPI = OFF_SF + STAGES * (SFA_BYTES + SFB_BYTES);
+    static constexpr int OFF_EPI = align1k(OFF_SF + STAGES * (SFA_BYTES + SFB_BYTES));
     static constexpr int OFF_BAR = OFF_EPI + 4 * 2 * EPI_BUF;
+    static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && OFF_B % 1024 == 0, "operand stages 1024-aligned");
+    static_assert(OFF_EPI % 1024 == 0 && EPI_BUF % 1024 == 0, "epilogue staging 1024-aligned");
     // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], cload[4 warps][2], drain
     static constexpr int NBAR = 2 * STAGES + 2 + 2 + 8 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base slot, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
-    // TMEM columns: accumulators [0, 2*BN), then one SFB slot (4 columns per
-    // 128 rows of B) and one SFA slot (4 columns, padded to 8) per stage; every
-    // slot starts on a multiple of 8 columns
-    static constexpr int SFB_COLS = SCALED ? 4 * ((BN + 127) / 128) : 0;
-    static constexpr int SFA_COLS = SCALED ? 8 : 0;
-    static constexpr int SFB_COL0 = 2 * BN;
-    static constexpr int SFA_COL0 = SFB_COL0 + STAGES * SFB_COLS;
-    static_assert(2 * BN + STAGES * (SFB_COLS + SFA_COLS) <= 512, "TMEM budget");
-    static_assert(!SCALED || (SFB_COL0 % 8 == 0 && SFB_COLS % 8 == 0), "scale slots on 8-column boundaries");
+    // TMEM columns: accumulators [0, 2*BN), then one scale slot per stage: SFA in
+    // 4 columns, SFB in 4 columns per 128 rows of B.  A slot is reused only when
+    // its stage is refilled, i.e. after the MMAs that read it have completed.
+    static constexpr int SF_SLOT = SCALED ? 4 + 4 * ((BN + 127) / 128) : 0;
+    static constexpr int SF_COL0 = 2 * BN;
+    static_assert(2 * BN + STAGES * SF_SLOT <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
     static_assert(BN % EPI_COLS == 0 && BN % 16 == 0 && BN <= 256, "tile N");
-    static_assert(!SCALED || CG == 1, "block-scaled tiles use single CTAs");
 };
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int group_m, int &tm, int &tn, int tiles_n) {
@@ -131,6 +135,7 @@ template <class Cfg>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                   const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                    const KParams p) {
     constexpr int CG = Cfg::CG;
     constexpr int STAGES = Cfg::STAGES;
@@ -160,6 +165,10 @@ __global__ void __launch_bounds__(192, 1)
         prefetch_tensormap(&tmB);
         if (p.has_c) prefetch_tensormap(&tmC);
         prefetch_tensormap(&tmD);
+        if constexpr (Cfg::SCALED) {
+            prefetch_tensormap(&tmSFA);
+            prefetch_tensormap(&tmSFB);
+        }
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -203,21 +212,26 @@ __global__ void __launch_bounds__(192, 1)
                     const uint32_t a_dst = smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES);
                     const uint32_t b_dst = smem_addr(smem + Cfg::OFF_B + s * Cfg::B_BYTES);
                     const uint32_t fb = smem_addr(&full[s]);
+                    // packed scale factors of this (128-row block, k-block) and (tile column, k-block):
+                    // 512-byte blocks, viewed by their tensor maps as rows of 128 bytes
+                    const uint32_t sf_dst = smem_addr(smem + Cfg::OFF_SF + s * (Cfg::SFA_BYTES + Cfg::SFB_BYTES));
+                    const int sfa_row = ((tm * CG + (int)rank) * p.num_kb + kb) * (Cfg::SFA_BYTES / 128);
+                    const int sfb_row = (tn * p.num_kb + kb) * (Cfg::SFB_BYTES / 128);
                     if constexpr (CG == 1) {
                         tma_load_2d(a_dst, &tmA, fb, kb * Cfg::BK, m0);
                         tma_load_2d(b_dst, &tmB, fb, kb * Cfg::BK, n0);
+                        if constexpr (Cfg::SCALED) {
+                            tma_load_2d(sf_dst, &tmSFA, fb, 0, sfa_row);
+                            tma_load_2d(sf_dst + Cfg::SFA_BYTES, &tmSFB, fb, 0, sfb_row);
+                        }
                     } else {
                         const uint32_t leader_fb = mapa_shared(fb, 0);
                         tma_load_2d_pair(a_dst, &tmA, leader_fb, kb * Cfg::BK, m0);
                         tma_load_2d_pair(b_dst, &tmB, leader_fb, kb * Cfg::BK, n0);
-                    }
-                    if constexpr (Cfg::SCALED) {
-                        // packed scale factors of this (tile, k-block): 512 bytes of SFA, 512 per
-                        // 128 B rows of SFB, contiguous in the workspace
-                        const uint32_t sf_dst = smem_addr(smem + Cfg::OFF_SF + s * (Cfg::SFA_BYTES + Cfg::SFB_BYTES));
-                        bulk_load(sf_dst, p.sfa + ((size_t)tm * p.num_kb + kb) * Cfg::SFA_BYTES, Cfg::SFA_BYTES, fb);
-                        bulk_load(sf_dst + Cfg::SFA_BYTES, p.sfb + ((size_t)tn * p.num_kb + kb) * Cfg::SFB_BYTES,
-                                  Cfg::SFB_BYTES, fb);
+                        if constexpr (Cfg::SCALED) {
+                            tma_load_2d_pair(sf_dst, &tmSFA, leader_fb, 0, sfa_row);
+                            tma_load_2d_pair(sf_dst + Cfg::SFA_BYTES, &tmSFB, leader_fb, 0, sfb_row);
+                        }
                     }
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
@@ -242,8 +256,8 @@ __global__ void __launch_bounds__(192, 1)
                     if constexpr (Cfg::SCALED) {
                         // stage s's scales: SFA in 4 columns, SFB in 4 per 128 rows of B,
                         // each a 32-lane x 16-byte SMEM block replicated to the 4 lane windows
-                        const uint32_t sfa_t = tmem_base + Cfg::SFA_COL0 + s * Cfg::SFA_COLS;
-                        const uint32_t sfb_t = tmem_base + Cfg::SFB_COL0 + s * Cfg::SFB_COLS;
+                        const uint32_t sfa_t = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_SLOT;
+                        const uint32_t sfb_t = sfa_t + 4;
                         const uint32_t sf_src = smem_addr(smem + Cfg::OFF_SF + s * (Cfg::SFA_BYTES + Cfg::SFB_BYTES));
                         tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc(sf_src, 512, 128, SWZ_NONE));
 #pragma unroll
@@ -401,7 +415,8 @@ cudaError_t launch_tc(const LaunchShape &shape, const CUtensorMap *maps, const K
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    void *args[5] = {(void *)&maps[0], (void *)&maps[1], (void *)&maps[2], (void *)&maps[3], (void *)&p};
+    void *args[7] = {(void *)&maps[0], (void *)&maps[1], (void *)&maps[2], (void *)&maps[3],
+                     (void *)&maps[4], (void *)&maps[5], (void *)&p};
     return cudaLaunchKernelExC(&lc, reinterpret_cast<const void *>(&gemm_tc_kernel<Cfg>), args);
 }
 

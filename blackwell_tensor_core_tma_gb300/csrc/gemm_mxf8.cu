@@ -16,19 +16,24 @@
 // sf_pack_kernel writes the caller's row-major SFA (M x SFK) and SFB (N x SFK)
 // in exactly that order into the plan's workspace, one 512-byte block per
 // (128-row block, k-block of 128 elements), so that the producer copies a
-// stage's scales with one contiguous bulk copy.  Rows or K blocks past the
+// stage's scales with one TMA copy per operand (the workspace is viewed as
+// rows of 128 bytes).  Rows or K blocks past the
 // matrix get scale code 127 (2^0): they multiply the zero-filled operand
 // elements of the edge tiles.
 //
-// Tiles are 128 x 224: two 224-column fp32 accumulators (448 TMEM columns)
-// leave 64 columns for four stages of scales (4 SFA + 8 SFB columns each).
+// Tiles are 128 x 224 per CTA (256 x 224 per CTA pair): two 224-column fp32
+// accumulators (448 TMEM columns) leave 64 columns for the stages' scales
+// (4 SFA + 8 SFB columns each).  In a CTA pair each CTA holds the SFA of its
+// own 128 rows and the SFB of all 224 columns.
 #include "gemm_kernel.cuh"
 
 namespace gb300 {
 namespace {
 
-template <bool OUT_BF16>
-using MxCfg = TileCfg<1, OUT_BF16, true, MXF8_TILE_N, 4>;
+// single CTAs: 4 stages fill shared memory; pairs (half of B per CTA): 5 stages,
+// which with 12-column scale slots fill TMEM (448 + 5 * 12 = 508 columns)
+template <int CG, bool OUT_BF16>
+using MxCfg = TileCfg<CG, OUT_BF16, true, MXF8_TILE_N, CG == 1 ? 4 : 5>;
 
 constexpr uint8_t kUnitScale = 127;
 
@@ -83,16 +88,29 @@ __global__ void sf_pack_kernel(const uint8_t *__restrict__ sfa, const uint8_t *_
 
 }  // namespace
 
-int mxf8_stages() { return MxCfg<false>::STAGES; }
+int mxf8_stages(int cta_group) { return cta_group == 1 ? MxCfg<1, false>::STAGES : MxCfg<2, false>::STAGES; }
 
-int mxf8_smem_bytes() { return MxCfg<false>::SMEM_BYTES; }
+int mxf8_smem_bytes(int cta_group) {
+    return cta_group == 1 ? MxCfg<1, false>::SMEM_BYTES : MxCfg<2, false>::SMEM_BYTES;
+}
 
-size_t mxf8_workspace_a(int tiles_m, int num_kb) { return (size_t)tiles_m * num_kb * MxCfg<false>::SFA_BYTES; }
+size_t mxf8_workspace_a(int row_blocks, int num_kb) { return (size_t)row_blocks * num_kb * MxCfg<1, false>::SFA_BYTES; }
 
-size_t mxf8_workspace_b(int tiles_n, int num_kb) { return (size_t)tiles_n * num_kb * MxCfg<false>::SFB_BYTES; }
+size_t mxf8_workspace_b(int tiles_n, int num_kb) { return (size_t)tiles_n * num_kb * MxCfg<1, false>::SFB_BYTES; }
 
-cudaError_t mxf8_prepare(int out_bf16) {
-    return out_bf16 ? prepare_tc<MxCfg<true>>() : prepare_tc<MxCfg<false>>();
+int mxf8_sfb_block_bytes() { return MxCfg<1, false>::SFB_BYTES; }
+
+cudaError_t mxf8_prepare(int cta_group, int out_bf16) {
+    if (cta_group == 1) return out_bf16 ? prepare_tc<MxCfg<1, true>>() : prepare_tc<MxCfg<1, false>>();
+    return out_bf16 ? prepare_tc<MxCfg<2, true>>() : prepare_tc<MxCfg<2, false>>();
+}
+
+cudaError_t mxf8_max_active_clusters(int cta_group, int out_bf16, int *clusters) {
+    if (cta_group == 1)
+        return out_bf16 ? max_active_clusters_tc<MxCfg<1, true>>(clusters)
+                        : max_active_clusters_tc<MxCfg<1, false>>(clusters);
+    return out_bf16 ? max_active_clusters_tc<MxCfg<2, true>>(clusters)
+                    : max_active_clusters_tc<MxCfg<2, false>>(clusters);
 }
 
 cudaError_t mxf8_pack(const uint8_t *sfa, const uint8_t *sfb, uint8_t *out_a, uint8_t *out_b, int M, int N, int K,
@@ -106,9 +124,13 @@ cudaError_t mxf8_pack(const uint8_t *sfa, const uint8_t *sfb, uint8_t *out_a, ui
     return cudaGetLastError();
 }
 
-cudaError_t mxf8_launch(int out_bf16, const LaunchShape &shape, const CUtensorMap *maps, const KParams &p,
-                        cudaStream_t stream) {
-    return out_bf16 ? launch_tc<MxCfg<true>>(shape, maps, p, stream) : launch_tc<MxCfg<false>>(shape, maps, p, stream);
+cudaError_t mxf8_launch(int cta_group, int out_bf16, const LaunchShape &shape, const CUtensorMap *maps,
+                        const KParams &p, cudaStream_t stream) {
+    if (cta_group == 1)
+        return out_bf16 ? launch_tc<MxCfg<1, true>>(shape, maps, p, stream)
+                        : launch_tc<MxCfg<1, false>>(shape, maps, p, stream);
+    return out_bf16 ? launch_tc<MxCfg<2, true>>(shape, maps, p, stream)
+                    : launch_tc<MxCfg<2, false>>(shape, maps, p, stream);
 }
 
 }  // namespace gb300

@@ -106,7 +106,7 @@ extern "C" gemm_status gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dt
     // same kernel choice as a plan without flags
     const int cg = (M >= 1024 && N >= 1024) ? 2 : 1;
     const F16Config cfg{cg, d == GEMM_BF16};
-    CUtensorMap maps[4];
+    CUtensorMap maps[NUM_MAPS];
     std::memset(maps, 0, sizeof maps);
     const CUtensorMapDataType abt = ab == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     bool ok = encode(&maps[0], abt, 2, A, K, M, TILE_K16, TILE_M, CU_TENSOR_MAP_SWIZZLE_128B) &&

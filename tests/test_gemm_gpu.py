@@ -95,13 +95,15 @@ def test_repeated_runs_identical():
     (300, 232, 96, "bf16", "normal"),    # bf16 D; one k-block, 3 scale blocks
     (129, 8, 32, "f32", "zero"),         # one scale block
 ])
-def test_block_scaled_small(M, N, K, d, c):
+@pytest.mark.parametrize("variant", ["1cta", "2cta"])
+def test_block_scaled_small(variant, M, N, K, d, c):
     """e4m3 x e4m3 with one UE8M0 scale per 32 K, distinct per (row, block): a wrong
     scale byte or block shows as errors of up to 2^8."""
     w = synth.scaled(MXF8, M, N, K, d=d, c=c)
-    x, D, info, st, intact = gpucase.run(w, guard=512)
+    x, D, info, st, intact = gpucase.run(w, flags=FORCE[variant], guard=512)
     assert st == gemm.GEMM_OK and intact
     assert info["tile_n"] == 224 and info["launches_per_run"] == 2
+    assert info["cta_group"] == (1 if variant == "1cta" else 2)
     gpucase.check_full(w, x, D)
 
 
