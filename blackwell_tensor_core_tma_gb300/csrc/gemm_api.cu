@@ -165,12 +165,12 @@ gemm_status configure_mxf8(gemm_plan *p) {
     if (mxf8_prepare(cg, bf) != cudaSuccess) return GEMM_ERR_CUDA;
     p->family = 1;
     p->cta_group = cg;
-    p->tile_n = MXF8_TILE_N;
+    p->tile_n = mxf8_tile_n(cg);
     p->stages = mxf8_stages(cg);
     p->smem = mxf8_smem_bytes(cg);
     p->num_kb = (int)((p->K + 127) / 128);
     p->tiles_m = (int)((p->M + TILE_M * cg - 1) / (TILE_M * cg));
-    p->tiles_n = (int)((p->N + MXF8_TILE_N - 1) / MXF8_TILE_N);
+    p->tiles_n = (int)((p->N + p->tile_n - 1) / p->tile_n);
     p->tiles = p->tiles_m * p->tiles_n;
     int units = p->sm_count / cg;
     if (cg == 2) {
@@ -288,11 +288,11 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
     kp.fault = p->fault;
     LaunchShape shape{p->grid, p->cta_group, p->smem};
     if (p->family == 1) {
-        kp.idesc = idesc_mxf8((uint32_t)(TILE_M * p->cta_group), (uint32_t)MXF8_TILE_N, 0, 0);
+        kp.idesc = idesc_mxf8((uint32_t)(TILE_M * p->cta_group), (uint32_t)p->tile_n, 0, 0);
         kp.sfa = p->ws_a;
         kp.sfb = p->ws_b;
-        if (mxf8_pack(SFA, SFB, p->ws_a, p->ws_b, kp.M, kp.N, kp.K, p->tiles_m * p->cta_group, p->tiles_n, p->num_kb,
-                      p->sm_count, stream) != cudaSuccess)
+        if (mxf8_pack(SFA, SFB, p->ws_a, p->ws_b, kp.M, kp.N, kp.K, p->tiles_m * p->cta_group, p->tiles_n, p->tile_n,
+                      p->num_kb, p->sm_count, stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
         if (mxf8_launch(p->cta_group, p->d == GEMM_BF16, shape, p->maps, kp, stream) != cudaSuccess)
             return GEMM_ERR_CUDA;

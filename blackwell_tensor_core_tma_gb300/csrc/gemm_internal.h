@@ -46,8 +46,8 @@ cudaError_t f16_max_active_clusters(const F16Config &cfg, int *clusters);
 cudaError_t f16_launch(const F16Config &cfg, const LaunchShape &shape, const CUtensorMap *maps,
                        const KParams &p, cudaStream_t stream);
 
-// block-scaled e4m3 kernel family (gemm_mxf8.cu): 128 x MXF8_TILE_N tiles per CTA
-constexpr int MXF8_TILE_N = 224;
+// block-scaled e4m3 kernel family (gemm_mxf8.cu)
+int mxf8_tile_n(int cta_group);
 int mxf8_stages(int cta_group);
 int mxf8_smem_bytes(int cta_group);
 size_t mxf8_workspace_a(int row_blocks, int num_kb);
@@ -56,7 +56,7 @@ int mxf8_sfb_block_bytes();
 cudaError_t mxf8_prepare(int cta_group, int out_bf16);
 cudaError_t mxf8_max_active_clusters(int cta_group, int out_bf16, int *clusters);
 cudaError_t mxf8_pack(const uint8_t *sfa, const uint8_t *sfb, uint8_t *out_a, uint8_t *out_b, int M, int N, int K,
-                      int tiles_m, int tiles_n, int num_kb, int sm_count, cudaStream_t stream);
+                      int row_blocks, int tiles_n, int tile_n, int num_kb, int sm_count, cudaStream_t stream);
 cudaError_t mxf8_launch(int cta_group, int out_bf16, const LaunchShape &shape, const CUtensorMap *maps,
                         const KParams &p, cudaStream_t stream);
 

@@ -34,6 +34,11 @@
 
 #include <cstdint>
 
+// operand tiles marked evict-last in L2 (tuning knob)
+#ifndef GB300_OPERANDS_EVICT_LAST
+#define GB300_OPERANDS_EVICT_LAST 0
+#endif
+
 #include "gemm_internal.h"
 #include "ptx.cuh"
 
@@ -44,13 +49,27 @@ namespace gb300 {
 //   OUT_BF16  D is bf16 (else fp32)
 //   SCALED  block-scaled e4m3 operands (kind::mxf8f6f4, scale_vec::1X)
 //   BN      tile columns (MMA N)
-template <int CG_, bool OUT_BF16_, bool SCALED_, int BN_, int STAGES_>
+//   ACC_BUFS  TMEM accumulators: 2 = the epilogue drains one while the MMA fills
+//             the other; 1 = the epilogue copies the accumulator to registers
+//             and frees it before converting and storing (leaves TMEM columns
+//             for scale slots at N = 256)
+//   EPI_WARPS epilogue warps: 4 (one per TMEM lane window) or 8 (two per window,
+//             each taking half of the tile's columns)
+template <int CG_, bool OUT_BF16_, bool SCALED_, int BN_, int STAGES_, int ACC_BUFS_ = 2, int EPI_WARPS_ = 4>
 struct TileCfg {
     static constexpr int CG = CG_;
     static constexpr bool OUT_BF16 = OUT_BF16_;
     static constexpr bool SCALED = SCALED_;
     static constexpr int BN = BN_;
     static constexpr int STAGES = STAGES_;
+    static constexpr int ACC_BUFS = ACC_BUFS_;
+    static constexpr int EPI_WARPS = EPI_WARPS_;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int WCOLS = BN * 4 / EPI_WARPS;             // columns one epilogue warp handles
+    static constexpr int WCHUNKS = WCOLS / EPI_COLS;
+    static_assert(ACC_BUFS == 1 || ACC_BUFS == 2, "accumulator buffers");
+    static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
+    static_assert(WCOLS % EPI_COLS == 0, "epilogue columns per warp");
     static constexpr int ELEM = SCALED ? 1 : 2;                 // operand bytes
     static constexpr int BK = 128 / ELEM;                       // K elements per stage: one 128-byte row
     static constexpr int MMA_K = 32 / ELEM;                     // K per instruction: 32 bytes
@@ -71,19 +90,19 @@ struct TileCfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_EPI = align1k(OFF_SF + STAGES * (SFA_BYTES + SFB_BYTES));
-    static constexpr int OFF_BAR = OFF_EPI + 4 * 2 * EPI_BUF;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF;
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && OFF_B % 1024 == 0, "operand stages 1024-aligned");
     static_assert(OFF_EPI % 1024 == 0 && EPI_BUF % 1024 == 0, "epilogue staging 1024-aligned");
-    // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], cload[4 warps][2], drain
-    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 8 + 1;
+    // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], cload[EPI_WARPS][2], drain
+    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 * EPI_WARPS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base slot, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
     // TMEM columns: accumulators [0, 2*BN), then one scale slot per stage: SFA in
     // 4 columns, SFB in 4 columns per 128 rows of B.  A slot is reused only when
     // its stage is refilled, i.e. after the MMAs that read it have completed.
     static constexpr int SF_SLOT = SCALED ? 4 + 4 * ((BN + 127) / 128) : 0;
-    static constexpr int SF_COL0 = 2 * BN;
-    static_assert(2 * BN + STAGES * SF_SLOT <= 512, "TMEM budget");
+    static constexpr int SF_COL0 = ACC_BUFS * BN;
+    static_assert(ACC_BUFS * BN + STAGES * SF_SLOT <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
     static_assert(BN % EPI_COLS == 0 && BN % 16 == 0 && BN <= 256, "tile N");
 };
@@ -132,7 +151,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 template <class Cfg>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                    const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -140,7 +159,6 @@ __global__ void __launch_bounds__(192, 1)
     constexpr int CG = Cfg::CG;
     constexpr int STAGES = Cfg::STAGES;
     constexpr int BN = Cfg::BN;
-    constexpr int CHUNKS = BN / EPI_COLS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -155,7 +173,7 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t *tfull = bars + 2 * STAGES;
     uint64_t *tempty = tfull + 2;
     uint64_t *cload = tempty + 2;
-    uint64_t *drain = cload + 8;
+    uint64_t *drain = cload + 2 * Cfg::EPI_WARPS;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 4);
     const Waiter W{abort_flag, p.status, p.timeout_ns};
@@ -175,9 +193,9 @@ __global__ void __launch_bounds__(192, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 4 * CG);   // every epilogue warp of the pair
+            mbar_init(&tempty[b], Cfg::EPI_WARPS * CG);   // every epilogue warp of the pair
         }
-        for (int i = 0; i < 8; ++i) mbar_init(&cload[i], 1);
+        for (int i = 0; i < 2 * Cfg::EPI_WARPS; ++i) mbar_init(&cload[i], 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -200,6 +218,9 @@ __global__ void __launch_bounds__(192, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
+#if GB300_OPERANDS_EVICT_LAST
+            const uint64_t keep = l2_policy_evict_last();
+#endif
             for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
                 int tm, tn;
                 tile_coords(t, p.tiles_m, p.group_m, tm, tn, p.tiles_n);
@@ -218,16 +239,26 @@ __global__ void __launch_bounds__(192, 1)
                     const int sfa_row = ((tm * CG + (int)rank) * p.num_kb + kb) * (Cfg::SFA_BYTES / 128);
                     const int sfb_row = (tn * p.num_kb + kb) * (Cfg::SFB_BYTES / 128);
                     if constexpr (CG == 1) {
+#if GB300_OPERANDS_EVICT_LAST
+                        tma_load_2d_hint(a_dst, &tmA, fb, kb * Cfg::BK, m0, keep);
+                        tma_load_2d_hint(b_dst, &tmB, fb, kb * Cfg::BK, n0, keep);
+#else
                         tma_load_2d(a_dst, &tmA, fb, kb * Cfg::BK, m0);
                         tma_load_2d(b_dst, &tmB, fb, kb * Cfg::BK, n0);
+#endif
                         if constexpr (Cfg::SCALED) {
                             tma_load_2d(sf_dst, &tmSFA, fb, 0, sfa_row);
                             tma_load_2d(sf_dst + Cfg::SFA_BYTES, &tmSFB, fb, 0, sfb_row);
                         }
                     } else {
                         const uint32_t leader_fb = mapa_shared(fb, 0);
+#if GB300_OPERANDS_EVICT_LAST
+                        tma_load_2d_pair_hint(a_dst, &tmA, leader_fb, kb * Cfg::BK, m0, keep);
+                        tma_load_2d_pair_hint(b_dst, &tmB, leader_fb, kb * Cfg::BK, n0, keep);
+#else
                         tma_load_2d_pair(a_dst, &tmA, leader_fb, kb * Cfg::BK, m0);
                         tma_load_2d_pair(b_dst, &tmB, leader_fb, kb * Cfg::BK, n0);
+#endif
                         if constexpr (Cfg::SCALED) {
                             tma_load_2d_pair(sf_dst, &tmSFA, leader_fb, 0, sfa_row);
                             tma_load_2d_pair(sf_dst + Cfg::SFA_BYTES, &tmSFB, leader_fb, 0, sfb_row);
@@ -244,7 +275,8 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t ph = 0, acc_it = 0;
             bool ok = true;
             for (int t = tile0; ok && t < p.num_tiles; t += tile_step, ++acc_it) {
-                const uint32_t b = acc_it & 1u, aph = (acc_it >> 1) & 1u;
+                const uint32_t b = Cfg::ACC_BUFS == 2 ? (acc_it & 1u) : 0u;
+                const uint32_t aph = Cfg::ACC_BUFS == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
                 if (!W.wait(&tempty[b], aph ^ 1u)) { ok = false; break; }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * BN;
@@ -288,60 +320,63 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        const int e = warp - 2;                           // epilogue warp index
         const int q = warp & 3;                           // TMEM lane window of this warp
-        uint8_t *ebuf = smem + Cfg::OFF_EPI + q * 2 * Cfg::EPI_BUF;
-        uint64_t *cb = cload + 2 * q;
+        const int h = e / 4;                              // which WCOLS-wide column slice of the tile
+        uint8_t *ebuf = smem + Cfg::OFF_EPI + e * 2 * Cfg::EPI_BUF;
+        uint64_t *cb = cload + 2 * e;
+        // C is read once and D written once: let them leave L2 before the operand tiles
+        const uint64_t stream_pol = l2_policy_evict_first();
         // ec counts the 32 x 32 boxes this warp has stored; box ec uses staging
         // buffer ec % 2, and its C load is that buffer's (ec / 2)-th
         uint32_t acc_it = 0, ec = 0;
-        for (int t = tile0; t < p.num_tiles; t += tile_step, ++acc_it) {
+        bool ok = true;
+        for (int t = tile0; ok && t < p.num_tiles; t += tile_step, ++acc_it) {
             int tm, tn;
             tile_coords(t, p.tiles_m, p.group_m, tm, tn, p.tiles_n);
-            const uint32_t b = acc_it & 1u, aph = (acc_it >> 1) & 1u;
-            if (!__all_sync(0xffffffffu, W.wait(&tfull[b], aph))) break;
-            tc_fence_after_sync();
+            const uint32_t b = Cfg::ACC_BUFS == 2 ? (acc_it & 1u) : 0u;
+            const uint32_t aph = Cfg::ACC_BUFS == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
             const int m_warp = tm * TILE_M * CG + (int)rank * TILE_M + 32 * q;
-            const int n_tile = tn * BN;
+            const int n_warp = tn * BN + h * Cfg::WCOLS;
             // 32 x 32 boxes that lie wholly outside D are neither loaded nor stored
-            const bool rows_in = m_warp < p.M;
-            const int chunks_in = rows_in ? min(CHUNKS, (p.N - n_tile + EPI_COLS - 1) / EPI_COLS) : 0;
+            const int chunks_in = m_warp < p.M ? max(0, min(Cfg::WCHUNKS, (p.N - n_warp + EPI_COLS - 1) / EPI_COLS)) : 0;
             const bool use_c = p.has_c && chunks_in > 0;
-            if (use_c && lane == 0) {
+            if (use_c && lane == 0) {      // the tile's first C box loads while its accumulator is computed
                 bulk_wait_group_read0();
                 mbar_arrive_expect_tx(&cb[ec & 1u], Cfg::EPI_BUF);
-                tma_load_2d(smem_addr(ebuf + (ec & 1u) * Cfg::EPI_BUF), &tmC, smem_addr(&cb[ec & 1u]), n_tile, m_warp);
+                tma_load_2d_hint(smem_addr(ebuf + (ec & 1u) * Cfg::EPI_BUF), &tmC, smem_addr(&cb[ec & 1u]), n_warp,
+                                 m_warp, stream_pol);
             }
-            bool ok = true;
-            for (int j = 0; j < CHUNKS; ++j) {
+            if (!__all_sync(0xffffffffu, W.wait(&tfull[b], aph))) break;
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + b * BN + h * Cfg::WCOLS;
+
+            auto release_accumulator = [&]() {
+                // the accumulator is free once all 32 lanes have read it
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (CG == 1) mbar_arrive(&tempty[b]);
+                    else mbar_arrive_remote(mapa_shared(smem_addr(&tempty[b]), 0));
+                }
+            };
+            // one 32 x 32 box: add C, convert, stage in shared memory, TMA-store
+            auto store_box = [&](int j, const uint32_t (&acc)[32]) -> bool {
                 const uint32_t cur = ec & 1u;
                 uint8_t *buf = ebuf + cur * Cfg::EPI_BUF;
-                const bool in = j < chunks_in;
                 if (use_c && j + 1 < chunks_in && lane == 0) {
                     const uint32_t nx = cur ^ 1u;
                     bulk_wait_group_read0();              // the store from buffer nx has read it
                     mbar_arrive_expect_tx(&cb[nx], Cfg::EPI_BUF);
-                    tma_load_2d(smem_addr(ebuf + nx * Cfg::EPI_BUF), &tmC, smem_addr(&cb[nx]),
-                                n_tile + EPI_COLS * (j + 1), m_warp);
+                    tma_load_2d_hint(smem_addr(ebuf + nx * Cfg::EPI_BUF), &tmC, smem_addr(&cb[nx]),
+                                     n_warp + EPI_COLS * (j + 1), m_warp, stream_pol);
                 }
-                uint32_t acc[32];
-                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(32 * q) << 16) + b * BN + EPI_COLS * j, acc);
-                tmem_ld_wait(acc);
-                if (j == CHUNKS - 1) {
-                    // the accumulator buffer is free once all 32 lanes have read it
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (CG == 1) mbar_arrive(&tempty[b]);
-                        else mbar_arrive_remote(mapa_shared(smem_addr(&tempty[b]), 0));
-                    }
-                }
+                if (j >= chunks_in) return true;
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
-                if (!in) continue;
                 if (use_c) {
-                    ok = __all_sync(0xffffffffu, W.wait(&cb[cur], (ec >> 1) & 1u));
-                    if (!ok) break;
+                    if (!__all_sync(0xffffffffu, W.wait(&cb[cur], (ec >> 1) & 1u))) return false;
                     // row `lane` of the 128-byte-swizzled fp32 box: 16-byte chunk c at (c ^ (row % 8))
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
@@ -375,12 +410,35 @@ __global__ void __launch_bounds__(192, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(&tmD, smem_addr(buf), n_tile + EPI_COLS * j, m_warp);
+                    tma_store_2d_hint(&tmD, smem_addr(buf), n_warp + EPI_COLS * j, m_warp, stream_pol);
                     bulk_commit_group();
                 }
                 ++ec;
+                return true;
+            };
+
+            if constexpr (Cfg::ACC_BUFS == 1) {
+                // copy the whole slice to registers first so that the MMA can start the
+                // next tile while this one is converted and stored
+                uint32_t acc[Cfg::WCHUNKS][32];
+#pragma unroll
+                for (int j = 0; j < Cfg::WCHUNKS; ++j) tmem_ld_32x32b_x32(taddr + EPI_COLS * j, acc[j]);
+                tmem_ld_wait_all();
+#pragma unroll
+                for (int j = 0; j < Cfg::WCHUNKS; ++j) tie_registers(acc[j]);
+                release_accumulator();
+#pragma unroll
+                for (int j = 0; j < Cfg::WCHUNKS; ++j)
+                    if (ok) ok = store_box(j, acc[j]);
+            } else {
+                for (int j = 0; j < Cfg::WCHUNKS && ok; ++j) {
+                    uint32_t acc[32];
+                    tmem_ld_32x32b_x32(taddr + EPI_COLS * j, acc);
+                    tmem_ld_wait(acc);
+                    if (j == Cfg::WCHUNKS - 1) release_accumulator();
+                    ok = store_box(j, acc);
+                }
             }
-            if (!ok) break;
         }
         if (lane == 0) bulk_wait_group0();
     }
@@ -406,7 +464,7 @@ cudaError_t launch_tc(const LaunchShape &shape, const CUtensorMap *maps, const K
     cudaLaunchConfig_t lc = {};
     cudaLaunchAttribute attr[1];
     lc.gridDim = dim3(shape.grid, 1, 1);
-    lc.blockDim = dim3(192, 1, 1);
+    lc.blockDim = dim3(Cfg::THREADS, 1, 1);
     lc.dynamicSmemBytes = shape.smem;
     lc.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -431,7 +489,7 @@ cudaError_t max_active_clusters_tc(int *clusters) {
     cudaLaunchConfig_t lc = {};
     cudaLaunchAttribute attr[1];
     lc.gridDim = dim3(2 * 1024, 1, 1);
-    lc.blockDim = dim3(192, 1, 1);
+    lc.blockDim = dim3(Cfg::THREADS, 1, 1);
     lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = Cfg::CG;

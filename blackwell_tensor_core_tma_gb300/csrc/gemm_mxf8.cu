@@ -21,19 +21,24 @@
 // matrix get scale code 127 (2^0): they multiply the zero-filled operand
 // elements of the edge tiles.
 //
-// Tiles are 128 x 224 per CTA (256 x 224 per CTA pair): two 224-column fp32
-// accumulators (448 TMEM columns) leave 64 columns for the stages' scales
-// (4 SFA + 8 SFB columns each).  In a CTA pair each CTA holds the SFA of its
-// own 128 rows and the SFB of all 224 columns.
+// Each stage's scales take a 12-column TMEM slot (4 SFA + 8 SFB columns).  In
+// a CTA pair each CTA holds the SFA of its own 128 rows and the SFB of all the
+// tile's columns.
+#include <type_traits>
+
 #include "gemm_kernel.cuh"
 
 namespace gb300 {
 namespace {
 
-// single CTAs: 4 stages fill shared memory; pairs (half of B per CTA): 5 stages,
-// which with 12-column scale slots fill TMEM (448 + 5 * 12 = 508 columns)
+// single CTAs: 128 x 224 tiles, two accumulators (448 TMEM columns) and four
+// stages of 12-column scale slots, 4 epilogue warps.
+// CTA pairs: 256 x 256 tiles (an MMA of N = 256 keeps the tensor pipe busiest),
+// one 256-column accumulator that 8 epilogue warps copy to registers and free
+// at once, the other 256 TMEM columns for the stages' scale slots.
 template <int CG, bool OUT_BF16>
-using MxCfg = TileCfg<CG, OUT_BF16, true, MXF8_TILE_N, CG == 1 ? 4 : 5>;
+using MxCfg = typename std::conditional<CG == 1, TileCfg<1, OUT_BF16, true, 224, 4, 2, 4>,
+                                        TileCfg<2, OUT_BF16, true, 256, 4, 1, 8>>::type;
 
 constexpr uint8_t kUnitScale = 127;
 
@@ -100,6 +105,8 @@ size_t mxf8_workspace_b(int tiles_n, int num_kb) { return (size_t)tiles_n * num_
 
 int mxf8_sfb_block_bytes() { return MxCfg<1, false>::SFB_BYTES; }
 
+int mxf8_tile_n(int cta_group) { return cta_group == 1 ? MxCfg<1, false>::BN : MxCfg<2, false>::BN; }
+
 cudaError_t mxf8_prepare(int cta_group, int out_bf16) {
     if (cta_group == 1) return out_bf16 ? prepare_tc<MxCfg<1, true>>() : prepare_tc<MxCfg<1, false>>();
     return out_bf16 ? prepare_tc<MxCfg<2, true>>() : prepare_tc<MxCfg<2, false>>();
@@ -114,13 +121,13 @@ cudaError_t mxf8_max_active_clusters(int cta_group, int out_bf16, int *clusters)
 }
 
 cudaError_t mxf8_pack(const uint8_t *sfa, const uint8_t *sfb, uint8_t *out_a, uint8_t *out_b, int M, int N, int K,
-                      int tiles_m, int tiles_n, int num_kb, int sm_count, cudaStream_t stream) {
+                      int row_blocks, int tiles_n, int tile_n, int num_kb, int sm_count, cudaStream_t stream) {
     const int sfk = (K + 31) / 32;
-    const int64_t rows = ((int64_t)tiles_m * num_kb + (int64_t)tiles_n * num_kb * ((MXF8_TILE_N + 127) / 128)) * 32;
+    const int64_t rows = ((int64_t)row_blocks * num_kb + (int64_t)tiles_n * num_kb * ((tile_n + 127) / 128)) * 32;
     int blocks = (int)((rows + 255) / 256);
     if (blocks > 8 * sm_count) blocks = 8 * sm_count;
-    sf_pack_kernel<<<blocks, 256, 0, stream>>>(sfa, sfb, out_a, out_b, M, N, sfk, tiles_m, tiles_n, num_kb,
-                                               MXF8_TILE_N);
+    sf_pack_kernel<<<blocks, 256, 0, stream>>>(sfa, sfb, out_a, out_b, M, N, sfk, row_blocks, tiles_n, num_kb,
+                                               tile_n);
     return cudaGetLastError();
 }
 

@@ -114,6 +114,47 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
         : "memory");
 }
 
+// L2 eviction policies for the cache-hint forms of the bulk copies
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 2-D tiled load with an L2 cache policy (data read once: evict first)
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *m, uint32_t mbar, int32_t c0,
+                                                 int32_t c1, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(m), "r"(mbar), "r"(c0), "r"(c1), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap *m, uint32_t mbar, int32_t c0,
+                                                      int32_t c1, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(m), "r"(mbar), "r"(c0), "r"(c1), "l"(pol)
+        : "memory");
+}
+
+// 2-D tiled store with an L2 cache policy
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *m, uint32_t src, int32_t c0, int32_t c1,
+                                                  uint64_t pol) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+                     m),
+                 "r"(src), "r"(c0), "r"(c1), "l"(pol)
+                 : "memory");
+}
+
 // 2-D tiled store own SMEM -> GMEM (clipped to the tensor bounds), bulk-group completion
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src, int32_t c0, int32_t c1) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(m), "r"(src),
@@ -260,12 +301,18 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "r"(taddr));
 }
 
-// wait for this thread's tcgen05.ld; the "+r" ties keep every use of the
-// loaded registers after the wait
-__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+// wait for this thread's tcgen05.ld operations
+__device__ __forceinline__ void tmem_ld_wait_all() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// the "+r" ties keep every use of registers loaded by tcgen05.ld after the wait
+__device__ __forceinline__ void tie_registers(uint32_t (&r)[32]) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+    tmem_ld_wait_all();
+    tie_registers(r);
 }
 
 // ------------------------------------------------------------- descriptors
