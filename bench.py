@@ -180,6 +180,10 @@ def workload(args):
     if args.shape:
         M, N, K = (int(v) for v in args.shape.lower().split("x"))
         w = synth.scaled(w, M, N, K)
+    if args.a_col_major or args.b_row_major:
+        w = synth.dataclasses.replace(w, name=w.name + ("+Acol" if args.a_col_major else "") +
+                                      ("+Brow" if args.b_row_major else ""),
+                                      a_row_major=not args.a_col_major, b_row_major=args.b_row_major)
     return w
 
 
@@ -207,7 +211,8 @@ def run_ours(args, rank, world, local_rank):
     d_t = torch.bfloat16 if w.d == "bf16" else torch.float32
     D = torch.empty((w.M, w.N), dtype=d_t, device=dev)
     flags = {0: 0, 1: gemm.GEMM_FLAG_FORCE_1CTA, 2: gemm.GEMM_FLAG_FORCE_2CTA}[args.cta_group]
-    plan = gemm.Plan(w.M, w.N, w.K, w.ab, w.d, w.block_scaled, flags)
+    plan = gemm.Plan(w.M, w.N, w.K, w.ab, w.d, w.block_scaled, flags, a_row_major=w.a_row_major,
+                     b_row_major=w.b_row_major)
     info = plan.info
     stream = torch.cuda.Stream(device=dev)
 
@@ -291,6 +296,7 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.ab == "bf16" else w.ab,
         "data": "synthetic (seeded splitmix64; recipe of the workload)",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "ab": w.ab, "c": "fp32",
+                   "a_row_major": w.a_row_major, "b_row_major": w.b_row_major,
                    "d": w.d, "cta_group": info["cta_group"], "tile": [info["tile_m"], info["tile_n"],
                                                                       info["tile_k"]],
                    "stages": info["stages"], "grid": info["grid"], "replicas": world,
@@ -390,6 +396,8 @@ def main(argv=None):
     ap.add_argument("--shape", default=None, help="MxNxK: the workload's recipe at other sizes (profiling)")
     ap.add_argument("--cta-group", type=int, choices=[0, 1, 2], default=0,
                     help="force single CTAs (1) or CTA pairs (2); 0 = the plan's choice")
+    ap.add_argument("--a-col-major", action="store_true", help="store A column-major (M contiguous)")
+    ap.add_argument("--b-row-major", action="store_true", help="store B row-major (N contiguous)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")

@@ -31,6 +31,7 @@ struct gemm_plan {
     int64_t M, N, K;
     gemm_dtype ab, c, d;
     int block_scaled;
+    int a_mn, b_mn;           // A column-major (M contiguous), B row-major (N contiguous)
     unsigned flags;
     int device;
     int sm_count;
@@ -105,8 +106,13 @@ gemm_status encode_maps(gemm_plan *p, const void *A, const void *B, const void *
     const int eb = elem_bytes(p->ab);
     const uint32_t bk = 128u / (uint32_t)eb;                       // K elements in a 128-byte row
     const uint32_t b_rows = (uint32_t)(p->tile_n / p->cta_group);
-    bool ok = encode_2d(&p->maps[0], tma_dtype(p->ab), eb, A, p->K, p->M, bk, TILE_M, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_2d(&p->maps[1], tma_dtype(p->ab), eb, B, p->K, p->N, bk, b_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+    // K-major operand: [rows][K], box of bk x rows; MN-major operand: [K][rows], box one
+    // 128-byte atom (atom elements) wide along the rows and bk deep along K
+    const uint32_t atom = 128u / (uint32_t)eb;
+    bool ok = (p->a_mn ? encode_2d(&p->maps[0], tma_dtype(p->ab), eb, A, p->M, p->K, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B)
+                       : encode_2d(&p->maps[0], tma_dtype(p->ab), eb, A, p->K, p->M, bk, TILE_M, CU_TENSOR_MAP_SWIZZLE_128B)) &&
+              (p->b_mn ? encode_2d(&p->maps[1], tma_dtype(p->ab), eb, B, p->N, p->K, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B)
+                       : encode_2d(&p->maps[1], tma_dtype(p->ab), eb, B, p->K, p->N, bk, b_rows, CU_TENSOR_MAP_SWIZZLE_128B));
     if (ok && C)
         ok = encode_2d(&p->maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, p->N, p->M, EPI_COLS, 32,
                        CU_TENSOR_MAP_SWIZZLE_128B);
@@ -161,6 +167,12 @@ gemm_status configure_mxf8(gemm_plan *p) {
     int cg = (p->M >= 1024 && p->N >= 1024) ? 2 : 1;
     if (p->flags & GEMM_FLAG_FORCE_1CTA) cg = 1;
     if (p->flags & GEMM_FLAG_FORCE_2CTA) cg = 2;
+    // single-CTA tiles hold 224 rows of B, not a whole number of 128-element atoms:
+    // an N-contiguous B needs CTA pairs (128 rows each)
+    if (p->b_mn && cg == 1) {
+        if (p->flags & GEMM_FLAG_FORCE_1CTA) return GEMM_ERR_UNSUPPORTED;
+        cg = 2;
+    }
     const int bf = p->d == GEMM_BF16;
     if (mxf8_prepare(cg, bf) != cudaSuccess) return GEMM_ERR_CUDA;
     p->family = 1;
@@ -223,9 +235,12 @@ gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K, 
     if ((flags & GEMM_FLAG_FORCE_1CTA) && (flags & GEMM_FLAG_FORCE_2CTA)) return GEMM_ERR_INVALID_ARG;
     if (c != GEMM_F32 || (d != GEMM_F32 && d != GEMM_BF16)) return GEMM_ERR_UNSUPPORTED;
     if (block_scaled ? ab != GEMM_E4M3 : (ab != GEMM_F16 && ab != GEMM_BF16)) return GEMM_ERR_UNSUPPORTED;
-    if (!a_row_major || b_row_major) return GEMM_ERR_UNSUPPORTED;
-    // 16-byte row strides (the copy engine's stride rule)
-    if ((K * elem_bytes(ab)) % 16 != 0 || (N * 4) % 16 != 0 || (N * elem_bytes(d)) % 16 != 0)
+
+    // 16-byte row strides (the copy engine's stride rule): A rows hold K (row-major) or M
+    // (column-major) elements, B rows K (column-major) or N (row-major), C and D rows N
+    const int64_t a_row = a_row_major ? K : M, b_row = b_row_major ? N : K;
+    if ((a_row * elem_bytes(ab)) % 16 != 0 || (b_row * elem_bytes(ab)) % 16 != 0 || (N * 4) % 16 != 0 ||
+        (N * elem_bytes(d)) % 16 != 0)
         return GEMM_ERR_ALIGNMENT;
 
     int dev = 0;
@@ -243,6 +258,8 @@ gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K, 
     p->c = c;
     p->d = d;
     p->block_scaled = block_scaled;
+    p->a_mn = !a_row_major;
+    p->b_mn = b_row_major != 0;
     p->flags = flags;
     p->device = dev;
     p->sm_count = prop.multiProcessorCount;
@@ -283,12 +300,15 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
     kp.num_kb = p->num_kb;
     kp.group_m = p->group_m;
     kp.has_c = C != nullptr;
+    kp.a_mn = p->a_mn;
+    kp.b_mn = p->b_mn;
     kp.status = p->status;
     kp.timeout_ns = p->timeout_ns;
     kp.fault = p->fault;
     LaunchShape shape{p->grid, p->cta_group, p->smem};
     if (p->family == 1) {
-        kp.idesc = idesc_mxf8((uint32_t)(TILE_M * p->cta_group), (uint32_t)p->tile_n, 0, 0);
+        kp.idesc = idesc_mxf8((uint32_t)(TILE_M * p->cta_group), (uint32_t)p->tile_n, 0, 0) |
+                   ((uint32_t)p->a_mn << 15) | ((uint32_t)p->b_mn << 16);
         kp.sfa = p->ws_a;
         kp.sfb = p->ws_b;
         if (mxf8_pack(SFA, SFB, p->ws_a, p->ws_b, kp.M, kp.N, kp.K, p->tiles_m * p->cta_group, p->tiles_n, p->tile_n,
@@ -297,7 +317,8 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
         if (mxf8_launch(p->cta_group, p->d == GEMM_BF16, shape, p->maps, kp, stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
     } else {
-        kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * p->cta_group), (uint32_t)TILE_N);
+        kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * p->cta_group), (uint32_t)TILE_N) |
+                   ((uint32_t)p->a_mn << 15) | ((uint32_t)p->b_mn << 16);
         F16Config cfg{p->cta_group, p->d == GEMM_BF16};
         if (f16_launch(cfg, shape, p->maps, kp, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     }

@@ -16,6 +16,7 @@ struct KParams {
     int num_kb;          // K blocks (pipeline stages consumed per tile)
     int group_m;         // tile rasterisation: M tiles per group
     int has_c;
+    int a_mn, b_mn;      // operand stored MN-major (M or N contiguous) instead of K-major
     uint32_t idesc;      // tcgen05 instruction descriptor
     int *status;         // device status word (sticky error code)
     uint64_t timeout_ns; // limit of every wait

@@ -34,10 +34,6 @@
 
 #include <cstdint>
 
-// operand tiles marked evict-last in L2 (tuning knob)
-#ifndef GB300_OPERANDS_EVICT_LAST
-#define GB300_OPERANDS_EVICT_LAST 0
-#endif
 
 #include "gemm_internal.h"
 #include "ptx.cuh"
@@ -73,6 +69,9 @@ struct TileCfg {
     static constexpr int ELEM = SCALED ? 1 : 2;                 // operand bytes
     static constexpr int BK = 128 / ELEM;                       // K elements per stage: one 128-byte row
     static constexpr int MMA_K = 32 / ELEM;                     // K per instruction: 32 bytes
+    // MN-major operands: boxes one 128-byte swizzle atom wide along M (or N) and BK rows of K
+    static constexpr int ATOM_MN = 128 / ELEM;                  // M/N elements of one atom
+    static constexpr int ATOM_BYTES = BK * 128;                 // one atom column of a stage
     static constexpr int A_BYTES = TILE_M * 128;                // 16 KiB
     static constexpr int B_ROWS = BN / CG;                      // B rows held by one CTA
     static constexpr int B_BYTES = B_ROWS * 128;
@@ -218,9 +217,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-#if GB300_OPERANDS_EVICT_LAST
-            const uint64_t keep = l2_policy_evict_last();
-#endif
             for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
                 int tm, tn;
                 tile_coords(t, p.tiles_m, p.group_m, tm, tn, p.tiles_n);
@@ -238,31 +234,27 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t sf_dst = smem_addr(smem + Cfg::OFF_SF + s * (Cfg::SFA_BYTES + Cfg::SFB_BYTES));
                     const int sfa_row = ((tm * CG + (int)rank) * p.num_kb + kb) * (Cfg::SFA_BYTES / 128);
                     const int sfb_row = (tn * p.num_kb + kb) * (Cfg::SFB_BYTES / 128);
-                    if constexpr (CG == 1) {
-#if GB300_OPERANDS_EVICT_LAST
-                        tma_load_2d_hint(a_dst, &tmA, fb, kb * Cfg::BK, m0, keep);
-                        tma_load_2d_hint(b_dst, &tmB, fb, kb * Cfg::BK, n0, keep);
-#else
-                        tma_load_2d(a_dst, &tmA, fb, kb * Cfg::BK, m0);
-                        tma_load_2d(b_dst, &tmB, fb, kb * Cfg::BK, n0);
-#endif
-                        if constexpr (Cfg::SCALED) {
-                            tma_load_2d(sf_dst, &tmSFA, fb, 0, sfa_row);
-                            tma_load_2d(sf_dst + Cfg::SFA_BYTES, &tmSFB, fb, 0, sfb_row);
+                    // the completion of every copy of the stage counts on the leader's full[s]
+                    const uint32_t bar = CG == 1 ? fb : mapa_shared(fb, 0);
+                    auto load = [&](uint32_t dst, const CUtensorMap *m, int c0, int c1) {
+                        if constexpr (CG == 1) tma_load_2d(dst, m, bar, c0, c1);
+                        else tma_load_2d_pair(dst, m, bar, c0, c1);
+                    };
+                    // an operand tile: K-major, one box of BK x rows; MN-major, rows / ATOM_MN
+                    // boxes of ATOM_MN x BK, one per 128-byte atom column
+                    auto load_operand = [&](uint32_t dst, const CUtensorMap *m, int row0, int rows, bool mn) {
+                        if (!mn) {
+                            load(dst, m, kb * Cfg::BK, row0);
+                        } else {
+                            for (int i = 0; i < rows / Cfg::ATOM_MN; ++i)
+                                load(dst + i * Cfg::ATOM_BYTES, m, row0 + i * Cfg::ATOM_MN, kb * Cfg::BK);
                         }
-                    } else {
-                        const uint32_t leader_fb = mapa_shared(fb, 0);
-#if GB300_OPERANDS_EVICT_LAST
-                        tma_load_2d_pair_hint(a_dst, &tmA, leader_fb, kb * Cfg::BK, m0, keep);
-                        tma_load_2d_pair_hint(b_dst, &tmB, leader_fb, kb * Cfg::BK, n0, keep);
-#else
-                        tma_load_2d_pair(a_dst, &tmA, leader_fb, kb * Cfg::BK, m0);
-                        tma_load_2d_pair(b_dst, &tmB, leader_fb, kb * Cfg::BK, n0);
-#endif
-                        if constexpr (Cfg::SCALED) {
-                            tma_load_2d_pair(sf_dst, &tmSFA, leader_fb, 0, sfa_row);
-                            tma_load_2d_pair(sf_dst + Cfg::SFA_BYTES, &tmSFB, leader_fb, 0, sfb_row);
-                        }
+                    };
+                    load_operand(a_dst, &tmA, m0, TILE_M, p.a_mn != 0);
+                    load_operand(b_dst, &tmB, n0, Cfg::B_ROWS, p.b_mn != 0);
+                    if constexpr (Cfg::SCALED) {
+                        load(sf_dst, &tmSFA, 0, sfa_row);
+                        load(sf_dst + Cfg::SFA_BYTES, &tmSFB, 0, sfb_row);
                     }
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
@@ -271,6 +263,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA issue
         if (rank == 0 && lane == 0) {
+            // shared-memory descriptors (128-byte swizzle).  K-major: 8-row groups 1024 B
+            // apart, the leading offset unused (encoded 1), an MMA's K step = 32 bytes.
+            // MN-major: 8-row K groups 1024 B apart, atom columns ATOM_BYTES apart (the
+            // leading offset), an MMA's K step = MMA_K rows of 128 bytes.
+            const uint32_t a_lbo = p.a_mn ? Cfg::ATOM_BYTES : 16, b_lbo = p.b_mn ? Cfg::ATOM_BYTES : 16;
+            const uint32_t a_step = p.a_mn ? (Cfg::MMA_K * 128) >> 4 : 2, b_step = p.b_mn ? (Cfg::MMA_K * 128) >> 4 : 2;
             int s = 0;
             uint32_t ph = 0, acc_it = 0;
             bool ok = true;
@@ -283,8 +281,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!W.wait(&full[s], ph)) { ok = false; break; }
                     tc_fence_after_sync();
-                    const uint64_t ad = smem_desc(smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES), 16, 1024, SWZ_128B);
-                    const uint64_t bd = smem_desc(smem_addr(smem + Cfg::OFF_B + s * Cfg::B_BYTES), 16, 1024, SWZ_128B);
+                    const uint64_t ad = smem_desc(smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES), a_lbo, 1024, SWZ_128B);
+                    const uint64_t bd = smem_desc(smem_addr(smem + Cfg::OFF_B + s * Cfg::B_BYTES), b_lbo, 1024, SWZ_128B);
                     if constexpr (Cfg::SCALED) {
                         // stage s's scales: SFA in 4 columns, SFB in 4 per 128 rows of B,
                         // each a 32-lane x 16-byte SMEM block replicated to the 4 lane windows
@@ -298,12 +296,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                                        smem_desc(sf_src + Cfg::SFA_BYTES + 512 * h, 512, 128, SWZ_NONE));
 #pragma unroll
                         for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k)   // K block k of 32 uses scale byte k
-                            mma_mxf8<CG>(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc | (k << 4) | (k << 29), sfa_t, sfb_t,
+                            mma_mxf8<CG>(d_tmem, ad + a_step * k, bd + b_step * k, p.idesc | (k << 4) | (k << 29), sfa_t, sfb_t,
                                          (kb | k) != 0);
                     } else {
 #pragma unroll
                         for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k)   // 32 bytes of K = 2 descriptor units
-                            mma_f16<CG>(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, (kb | k) != 0);
+                            mma_f16<CG>(d_tmem, ad + a_step * k, bd + b_step * k, p.idesc, (kb | k) != 0);
                     }
                     if constexpr (CG == 1) tc_commit<1>(smem_addr(&empty[s]));
                     else tc_commit_pair(smem_addr(&empty[s]), 0x3);

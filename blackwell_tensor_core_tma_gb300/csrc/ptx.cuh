@@ -121,26 +121,11 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return pol;
 }
 
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    return pol;
-}
-
 // 2-D tiled load with an L2 cache policy (data read once: evict first)
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *m, uint32_t mbar, int32_t c0,
                                                  int32_t c1, uint64_t pol) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(m), "r"(mbar), "r"(c0), "r"(c1), "l"(pol)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap *m, uint32_t mbar, int32_t c0,
-                                                      int32_t c1, uint64_t pol) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
         "l"(m), "r"(mbar), "r"(c0), "r"(c1), "l"(pol)
         : "memory");
@@ -334,14 +319,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo_bytes,
 }
 
 // Instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A/B format in bits
-// 7-9 / 10-12 (0 = fp16, 1 = bf16), both K-major (bits 15, 16 = 0),
+// 7-9 / 10-12 (0 = fp16, 1 = bf16), K-major (bits 15, 16 = 0; the host sets
+// them for MN-major A / B),
 // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_bf16, uint32_t M, uint32_t N) {
     return (1u << 4) | (ab_bf16 << 7) | (ab_bf16 << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // Instruction descriptor, kind::mxf8f6f4 with block scaling: B scale-factor
-// byte id in bits 4-5, A/B format e4m3 (0) in bits 7-9 / 10-12, K-major,
+// byte id in bits 4-5, A/B format e4m3 (0) in bits 7-9 / 10-12, K-major (bits 15, 16
+// set by the host for MN-major A / B),
 // N >> 3 in bits 17-22, scale format UE8M0 (bit 23 = 1), M >> 4 in bits 24-28,
 // A scale-factor byte id in bits 29-30.
 __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32_t sfa_id, uint32_t sfb_id) {

@@ -159,10 +159,12 @@ def gemm_run_noalloc(M: int, N: int, K: int, ab, d, A, B, C, D, stream=None, wai
 class Plan:
     """Owning wrapper of a gemm_plan_t (destroyed on close / context exit)."""
 
-    def __init__(self, M, N, K, ab="bf16", d="f32", block_scaled=False, flags=0, c="f32"):
+    def __init__(self, M, N, K, ab="bf16", d="f32", block_scaled=False, flags=0, c="f32", a_row_major=True,
+                 b_row_major=False):
         self.M, self.N, self.K, self.ab, self.d = M, N, K, ab, d
         self.block_scaled = bool(block_scaled)
-        self.handle = gemm_plan_create(M, N, K, ab, c, d, 1, 0, int(block_scaled), flags)
+        self.handle = None
+        self.handle = gemm_plan_create(M, N, K, ab, c, d, int(a_row_major), int(b_row_major), int(block_scaled), flags)
 
     @property
     def info(self) -> dict:

@@ -18,9 +18,13 @@
  *     b[k][j] = e4m3(B[k][j]) * 2^(SFB[j][k/32] - 127)
  *
  * Memory layout (all buffers packed; no leading-dimension arguments):
- *   A    M x K, row-major (element (i,k) at A[i*K + k]).
- *   B    K x N, column-major (element (k,j) at B[j*K + k]); both operands
- *        are thus K-major, the layout the tensor core reads natively.
+ *   A    M x K, row-major (element (i,k) at A[i*K + k]) or, with
+ *        a_row_major = 0, column-major (at A[k*M + i]).
+ *   B    K x N, column-major (element (k,j) at B[j*K + k]) or, with
+ *        b_row_major = 1, row-major (at B[k*N + j]).  The tensor core reads
+ *        either order: K-major operands and M/N-major ones (described to it
+ *        by the shared-memory descriptor's layout and the instruction
+ *        descriptor's transpose bits).
  *   C    M x N fp32 row-major, or NULL for C = 0.
  *   D    M x N row-major, fp32 or bf16 (round to nearest even).
  *   SFA  M x ceil(K/32) UE8M0 codes, row-major (block-scaled plans only).
@@ -31,8 +35,9 @@
  * stride 1 and 16-byte aligned strides for the others ("(二) CUTLASS —— 掌握
  * Tensor Memory Accelerator（TMA）", section "使用 TMA 处理 remainder tiles
  * 以及 stride 要求": pad the tensor before calling otherwise).  For 16-bit
- * operands that means K % 8 == 0, for e4m3 K % 16 == 0; for C and fp32 D
- * N % 4 == 0, for bf16 D N % 8 == 0.  M, N and K need not be multiples of
+ * operands the contiguous extent (K, or M / N for column- / row-major A / B)
+ * must be a multiple of 8, for e4m3 of 16; for C and fp32 D N % 4 == 0, for
+ * bf16 D N % 8 == 0.  M, N and K need not be multiples of
  * any tile size: the copy engine predicates the remainder tiles.
  *
  * Ownership: the caller owns every device buffer.  A plan owns host state and
@@ -89,9 +94,10 @@ typedef struct {
 /*
  * Validate a problem and choose its kernel.  M, N, K > 0.  ab is GEMM_F16 or
  * GEMM_BF16 (block_scaled = 0) or GEMM_E4M3 (block_scaled = 1).  c must be
- * GEMM_F32; d is GEMM_F32 or GEMM_BF16.  a_row_major = 1 and b_row_major = 0
- * (both operands K-major) are the supported layout; other combinations return
- * GEMM_ERR_UNSUPPORTED.  Row-stride alignment (see above) is checked here and
+ * GEMM_F32; d is GEMM_F32 or GEMM_BF16.  a_row_major and b_row_major choose
+ * the storage order of A and B (all four combinations; a block-scaled plan
+ * with row-major B needs CTA pairs, so GEMM_FLAG_FORCE_1CTA then returns
+ * GEMM_ERR_UNSUPPORTED).  Row-stride alignment (see above) is checked here and
  * returns GEMM_ERR_ALIGNMENT.  The plan is bound to the CUDA device current
  * at creation, which must be compute capability 10.3.  *out is set only on
  * GEMM_OK.

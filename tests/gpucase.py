@@ -47,7 +47,8 @@ def run(w: synth.Workload, flags: int = 0, c_none: bool = False, guard: int = 0,
     g = guard
     buf = torch.full((n + 2 * g,), float("nan"), dtype=tdt, device="cuda")
     D = buf[g:g + n].view(w.M, w.N)
-    with gemm.Plan(w.M, w.N, w.K, w.ab, w.d, w.block_scaled, flags) as plan:
+    with gemm.Plan(w.M, w.N, w.K, w.ab, w.d, w.block_scaled, flags, a_row_major=w.a_row_major,
+                   b_row_major=w.b_row_major) as plan:
         for _ in range(reps):
             plan.run(A, B, C, D, SFA, SFB, torch.cuda.current_stream())
         torch.cuda.synchronize()

@@ -52,7 +52,7 @@ def test_plan_rejects_before_device(lib, args, status):
 
 def test_plan_rejects_unsupported_combinations(lib):
     cases = [
-        dict(ab="f32"), dict(c="bf16"), dict(d="f16"), dict(a_row_major=0), dict(b_row_major=1),
+        dict(ab="f32"), dict(c="bf16"), dict(d="f16"),
         dict(ab="e4m3", block_scaled=0), dict(ab="bf16", block_scaled=1),
     ]
     for kw in cases:
