@@ -45,6 +45,9 @@ struct gemm_plan {
     int fault;
     int *status;              // device word
     int family;               // 0: fp16/bf16 kernel, 1: block-scaled e4m3 kernel
+    int splits;               // K slices per tile (1 = no split-K)
+    int capacity;             // work units the persistent grid runs at once (CTAs or CTA pairs)
+    int split_request;        // 0 = choose automatically, n >= 1 = asked for
     int tile_n;
     int num_kb;
     uint8_t *ws_a, *ws_b;     // block-scaled: packed scale factors (workspace)
@@ -158,6 +161,7 @@ gemm_status configure_f16(gemm_plan *p) {
         int clusters = 0;
         if (f16_max_active_clusters(cfg, &clusters) == cudaSuccess && clusters > 0) units = clusters;
     }
+    p->capacity = units;
     p->grid = cg * (p->tiles < units ? p->tiles : units);
     p->group_m = cg == 2 ? GB300_GROUP_M_PAIRS : GB300_GROUP_M_SINGLE;
     return GEMM_OK;
@@ -189,6 +193,7 @@ gemm_status configure_mxf8(gemm_plan *p) {
         int clusters = 0;
         if (mxf8_max_active_clusters(cg, bf, &clusters) == cudaSuccess && clusters > 0) units = clusters;
     }
+    p->capacity = units;
     p->grid = cg * (p->tiles < units ? p->tiles : units);
     p->group_m = cg == 2 ? GB300_GROUP_M_PAIRS : GB300_GROUP_M_SINGLE;
     // workspace: one 512-byte SFA block per (128 rows, 128 K), one SFB block per (tile column, 128 K)
@@ -209,6 +214,27 @@ gemm_status configure_mxf8(gemm_plan *p) {
                    CU_TENSOR_MAP_SWIZZLE_NONE))
         return GEMM_ERR_CUDA;
     return GEMM_OK;
+}
+
+// Split-K: when the output tiles cannot fill the GPU, cut each tile's K range into
+// slices that run as separate work units and add their partial products into D
+// (fp32 only: rounding every partial sum to bf16 would cost accuracy).
+void choose_splits(gemm_plan *p) {
+    const int units = p->capacity;
+    int s = 1;
+    if (p->split_request >= 1) {
+        s = p->split_request;
+    } else if (p->d == GEMM_F32 && 2 * p->tiles <= units && p->num_kb >= 8) {
+        s = units / p->tiles;
+        if (s > p->num_kb / 4) s = p->num_kb / 4;
+        if (s > 16) s = 16;
+    }
+    if (s > p->num_kb) s = p->num_kb;
+    if (s < 1 || p->d != GEMM_F32 || (p->flags & GEMM_FLAG_DETERMINISTIC)) s = 1;
+    p->splits = s;
+    // more work units than tiles: the persistent grid may grow up to the machine
+    const int work = p->tiles * s;
+    p->grid = p->cta_group * (work < units ? work : units);
 }
 
 }  // namespace
@@ -266,9 +292,12 @@ gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K, 
     p->timeout_ns = 1000000000ull;
     gemm_status st = block_scaled ? configure_mxf8(p) : configure_f16(p);
     if (st != GEMM_OK) {
+        cudaFree(p->ws_a);
+        cudaFree(p->ws_b);
         delete p;
         return st;
     }
+    choose_splits(p);
     if (cudaMalloc(&p->status, sizeof(int)) != cudaSuccess) {
         delete p;
         return GEMM_ERR_CUDA;
@@ -302,6 +331,14 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
     kp.has_c = C != nullptr;
     kp.a_mn = p->a_mn;
     kp.b_mn = p->b_mn;
+    kp.splits = p->splits;
+    if (p->splits > 1) {
+        // D starts as C (or 0); every K slice then adds its partial product into it
+        if (init_d_launch(static_cast<float *>(D), static_cast<const float *>(C), (size_t)p->M * p->N, p->sm_count,
+                          stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        kp.has_c = 0;
+    }
     kp.status = p->status;
     kp.timeout_ns = p->timeout_ns;
     kp.fault = p->fault;
@@ -385,7 +422,8 @@ gemm_status gemm_plan_get_info(gemm_plan_t p, gemm_plan_info *info) {
     info->grid = p->grid;
     info->tiles = p->tiles;
     info->smem_bytes = p->smem;
-    info->launches_per_run = p->family == 1 ? 2 : 1;
+    info->launches_per_run = (p->family == 1 ? 2 : 1) + (p->splits > 1 ? 1 : 0);
+    info->splits = p->splits;
     info->sm_count = p->sm_count;
     return GEMM_OK;
 }
@@ -393,6 +431,14 @@ gemm_status gemm_plan_get_info(gemm_plan_t p, gemm_plan_info *info) {
 gemm_status gemm_plan_set_timeout(gemm_plan_t p, uint64_t ns) {
     if (!p || ns == 0) return GEMM_ERR_INVALID_ARG;
     p->timeout_ns = ns;
+    return GEMM_OK;
+}
+
+gemm_status gemm_plan_set_split_k(gemm_plan_t p, int splits) {
+    if (!p || splits < 0) return GEMM_ERR_INVALID_ARG;
+    if (splits > 1 && (p->d != GEMM_F32 || (p->flags & GEMM_FLAG_DETERMINISTIC))) return GEMM_ERR_UNSUPPORTED;
+    p->split_request = splits;
+    choose_splits(p);
     return GEMM_OK;
 }
 

@@ -18,7 +18,23 @@ namespace {
 template <int CG, bool OUT_BF16>
 using F16Cfg = TileCfg<CG, OUT_BF16, false, TILE_N, CG == 1 ? GB300_F16_CG1_STAGES : GB300_F16_CG2_STAGES>;
 
+// D = C (or 0): the starting value split-K slices add their partial products to
+__global__ void init_d_kernel(float4 *__restrict__ D, const float4 *__restrict__ C, size_t n4) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x)
+        D[i] = C ? C[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 }  // namespace
+
+cudaError_t init_d_launch(float *D, const float *C, size_t n, int sm_count, cudaStream_t stream) {
+    const size_t n4 = n / 4;
+    size_t blocks = (n4 + 255) / 256;
+    if (blocks > (size_t)sm_count * 8) blocks = (size_t)sm_count * 8;
+    if (blocks == 0) blocks = 1;
+    init_d_kernel<<<(unsigned)blocks, 256, 0, stream>>>(reinterpret_cast<float4 *>(D),
+                                                         reinterpret_cast<const float4 *>(C), n4);
+    return cudaGetLastError();
+}
 
 int f16_stages(int cta_group) { return cta_group == 1 ? F16Cfg<1, false>::STAGES : F16Cfg<2, false>::STAGES; }
 

@@ -17,6 +17,7 @@ struct KParams {
     int group_m;         // tile rasterisation: M tiles per group
     int has_c;
     int a_mn, b_mn;      // operand stored MN-major (M or N contiguous) instead of K-major
+    int splits;          // K slices per tile (split-K); > 1: D already holds C, slices reduce-add into it
     uint32_t idesc;      // tcgen05 instruction descriptor
     int *status;         // device status word (sticky error code)
     uint64_t timeout_ns; // limit of every wait
@@ -46,6 +47,9 @@ cudaError_t f16_prepare(const F16Config &cfg);   // set the kernel's shared-memo
 cudaError_t f16_max_active_clusters(const F16Config &cfg, int *clusters);
 cudaError_t f16_launch(const F16Config &cfg, const LaunchShape &shape, const CUtensorMap *maps,
                        const KParams &p, cudaStream_t stream);
+
+// split-K preparation (gemm_f16.cu): D = C, or D = 0 without C (fp32, n elements, n % 4 == 0)
+cudaError_t init_d_launch(float *D, const float *C, size_t n, int sm_count, cudaStream_t stream);
 
 // block-scaled e4m3 kernel family (gemm_mxf8.cu)
 int mxf8_tile_n(int cta_group);

@@ -118,6 +118,16 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int group_m, int
     tn = r / gsize;
 }
 
+// Work unit u = (tile, K slice): the splits slices of a tile are consecutive units, so
+// they run at about the same time on neighbouring CTAs.  Slice s covers k-blocks
+// [s * num_kb / splits, (s + 1) * num_kb / splits), never empty (splits <= num_kb).
+__device__ __forceinline__ void unit_coords(int u, const KParams &p, int &tm, int &tn, int &kb0, int &kb1) {
+    const int t = u / p.splits, s = u - t * p.splits;
+    tile_coords(t, p.tiles_m, p.group_m, tm, tn, p.tiles_n);
+    kb0 = (int)((int64_t)s * p.num_kb / p.splits);
+    kb1 = (int)((int64_t)(s + 1) * p.num_kb / p.splits);
+}
+
 struct Waiter {
     volatile int *abort_flag;
     int *status;
@@ -217,14 +227,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int t = tile0; ok && t < p.num_tiles; t += tile_step) {
-                int tm, tn;
-                tile_coords(t, p.tiles_m, p.group_m, tm, tn, p.tiles_n);
+            for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step) {
+                int tm, tn, kb0, kb1;
+                unit_coords(u, p, tm, tn, kb0, kb1);
                 const int m0 = tm * TILE_M * CG + (int)rank * TILE_M;
                 const int n0 = tn * BN + (int)rank * Cfg::B_ROWS;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!W.wait(&empty[s], ph ^ 1u)) { ok = false; break; }
-                    const bool withhold = p.fault == 1 && t == tile0 && kb == 0;
+                    const bool withhold = p.fault == 1 && u == tile0 && kb == kb0;
                     if (rank == 0 && !withhold) mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
                     const uint32_t a_dst = smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES);
                     const uint32_t b_dst = smem_addr(smem + Cfg::OFF_B + s * Cfg::B_BYTES);
@@ -272,13 +282,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int s = 0;
             uint32_t ph = 0, acc_it = 0;
             bool ok = true;
-            for (int t = tile0; ok && t < p.num_tiles; t += tile_step, ++acc_it) {
+            for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step, ++acc_it) {
+                int tm, tn, kb0, kb1;
+                unit_coords(u, p, tm, tn, kb0, kb1);
                 const uint32_t b = Cfg::ACC_BUFS == 2 ? (acc_it & 1u) : 0u;
                 const uint32_t aph = Cfg::ACC_BUFS == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
                 if (!W.wait(&tempty[b], aph ^ 1u)) { ok = false; break; }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * BN;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!W.wait(&full[s], ph)) { ok = false; break; }
                     tc_fence_after_sync();
                     const uint64_t ad = smem_desc(smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES), a_lbo, 1024, SWZ_128B);
@@ -297,11 +309,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                         for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k)   // K block k of 32 uses scale byte k
                             mma_mxf8<CG>(d_tmem, ad + a_step * k, bd + b_step * k, p.idesc | (k << 4) | (k << 29), sfa_t, sfb_t,
-                                         (kb | k) != 0);
+                                         (kb != kb0) | (k != 0));
                     } else {
 #pragma unroll
                         for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k)   // 32 bytes of K = 2 descriptor units
-                            mma_f16<CG>(d_tmem, ad + a_step * k, bd + b_step * k, p.idesc, (kb | k) != 0);
+                            mma_f16<CG>(d_tmem, ad + a_step * k, bd + b_step * k, p.idesc, (kb != kb0) | (k != 0));
                     }
                     if constexpr (CG == 1) tc_commit<1>(smem_addr(&empty[s]));
                     else tc_commit_pair(smem_addr(&empty[s]), 0x3);
@@ -329,9 +341,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // buffer ec % 2, and its C load is that buffer's (ec / 2)-th
         uint32_t acc_it = 0, ec = 0;
         bool ok = true;
-        for (int t = tile0; ok && t < p.num_tiles; t += tile_step, ++acc_it) {
-            int tm, tn;
-            tile_coords(t, p.tiles_m, p.group_m, tm, tn, p.tiles_n);
+        for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step, ++acc_it) {
+            int tm, tn, kb0, kb1;
+            unit_coords(u, p, tm, tn, kb0, kb1);
             const uint32_t b = Cfg::ACC_BUFS == 2 ? (acc_it & 1u) : 0u;
             const uint32_t aph = Cfg::ACC_BUFS == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
             const int m_warp = tm * TILE_M * CG + (int)rank * TILE_M + 32 * q;
@@ -408,7 +420,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d_hint(&tmD, smem_addr(buf), n_warp + EPI_COLS * j, m_warp, stream_pol);
+                    if (p.splits > 1) tma_reduce_add_2d(&tmD, smem_addr(buf), n_warp + EPI_COLS * j, m_warp);
+                    else tma_store_2d_hint(&tmD, smem_addr(buf), n_warp + EPI_COLS * j, m_warp, stream_pol);
                     bulk_commit_group();
                 }
                 ++ec;

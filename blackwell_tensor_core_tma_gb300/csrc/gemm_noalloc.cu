@@ -129,6 +129,7 @@ extern "C" gemm_status gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dt
     kp.num_kb = (int)((K + TILE_K16 - 1) / TILE_K16);
     kp.group_m = cg == 2 ? 8 : 16;
     kp.has_c = C != nullptr;
+    kp.splits = 1;
     kp.idesc = idesc_f16(ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * cg), (uint32_t)TILE_N);
     kp.status = s->status;
     kp.timeout_ns = 1000000000ull;

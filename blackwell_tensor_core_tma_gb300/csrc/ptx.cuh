@@ -147,6 +147,14 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *m, uint32_t src,
                  : "memory");
 }
 
+// 2-D tiled reduce-add own SMEM -> GMEM: gmem += smem element by element (fp32),
+// clipped to the tensor bounds, bulk-group completion
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *m, uint32_t src, int32_t c0, int32_t c1) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];" ::"l"(m),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // wait until no committed bulk store still reads shared memory

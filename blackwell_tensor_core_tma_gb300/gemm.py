@@ -15,14 +15,14 @@ from . import build as _build
 
 GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ALIGNMENT, GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT = range(6)
 GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_F32 = range(4)
-GEMM_FLAG_SYNC, GEMM_FLAG_FORCE_1CTA, GEMM_FLAG_FORCE_2CTA = 0x1, 0x2, 0x4
+GEMM_FLAG_SYNC, GEMM_FLAG_FORCE_1CTA, GEMM_FLAG_FORCE_2CTA, GEMM_FLAG_DETERMINISTIC = 0x1, 0x2, 0x4, 0x8
 
 DTYPE = {"f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM_E4M3, "f32": GEMM_F32}
 
 # every symbol include/gb300gemm.h and include/gb300gemm_testing.h declare
 EXPORTS = ["gemm_plan_create", "gemm_run", "gemm_run_host", "gemm_plan_last_status", "gemm_plan_get_info",
            "gemm_plan_set_timeout", "gemm_plan_destroy", "gemm_status_string", "gemm_testing_set_fault",
-           "gemm_run_noalloc"]
+           "gemm_run_noalloc", "gemm_plan_set_split_k"]
 
 
 class GemmError(RuntimeError):
@@ -33,7 +33,7 @@ class GemmError(RuntimeError):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "grid", "tiles",
-                                            "smem_bytes", "launches_per_run", "sm_count")]
+                                            "smem_bytes", "launches_per_run", "sm_count", "splits")]
 
 
 _lib = None
@@ -70,6 +70,8 @@ def lib():
         L.gemm_status_string.restype = ctypes.c_char_p
         L.gemm_testing_set_fault.argtypes = [vp, st]
         L.gemm_testing_set_fault.restype = st
+        L.gemm_plan_set_split_k.argtypes = [vp, st]
+        L.gemm_plan_set_split_k.restype = st
         L.gemm_run_noalloc.argtypes = [i64, i64, i64, st, st, vp, vp, vp, vp, vp, st]
         L.gemm_run_noalloc.restype = st
         _lib = L
@@ -140,6 +142,10 @@ def gemm_plan_set_timeout(plan: int, ns: int):
     _check(lib().gemm_plan_set_timeout(plan, ns), "gemm_plan_set_timeout")
 
 
+def gemm_plan_set_split_k(plan: int, splits: int):
+    _check(lib().gemm_plan_set_split_k(plan, splits), "gemm_plan_set_split_k")
+
+
 def gemm_plan_destroy(plan: int):
     _check(lib().gemm_plan_destroy(plan), "gemm_plan_destroy")
 
@@ -181,6 +187,9 @@ class Plan:
 
     def set_timeout(self, ns: int):
         gemm_plan_set_timeout(self.handle, ns)
+
+    def set_split_k(self, splits: int):
+        gemm_plan_set_split_k(self.handle, splits)
 
     def close(self):
         if self.handle:

@@ -75,6 +75,7 @@ typedef enum {
 #define GEMM_FLAG_SYNC        0x1u  /* gemm_run synchronises its stream and returns the kernel status */
 #define GEMM_FLAG_FORCE_1CTA  0x2u  /* use single-CTA tiles (cta_group::1) even where pairs would be chosen */
 #define GEMM_FLAG_FORCE_2CTA  0x4u  /* use CTA-pair tiles (cta_group::2) even where single CTAs would be chosen */
+#define GEMM_FLAG_DETERMINISTIC 0x8u /* bitwise-reproducible results run to run: no split-K (see gemm_plan_set_split_k) */
 
 typedef struct gemm_plan *gemm_plan_t;
 
@@ -89,6 +90,7 @@ typedef struct {
     int smem_bytes;         /* dynamic shared memory per CTA */
     int launches_per_run;   /* kernels one gemm_run enqueues */
     int sm_count;           /* SMs of the device the plan was made for */
+    int splits;             /* K slices per output tile (1 = no split-K) */
 } gemm_plan_info;
 
 /*
@@ -144,6 +146,24 @@ gemm_status gemm_plan_get_info(gemm_plan_t p, gemm_plan_info *info);
  * returns; the CUDA context stays usable.
  */
 gemm_status gemm_plan_set_timeout(gemm_plan_t p, uint64_t ns);
+
+/*
+ * Split-K ("(二) CUTLASS —— 掌握 Tensor Memory Accelerator（TMA）", section
+ * "TMA Store Reduce": a TMA store can add its shared-memory tile into global
+ * memory instead of overwriting it).  With splits > 1 each output tile's K
+ * range is cut into that many slices that run as separate work units: a
+ * small kernel first sets D = C (or 0), then every slice adds its partial
+ * product into D with a TMA reduce-add.  This fills the GPU when there are
+ * fewer output tiles than SMs.  splits = 0 lets the plan choose (it splits
+ * fp32-D problems whose tiles fill at most half the GPU and whose K spans
+ * at least 8 k-blocks), 1 turns split-K off; splits is clamped to the number
+ * of k-blocks.  Requires fp32 D (GEMM_ERR_UNSUPPORTED otherwise): rounding
+ * every partial sum to bf16 would cost accuracy.  The order in which slices
+ * are added varies between runs, so results may differ in the last bits; a
+ * plan created with GEMM_FLAG_DETERMINISTIC never splits (splits > 1 then
+ * returns GEMM_ERR_UNSUPPORTED).
+ */
+gemm_status gemm_plan_set_split_k(gemm_plan_t p, int splits);
 
 /* Release the plan (its status word and any host-run buffers).  NULL is a no-op. */
 gemm_status gemm_plan_destroy(gemm_plan_t p);

@@ -82,10 +82,13 @@ def test_long_k_and_many_tiles_per_cta():
 
 
 def test_repeated_runs_identical():
+    """A deterministic plan gives bitwise-identical results run after run (this
+    shape would otherwise be split along K)."""
     w = synth.scaled(BF16_UNI, 512, 512, 640)
-    x, D1, _, st1, _ = gpucase.run(w, reps=1)
-    _, D3, _, st3, _ = gpucase.run(w, inputs=x, reps=3)
-    assert st1 == st3 == gemm.GEMM_OK
+    det = gemm.GEMM_FLAG_DETERMINISTIC
+    x, D1, info, st1, _ = gpucase.run(w, flags=det, reps=1)
+    _, D3, _, st3, _ = gpucase.run(w, flags=det, inputs=x, reps=3)
+    assert st1 == st3 == gemm.GEMM_OK and info["splits"] == 1
     assert np.array_equal(D1, D3)
 
 
