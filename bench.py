@@ -39,8 +39,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture
 # summarised in profiles/; valid only for the kernel sources the capture ran on
 MEASURED_TRAFFIC = {
-    "bf16_8192x8192x8192_bf16out": {"bytes": 1593426944, "src": "06631707aa4637dd",
+    "bf16_8192x8192x8192_bf16out": {"bytes": 1398978816 + 123798272, "src": "f35a24c8279ff119",
                                     "ncu": "profiles/gemm_tc_kernel_bf16_8192x8192x8192_bf16out_launches.md"},
+    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 706623232 + 237450752, "src": "f35a24c8279ff119",
+                                          "ncu": "profiles/gemm_tc_kernel_mxf8_8192x8192x8192_launches.md"},
 }
 
 
