@@ -39,28 +39,34 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture
 # summarised in profiles/; valid only for the kernel sources the capture ran on
 MEASURED_TRAFFIC = {
-    "bf16_8192x8192x8192_bf16out": {"bytes": 1398978816 + 123798272, "src": "f35a24c8279ff119",
+    "bf16_8192x8192x8192_bf16out": {"bytes": 1398978816 + 123798272, "src": "ef60784a3f85e76d",
                                     "ncu": "profiles/gemm_tc_kernel_bf16_8192x8192x8192_bf16out_launches.md"},
-    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 706623232 + 237450752, "src": "f35a24c8279ff119",
+    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 706623232 + 237450752, "src": "ef763b86e4aea305",
                                           "ncu": "profiles/gemm_tc_kernel_mxf8_8192x8192x8192_launches.md"},
 }
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources (csrc/*) that build the kernels."""
-    import glob
+KERNEL_SOURCES = {
+    "f16": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_f16.cu"],
+    "mxf8": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_mxf8.cu"],
+}
+
+
+def kernel_source_hash(family: str = "f16") -> str:
+    """Hash of the CUDA sources the GEMM kernel of a family is built from."""
     import hashlib
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "blackwell_tensor_core_tma_gb300", "csrc", "*"))):
-        h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
+    for f in KERNEL_SOURCES[family]:
+        h.update(f.encode())
+        with open(os.path.join(ROOT, "blackwell_tensor_core_tma_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def measured_traffic(workload_name: str):
     t = MEASURED_TRAFFIC.get(workload_name)
-    if t is None or t["src"] != kernel_source_hash():
+    family = "mxf8" if workload_name.startswith("mxf8") else "f16"
+    if t is None or t["src"] != kernel_source_hash(family):
         return None, None
     return t["bytes"], t["ncu"]
 # dense tensor-core rate of e4m3 relative to bf16 (nominal 4.5 vs 2.25 PFLOP/s)

@@ -24,6 +24,7 @@
 // Each stage's scales take a 12-column TMEM slot (4 SFA + 8 SFB columns).  In
 // a CTA pair each CTA holds the SFA of its own 128 rows and the SFB of all the
 // tile's columns.
+#include <cstring>
 #include <type_traits>
 
 #include "gemm_kernel.cuh"
@@ -42,52 +43,75 @@ using MxCfg = typename std::conditional<CG == 1, TileCfg<1, OUT_BF16, true, 224,
 
 constexpr uint8_t kUnitScale = 127;
 
-// one thread per 16-byte row of a 512-byte block
-__global__ void sf_pack_kernel(const uint8_t *__restrict__ sfa, const uint8_t *__restrict__ sfb,
-                               uint8_t *__restrict__ out_a, uint8_t *__restrict__ out_b, int M, int N, int sfk,
-                               int tiles_m, int tiles_n, int num_kb, int tile_n) {
-    const int64_t a_rows = (int64_t)tiles_m * num_kb * 32;
-    const int64_t halves = (tile_n + 127) / 128;
-    const int64_t b_rows = (int64_t)tiles_n * num_kb * halves * 32;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < a_rows + b_rows;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const bool is_a = i < a_rows;
-        const int64_t r = is_a ? i : i - a_rows;
-        const int lane = (int)(r & 31);
-        const int64_t blk = r >> 5;                     // 512-byte block index
-        uint32_t w[4];
-        if (is_a) {
-            const int kb = (int)(blk % num_kb);
-            const int mb = (int)(blk / num_kb);
-            for (int mg = 0; mg < 4; ++mg) {
-                const int row = mb * 128 + mg * 32 + lane;
-                uint32_t word = 0;
-                for (int s = 0; s < 4; ++s) {
-                    const int col = kb * 4 + s;
-                    const uint32_t v = (row < M && col < sfk) ? sfa[(int64_t)row * sfk + col] : kUnitScale;
-                    word |= v << (8 * s);
-                }
-                w[mg] = word;
-            }
+// One CTA packs one 128-row block of scales for 16 consecutive k-blocks: it reads
+// the 128 x 64-byte slab of the row-major scale matrix (rows of the block, scale
+// columns 64*g .. 64*g+63) into shared memory with coalesced loads, then writes the
+// 16 resulting 512-byte blocks (byte lane*16 + Mgroup*4 + sfk) with coalesced
+// 16-byte stores.  Blocks of SFA: one per 128 rows of A; blocks of SFB: one per
+// 128-row half of each tile_n-wide tile column.  Rows outside the matrix (or
+// beyond tile_n in a tile column) and scale columns beyond SFK read as 127.
+constexpr int PACK_KB = 16;                 // k-blocks per CTA
+constexpr int PACK_COLS = PACK_KB * 4;      // scale bytes per row per CTA
+
+__global__ void __launch_bounds__(256) sf_pack_kernel(const uint8_t *__restrict__ sfa, const uint8_t *__restrict__ sfb,
+                                                      uint8_t *__restrict__ out_a, uint8_t *__restrict__ out_b, int M,
+                                                      int N, int sfk, int row_blocks, int tiles_n, int num_kb,
+                                                      int tile_n) {
+    __shared__ __align__(16) uint8_t slab[128][PACK_COLS];
+    const int kb_groups = (num_kb + PACK_KB - 1) / PACK_KB;
+    const int halves = (tile_n + 127) / 128;
+    const int a_ctas = row_blocks * kb_groups;
+    int cta = blockIdx.x;
+    const bool is_a = cta < a_ctas;
+    if (!is_a) cta -= a_ctas;
+    const int g = cta % kb_groups;                  // k-block group
+    const int blk_row = cta / kb_groups;            // SFA: 128-row block; SFB: tn * halves + h
+    const uint8_t *src = is_a ? sfa : sfb;
+    // rows of this block in the scale matrix and how many of them are real
+    int row0, valid;
+    if (is_a) {
+        row0 = blk_row * 128;
+        valid = min(128, M - row0);
+    } else {
+        const int tn = blk_row / halves, h = blk_row % halves;
+        row0 = tn * tile_n + h * 128;
+        valid = min(min(128, tile_n - h * 128), N - row0);
+    }
+    const int col0 = g * PACK_COLS;
+    const bool vec = (sfk % 16 == 0) && ((reinterpret_cast<uintptr_t>(src) & 15) == 0) && col0 + PACK_COLS <= sfk;
+    // load: 128 rows x 64 bytes = 512 chunks of 16 bytes, two per thread
+    for (int c = threadIdx.x; c < 128 * (PACK_COLS / 16); c += blockDim.x) {
+        const int r = c / (PACK_COLS / 16), q = c % (PACK_COLS / 16);
+        uint4 v;
+        if (r < valid && vec) {
+            v = *reinterpret_cast<const uint4 *>(src + (int64_t)(row0 + r) * sfk + col0 + 16 * q);
         } else {
-            const int h = (int)(blk % halves);
-            const int kb = (int)((blk / halves) % num_kb);
-            const int tn = (int)(blk / halves / num_kb);
-            for (int mg = 0; mg < 4; ++mg) {
-                const int in_tile = h * 128 + mg * 32 + lane;
-                const int row = tn * tile_n + in_tile;
-                uint32_t word = 0;
-                for (int s = 0; s < 4; ++s) {
-                    const int col = kb * 4 + s;
-                    const uint32_t v =
-                        (in_tile < tile_n && row < N && col < sfk) ? sfb[(int64_t)row * sfk + col] : kUnitScale;
-                    word |= v << (8 * s);
-                }
-                w[mg] = word;
+            uint8_t b[16];
+            for (int e = 0; e < 16; ++e) {
+                const int col = col0 + 16 * q + e;
+                b[e] = (r < valid && col < sfk) ? src[(int64_t)(row0 + r) * sfk + col] : kUnitScale;
             }
+            memcpy(&v, b, 16);
         }
-        uint8_t *dst = (is_a ? out_a : out_b) + blk * 512 + lane * 16;
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4 *>(&slab[r][16 * q]) = v;
+    }
+    __syncthreads();
+    // store: PACK_KB blocks of 512 bytes = 32 lanes x 16 bytes each
+    uint8_t *dst_base = is_a ? out_a : out_b;
+    for (int u = threadIdx.x; u < PACK_KB * 32; u += blockDim.x) {
+        const int kbl = u / 32, lane = u % 32;
+        const int kb = g * PACK_KB + kbl;
+        if (kb >= num_kb) continue;
+        uint32_t w[4];
+        for (int mg = 0; mg < 4; ++mg) w[mg] = *reinterpret_cast<const uint32_t *>(&slab[mg * 32 + lane][4 * kbl]);
+        int64_t blk;
+        if (is_a) {
+            blk = (int64_t)blk_row * num_kb + kb;
+        } else {
+            const int tn = blk_row / halves, h = blk_row % halves;
+            blk = ((int64_t)tn * num_kb + kb) * halves + h;
+        }
+        *reinterpret_cast<uint4 *>(dst_base + blk * 512 + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -122,12 +146,12 @@ cudaError_t mxf8_max_active_clusters(int cta_group, int out_bf16, int *clusters)
 
 cudaError_t mxf8_pack(const uint8_t *sfa, const uint8_t *sfb, uint8_t *out_a, uint8_t *out_b, int M, int N, int K,
                       int row_blocks, int tiles_n, int tile_n, int num_kb, int sm_count, cudaStream_t stream) {
+    (void)sm_count;
     const int sfk = (K + 31) / 32;
-    const int64_t rows = ((int64_t)row_blocks * num_kb + (int64_t)tiles_n * num_kb * ((tile_n + 127) / 128)) * 32;
-    int blocks = (int)((rows + 255) / 256);
-    if (blocks > 8 * sm_count) blocks = 8 * sm_count;
-    sf_pack_kernel<<<blocks, 256, 0, stream>>>(sfa, sfb, out_a, out_b, M, N, sfk, row_blocks, tiles_n, num_kb,
-                                               tile_n);
+    const int kb_groups = (num_kb + PACK_KB - 1) / PACK_KB;
+    const int64_t ctas = (int64_t)(row_blocks + tiles_n * ((tile_n + 127) / 128)) * kb_groups;
+    sf_pack_kernel<<<(unsigned)ctas, 256, 0, stream>>>(sfa, sfb, out_a, out_b, M, N, sfk, row_blocks, tiles_n, num_kb,
+                                                       tile_n);
     return cudaGetLastError();
 }
 
