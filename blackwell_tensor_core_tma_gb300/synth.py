@@ -1,8 +1,8 @@
 """Seeded synthetic inputs for D = A·B + C.
 
 This module is shared by the CUDA path and the CPU oracle: it produces the
-operand *bit patterns* (bf16 / fp16 / e4m3 codes, UE8M0 scale codes, fp32 C)
-and nothing else.  It contains none of the multiply-accumulate arithmetic.
+operand *bit patterns* (bf16 / fp16 / e4m3 / e2m1 codes, UE8M0 and UE4M3
+scale codes, fp32 C) and nothing else.  It contains none of the multiply-accumulate arithmetic.
 
 Random numbers
     A counter-based splitmix64 stream (Steele, Lea & Flood, "Fast splittable
@@ -16,12 +16,17 @@ Distributions
     N(0, sigma): Box & Muller (1958), two stream outputs per sample, evaluated
     in fp64 and rounded to fp32 (sigma is the standard deviation).
     UE8M0 scale 2**e with e uniform over {-4, ..., 4}: code = e + 127.
+    UE4M3 scale (1 + m/8) * 2**e with e uniform over {-4, ..., 4} and m over
+    {0, ..., 7}: code = (e + 7) << 3 | m (two stream outputs per code).
 
 Rounding of operands (round to nearest, ties to even, from an fp32 sample)
     bf16 : the upper half of the binary32 pattern after RNE on bit 16.
     fp16 : IEEE binary16 (numpy's correctly rounded conversion).
     e4m3 : OCP 8-bit floating point (E4M3: bias 7, no infinities, max 448,
            S.1111.111 is NaN), saturating to +-448.
+    e2m1 : OCP 4-bit floating point (E2M1: bias 1, values 0, 0.5, 1, 1.5, 2,
+           3, 4, 6 and their negatives), saturating to +-6; stored two per
+           byte, element 2t in the low nibble of byte t of the storage order.
 """
 
 from __future__ import annotations
@@ -97,6 +102,19 @@ def ue8m0_codes(seed: int, tensor: int, n: int, lo: int = -4, hi: int = 4) -> np
     return out
 
 
+def ue4m3_codes(seed: int, tensor: int, n: int, lo: int = -4, hi: int = 4) -> np.ndarray:
+    """n UE4M3 codes of (1 + m/8) * 2**e, e uniform over {lo..hi}, m over {0..7}."""
+    span = np.uint64(hi - lo + 1)
+    out = np.empty(n, dtype=np.uint8)
+    for s in range(0, n, _CHUNK):
+        c = min(_CHUNK, n - s)
+        x = stream(seed, tensor, 2 * s, 2 * c) >> np.uint64(32)
+        e = ((x[0::2] * span) >> np.uint64(32)).astype(np.int64) + lo
+        m = ((x[1::2] * np.uint64(8)) >> np.uint64(32)).astype(np.int64)
+        out[s:s + c] = ((e + 7) << 3 | m).astype(np.uint8)
+    return out
+
+
 # ---------------------------------------------------------------- rounding
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -133,7 +151,43 @@ def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
     return (code.astype(np.uint8) | sign).astype(np.uint8)
 
 
+E2M1_MAGNITUDES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def f32_to_e2m1_bits(x: np.ndarray) -> np.ndarray:
+    """RNE fp32 -> OCP E2M1 codes (one per uint8, low 4 bits), saturating to +-6."""
+    x = np.ascontiguousarray(x, dtype=np.float32).astype(np.float64)
+    sign = (np.signbit(x)).astype(np.uint8) << np.uint8(3)
+    a = np.abs(x)
+    _, e2 = np.frexp(np.where(a > 0, a, 1.0))          # a = m * 2**e2, m in [0.5, 1)
+    ex = np.maximum(e2 - 1, 0)                          # unbiased exponent, the subnormal shares 0
+    q = np.ldexp(1.0, ex - 1)                           # spacing of the 1-bit mantissa grid
+    r = np.minimum(np.rint(a / q) * q, 6.0)             # ties to even, then satfinite
+    code = np.searchsorted(E2M1_MAGNITUDES, r)          # r is one of the magnitudes
+    return (code.astype(np.uint8) | sign).astype(np.uint8)
+
+
+def pack_e2m1(codes: np.ndarray) -> np.ndarray:
+    """Pack E2M1 codes two per byte along the last axis (even element in the low nibble)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    if c.shape[-1] % 2:
+        raise ValueError("the packed axis needs an even length")
+    return (c[..., 0::2] & np.uint8(0xF)) | ((c[..., 1::2] & np.uint8(0xF)) << np.uint8(4))
+
+
+def unpack_e2m1(packed: np.ndarray) -> np.ndarray:
+    """Inverse of pack_e2m1: one code per uint8."""
+    p = np.ascontiguousarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = p & np.uint8(0xF)
+    out[..., 1::2] = p >> np.uint8(4)
+    return out
+
+
 # ---------------------------------------------------------------- workloads
+
+# scale modes (the C ABI's block_scaled argument)
+SCALE_NONE, SCALE_UE8M0_32, SCALE_UE4M3_16 = 0, 1, 2
 
 @dataclasses.dataclass(frozen=True)
 class Workload:
@@ -141,8 +195,10 @@ class Workload:
 
     A is M x K, row-major when ``a_row_major`` (else column-major); B is K x N,
     column-major unless ``b_row_major`` (column-major K x N = N rows of K).
-    ``ab`` is "bf16", "f16" or "e4m3"; ``dist`` "uniform" or "normal" with
-    ``sigma``; ``c`` "zero" or "normal"; ``d`` "f32" or "bf16".
+    ``ab`` is "bf16", "f16", "e4m3" or "e2m1"; ``dist`` "uniform" or "normal"
+    with ``sigma``; ``c`` "zero" or "normal"; ``d`` "f32" or "bf16".
+    ``block_scaled`` is a scale mode: 0 none, 1 (or True) UE8M0 per 32 K
+    elements, 2 UE4M3 per 16.
     """
     name: str
     M: int
@@ -154,7 +210,7 @@ class Workload:
     c: str
     d: str
     seed: int
-    block_scaled: bool = False
+    block_scaled: int = SCALE_NONE
     a_row_major: bool = True
     b_row_major: bool = False
 
@@ -163,8 +219,12 @@ class Workload:
         return 2 * self.M * self.N * self.K
 
     @property
+    def sf_block(self) -> int:
+        return 16 if int(self.block_scaled) == SCALE_UE4M3_16 else 32
+
+    @property
     def sfk(self) -> int:
-        return (self.K + 31) // 32
+        return -(-self.K // self.sf_block)
 
 
 WORKLOADS = {
@@ -174,7 +234,12 @@ WORKLOADS = {
         Workload("f16_4000x3000x2056_f32out", 4000, 3000, 2056, "f16", "normal", 0.5, "normal", "f32", 2),
         Workload("bf16_8192x8192x8192_bf16out", 8192, 8192, 8192, "bf16", "uniform", 1.0, "normal", "bf16", 3),
         Workload("mxf8e4m3_8192x8192x8192_c0_f32out", 8192, 8192, 8192, "e4m3", "normal", 1.0, "zero", "f32", 4,
-                 block_scaled=True),
+                 block_scaled=SCALE_UE8M0_32),
+        # 4-bit operands with two (UE8M0 per 32) or four (UE4M3 per 16) scales per 64-element MMA step
+        Workload("mxf4e2m1_8192x8192x8192_c0_f32out", 8192, 8192, 8192, "e2m1", "normal", 1.0, "zero", "f32", 5,
+                 block_scaled=SCALE_UE8M0_32),
+        Workload("nvf4e2m1_8192x8192x8192_c0_f32out", 8192, 8192, 8192, "e2m1", "normal", 1.0, "zero", "f32", 6,
+                 block_scaled=SCALE_UE4M3_16),
     ]
 }
 
@@ -197,6 +262,8 @@ def _operand(w: Workload, tensor: int, n: int) -> np.ndarray:
         return f32_to_f16_bits(x)
     if w.ab == "e4m3":
         return f32_to_e4m3_bits(np.clip(x, -448.0, 448.0))
+    if w.ab == "e2m1":
+        return f32_to_e2m1_bits(x)
     raise ValueError(w.ab)
 
 
@@ -205,17 +272,27 @@ def make_inputs(w: Workload) -> dict:
 
     Shapes follow the memory layout: A is (M, K) when row-major, else (K, M);
     B is (N, K) when column-major, else (K, N); C is (M, N) fp32 row-major;
-    SFA is (M, ceil(K/32)) and SFB is (N, ceil(K/32)), both row-major u8.
+    SFA is (M, sfk) and SFB is (N, sfk), sfk = ceil(K / block), both row-major
+    u8.  e2m1 operands are packed two per byte along the contiguous axis, which
+    halves its length (K must then be even for a K-major operand, M or N for an
+    M- or N-major one).
     """
     M, N, K = w.M, w.N, w.K
-    A = _operand(w, T_A, M * K).reshape((M, K) if w.a_row_major else (K, M))
-    B = _operand(w, T_B, K * N).reshape((K, N) if w.b_row_major else (N, K))
+
+    def operand(tensor, shape):
+        x = _operand(w, tensor, shape[0] * shape[1]).reshape(shape)
+        return pack_e2m1(x) if w.ab == "e2m1" else x
+
+    A = operand(T_A, (M, K) if w.a_row_major else (K, M))
+    B = operand(T_B, (K, N) if w.b_row_major else (N, K))
     if w.c == "zero":
         C = np.zeros((M, N), dtype=np.float32)
     else:
         C = normal(w.seed, T_C, M * N, 1.0).reshape(M, N)
     out = {"A": A, "B": B, "C": C}
-    if w.block_scaled:
-        out["SFA"] = ue8m0_codes(w.seed, T_SFA, M * w.sfk).reshape(M, w.sfk)
-        out["SFB"] = ue8m0_codes(w.seed, T_SFB, N * w.sfk).reshape(N, w.sfk)
+    mode = int(w.block_scaled)
+    if mode:
+        codes = ue4m3_codes if mode == SCALE_UE4M3_16 else ue8m0_codes
+        out["SFA"] = codes(w.seed, T_SFA, M * w.sfk).reshape(M, w.sfk)
+        out["SFB"] = codes(w.seed, T_SFB, N * w.sfk).reshape(N, w.sfk)
     return out

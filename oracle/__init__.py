@@ -7,8 +7,9 @@ calls it, and it imports nothing from the CUDA package.
 ``gemm`` / ``gemm_entries`` wrap the plain fp64 triple loop in
 ``gemm_oracle.c`` (the definition D[i][j] = C[i][j] + sum_k a[i][k] b[k][j]
 from "Tensor Core 数据布局的演进", overview, with the block-scaling rule of its
-section "Block-Scaled MMA 的 Scale Factors").  ``layouts`` holds the pages'
-register-fragment and TMEM layout maps.
+section "Block-Scaled MMA 的 Scale Factors": one scale per 32 K elements
+(UE8M0, e4m3 or e2m1 operands) or per 16 (UE4M3, e2m1 operands)).
+``layouts`` holds the pages' register-fragment and TMEM layout maps.
 
 Parity pins (tests/test_oracle_*.py): exhaustive format decodes against
 torch/numpy conversions and the OCP/IEEE tables; A = I, rank-1, all-ones and
@@ -30,7 +31,11 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gemm_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-DTYPES = {"f16": 0, "bf16": 1, "e4m3": 2}
+DTYPES = {"f16": 0, "bf16": 1, "e4m3": 2, "e2m1": 3}
+
+# scale modes: none; UE8M0 per 32 K elements; UE4M3 per 16 K elements
+SCALE_NONE, SCALE_UE8M0_32, SCALE_UE4M3_16 = 0, 1, 2
+SCALE_BLOCK = {SCALE_UE8M0_32: 32, SCALE_UE4M3_16: 16}
 
 _lib = None
 
@@ -61,7 +66,8 @@ def lib():
                                           vp, vp, vp, ctypes.c_int, i64, vp, vp, dp, dp, ctypes.c_int]
         L.oracle_gemm_entries.restype = ctypes.c_int
         for name, arg in [("oracle_decode_bf16", ctypes.c_uint16), ("oracle_decode_f16", ctypes.c_uint16),
-                          ("oracle_decode_e4m3", ctypes.c_uint8), ("oracle_decode_ue8m0", ctypes.c_uint8)]:
+                          ("oracle_decode_e4m3", ctypes.c_uint8), ("oracle_decode_ue8m0", ctypes.c_uint8),
+                          ("oracle_decode_e2m1", ctypes.c_uint8), ("oracle_decode_ue4m3", ctypes.c_uint8)]:
             f = getattr(L, name)
             f.argtypes = [arg]
             f.restype = ctypes.c_double
@@ -76,7 +82,8 @@ def threads(nthreads: int = 0) -> int:
 
 
 def decode(codes, dtype: str) -> np.ndarray:
-    """fp64 values of bf16 / f16 / e4m3 / ue8m0 codes (element by element)."""
+    """fp64 values of bf16 / f16 / e4m3 / ue8m0 / ue4m3 codes, or of e2m1 codes
+    given one per element in the low 4 bits (element by element)."""
     f = getattr(lib(), "oracle_decode_" + dtype)
     flat = np.asarray(codes).ravel()
     return np.array([f(int(c)) for c in flat], dtype=np.float64).reshape(np.shape(codes))
@@ -86,33 +93,41 @@ def _ptr(a):
     return None if a is None else a.ctypes.data
 
 
+def _packed_bytes(n: int, dtype: str) -> int:
+    """Bytes holding n elements: e2m1 two per byte (element 2t in the low nibble of byte t)."""
+    return (n + 1) // 2 if dtype == "e2m1" else n
+
+
 def _check_operands(A, B, C, SFA, SFB, M, N, K, dtype, block_scaled):
-    width = np.uint8 if dtype == "e4m3" else np.uint16
+    width = np.uint8 if dtype in ("e4m3", "e2m1") else np.uint16
     A = np.ascontiguousarray(A, dtype=width)
     B = np.ascontiguousarray(B, dtype=width)
-    if A.size != M * K or B.size != K * N:
+    if A.size != _packed_bytes(M * K, dtype) or B.size != _packed_bytes(K * N, dtype):
         raise ValueError("operand sizes do not match M, N, K")
     if C is not None:
         C = np.ascontiguousarray(C, dtype=np.float32)
         if C.size != M * N:
             raise ValueError("C size does not match M, N")
-    sfk = (K + 31) // 32
-    if block_scaled:
+    mode = int(block_scaled)
+    if mode:
+        sfk = -(-K // SCALE_BLOCK[mode])
         SFA = np.ascontiguousarray(SFA, dtype=np.uint8)
         SFB = np.ascontiguousarray(SFB, dtype=np.uint8)
         if SFA.size != M * sfk or SFB.size != N * sfk:
-            raise ValueError("scale-factor sizes do not match M, N, ceil(K/32)")
+            raise ValueError("scale-factor sizes do not match M, N, ceil(K/block)")
     else:
         SFA = SFB = None
     return A, B, C, SFA, SFB
 
 
 def gemm(A, B, C, M: int, N: int, K: int, dtype: str, a_row_major: bool = True,
-         b_row_major: bool = False, SFA=None, SFB=None, block_scaled: bool = False,
+         b_row_major: bool = False, SFA=None, SFB=None, block_scaled: int = 0,
          rows: tuple | None = None, nthreads: int = 0):
     """(D, S) as fp64 arrays of shape (rows, N): D = C + sum_k a b, S = sum_k |a b|.
 
-    ``rows`` = (row0, row1) restricts the work to a row slab (default: all).
+    ``block_scaled``: 0 (or False) none, 1 (or True) UE8M0 per 32 K, 2 UE4M3
+    per 16 K.  ``rows`` = (row0, row1) restricts the work to a row slab
+    (default: all).
     """
     A, B, C, SFA, SFB = _check_operands(A, B, C, SFA, SFB, M, N, K, dtype, block_scaled)
     r0, r1 = rows if rows is not None else (0, M)
@@ -127,7 +142,7 @@ def gemm(A, B, C, M: int, N: int, K: int, dtype: str, a_row_major: bool = True,
 
 
 def gemm_entries(A, B, C, M: int, N: int, K: int, dtype: str, rows, cols, a_row_major: bool = True,
-                 b_row_major: bool = False, SFA=None, SFB=None, block_scaled: bool = False,
+                 b_row_major: bool = False, SFA=None, SFB=None, block_scaled: int = 0,
                  nthreads: int = 0):
     """(D, S) at the listed (row, col) entries, each computed on its own."""
     A, B, C, SFA, SFB = _check_operands(A, B, C, SFA, SFB, M, N, K, dtype, block_scaled)

@@ -17,11 +17,15 @@
  *
  * Block scaling ("Tensor Core 数据布局的演进", section "Block-Scaled MMA 的
  * Scale Factors"): SFA[m][sfk] scales the elements of row m of A inside the
- * sfk-th K block, SFB[n][sfk] the elements of column n of B.  The K block is
- * 32 elements (one UE8M0 scale per 32 contiguous K elements), so
- *     a[i][k] = e4m3(A[i][k]) * 2^(SFA[i][k/32] - 127)
- *     b[k][j] = e4m3(B[k][j]) * 2^(SFB[j][k/32] - 127)
- * SFA is stored M x ceil(K/32) row-major, SFB N x ceil(K/32) row-major.
+ * sfk-th K block, SFB[n][sfk] the elements of column n of B:
+ *     a[i][k] = A[i][k] * sf(SFA[i][k/blk])
+ *     b[k][j] = B[k][j] * sf(SFB[j][k/blk])
+ * Two scale modes (the same section: a 32-bit scale word holds one, two or
+ * four scales per row, scale_vec::1X / 2X / 4X):
+ *   block_scaled = 1  UE8M0 scales, blk = 32: e4m3 operands (one scale per
+ *                     32-element MMA K step) or e2m1 operands (two per 64);
+ *   block_scaled = 2  UE4M3 scales, blk = 16: e2m1 operands (four per 64).
+ * SFA is stored M x ceil(K/blk) row-major, SFB N x ceil(K/blk) row-major.
  *
  * Operand storage: A is M x K, row-major (A[i*K+k]) when a_row_major, else
  * column-major (A[k*M+i]).  B is K x N, row-major (B[k*N+j]) when b_row_major,
@@ -32,7 +36,13 @@
  *   fp16  IEEE-754 binary16 (1/5/10, bias 15, subnormals, inf/NaN at 31);
  *   e4m3  OCP 8-bit floating point E4M3 (1/4/3, bias 7, subnormals,
  *         no infinities, S.1111.111 is NaN, max normal 448);
- *   ue8m0 OCP microscaling scale: 2^(code-127), code 255 is NaN.
+ *   e2m1  OCP 4-bit floating point E2M1 (1/2/1, bias 1, one subnormal
+ *         0.5, no infinities or NaN, max 6), two per byte: element 2t in
+ *         bits 0..3 of byte t, element 2t+1 in bits 4..7 (t counts along
+ *         the storage order's contiguous dimension);
+ *   ue8m0 OCP microscaling scale: 2^(code-127), code 255 is NaN;
+ *   ue4m3 unsigned E4M3 scale: the 7 low bits read as a non-negative e4m3
+ *         value (0x7F is NaN); codes with bit 7 set have no value (NaN).
  */
 #include <math.h>
 #include <stddef.h>
@@ -43,7 +53,8 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 2 };
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 2, ORACLE_E2M1 = 3 };
+enum { SCALE_NONE = 0, SCALE_UE8M0_32 = 1, SCALE_UE4M3_16 = 2 };
 
 double oracle_decode_bf16(uint16_t h) {
     uint32_t u = (uint32_t)h << 16;
@@ -84,26 +95,50 @@ double oracle_decode_ue8m0(uint8_t c) {
     return c == 255 ? NAN : ldexp(1.0, (int)c - 127);
 }
 
+/* one E2M1 code in the low 4 bits of c */
+double oracle_decode_e2m1(uint8_t c) {
+    int sign = (c >> 3) & 1;
+    int e = (c >> 1) & 0x3;
+    int m = c & 0x1;
+    double v = e == 0 ? 0.5 * m                            /* subnormal: m/2 * 2^(1-1) */
+                      : ldexp(2.0 + m, e - 2);              /* (1 + m/2) * 2^(e-1) */
+    return sign ? -v : v;
+}
+
+double oracle_decode_ue4m3(uint8_t c) {
+    if (c & 0x80) return NAN;
+    return oracle_decode_e4m3(c);
+}
+
+/* element idx (in storage order) of an operand */
 static double decode(int dtype, const void *p, int64_t idx) {
     switch (dtype) {
     case ORACLE_F16: return oracle_decode_f16(((const uint16_t *)p)[idx]);
     case ORACLE_BF16: return oracle_decode_bf16(((const uint16_t *)p)[idx]);
+    case ORACLE_E2M1: {
+        uint8_t byte = ((const uint8_t *)p)[idx / 2];
+        return oracle_decode_e2m1(idx % 2 ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xF));
+    }
     default: return oracle_decode_e4m3(((const uint8_t *)p)[idx]);
     }
 }
 
 typedef struct {
-    int64_t M, N, K, sfk;
+    int64_t M, N, K, sfk, blk;
     int dtype, a_row_major, b_row_major, block_scaled;
     const void *A, *B;
     const uint8_t *SFA, *SFB;
 } problem;
 
+static double scale(const problem *p, uint8_t code) {
+    return p->block_scaled == SCALE_UE4M3_16 ? oracle_decode_ue4m3(code) : oracle_decode_ue8m0(code);
+}
+
 /* a[i][k] with its block scale applied */
 static double a_elem(const problem *p, int64_t i, int64_t k) {
     int64_t idx = p->a_row_major ? i * p->K + k : k * p->M + i;
     double v = decode(p->dtype, p->A, idx);
-    if (p->block_scaled) v *= oracle_decode_ue8m0(p->SFA[i * p->sfk + k / 32]);
+    if (p->block_scaled) v *= scale(p, p->SFA[i * p->sfk + k / p->blk]);
     return v;
 }
 
@@ -111,8 +146,23 @@ static double a_elem(const problem *p, int64_t i, int64_t k) {
 static double b_elem(const problem *p, int64_t k, int64_t j) {
     int64_t idx = p->b_row_major ? k * p->N + j : j * p->K + k;
     double v = decode(p->dtype, p->B, idx);
-    if (p->block_scaled) v *= oracle_decode_ue8m0(p->SFB[j * p->sfk + k / 32]);
+    if (p->block_scaled) v *= scale(p, p->SFB[j * p->sfk + k / p->blk]);
     return v;
+}
+
+/* Fill *p; -1 when the operand type and scale mode do not go together:
+ * fp16 / bf16 take no scales, e4m3 none or UE8M0 / 32, e2m1 any mode. */
+static int make_problem(problem *p, int64_t M, int64_t N, int64_t K, int dtype, const void *A, int a_row_major,
+                        const void *B, int b_row_major, const uint8_t *SFA, const uint8_t *SFB, int block_scaled) {
+    if (block_scaled < SCALE_NONE || block_scaled > SCALE_UE4M3_16) return -1;
+    if (dtype < ORACLE_F16 || dtype > ORACLE_E2M1) return -1;
+    if (block_scaled && (!SFA || !SFB)) return -1;
+    if (dtype == ORACLE_E4M3 && block_scaled != SCALE_NONE && block_scaled != SCALE_UE8M0_32) return -1;
+    if (dtype < ORACLE_E4M3 && block_scaled != SCALE_NONE) return -1;
+    int64_t blk = block_scaled == SCALE_UE4M3_16 ? 16 : 32;
+    problem q = {M, N, K, (K + blk - 1) / blk, blk, dtype, a_row_major, b_row_major, block_scaled, A, B, SFA, SFB};
+    *p = q;
+    return 0;
 }
 
 static int set_threads(int nthreads) {
@@ -138,8 +188,8 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K, int dtype,
                 const float *C, const uint8_t *SFA, const uint8_t *SFB, int block_scaled,
                 int64_t row0, int64_t row1, double *D, double *S, int nthreads) {
     if (M < 0 || N < 0 || K < 0 || row0 < 0 || row1 > M || row0 > row1) return -1;
-    if (block_scaled && (dtype != ORACLE_E4M3 || !SFA || !SFB)) return -1;
-    problem p = {M, N, K, (K + 31) / 32, dtype, a_row_major, b_row_major, block_scaled, A, B, SFA, SFB};
+    problem p;
+    if (make_problem(&p, M, N, K, dtype, A, a_row_major, B, b_row_major, SFA, SFB, block_scaled)) return -1;
     int64_t rows = row1 - row0;
     /* decode the operands once into plain fp64 matrices: ad (rows x K), bd (K x N) */
     double *ad = (double *)malloc(sizeof(double) * (size_t)(rows * K > 0 ? rows * K : 1));
@@ -184,10 +234,10 @@ int oracle_gemm_entries(int64_t M, int64_t N, int64_t K, int dtype,
                         int64_t n, const int64_t *rows, const int64_t *cols,
                         double *D, double *S, int nthreads) {
     if (M < 0 || N < 0 || K < 0 || n < 0) return -1;
-    if (block_scaled && (dtype != ORACLE_E4M3 || !SFA || !SFB)) return -1;
+    problem p;
+    if (make_problem(&p, M, N, K, dtype, A, a_row_major, B, b_row_major, SFA, SFB, block_scaled)) return -1;
     for (int64_t e = 0; e < n; ++e)
         if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;
-    problem p = {M, N, K, (K + 31) / 32, dtype, a_row_major, b_row_major, block_scaled, A, B, SFA, SFB};
     int nt = set_threads(nthreads);
     #pragma omp parallel for num_threads(nt) schedule(dynamic, 64)
     for (int64_t e = 0; e < n; ++e) {

@@ -2,7 +2,8 @@
 
 Decoders are checked exhaustively against independent conversions (torch and
 numpy) and against fixed points of the format definitions (IEEE 754 binary16,
-bf16 = upper half of binary32, OCP FP8 E4M3, OCP UE8M0).  The generator's
+bf16 = upper half of binary32, OCP FP8 E4M3, OCP UE8M0, the OCP MX FP4 E2M1
+value table).  The generator's
 encoders are pinned by decode -> encode identity on every finite code.
 """
 import numpy as np
@@ -109,3 +110,56 @@ def test_bf16_ulp_is_grid_spacing(oracle_mod):
     assert oracle_mod.bf16_ulp(1.0) == 2.0 ** -7
     assert oracle_mod.bf16_ulp(-3.0) == 2.0 ** -6
     assert oracle_mod.bf16_ulp(0.0) == 2.0 ** -133
+
+
+# OCP Microscaling Formats (MX) v1.0, FP4 E2M1: the eight magnitudes of codes
+# 0b0000 .. 0b0111 (bias 1; 0b0001 is the one subnormal), bit 3 the sign
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_decode_exhaustive(oracle_mod):
+    codes = np.arange(16, dtype=np.uint8)
+    ours = oracle_mod.decode(codes, "e2m1")
+    ref = np.array(E2M1_TABLE + [-v for v in E2M1_TABLE])
+    assert _same(ours, ref)
+    # only the low nibble is the code
+    assert _same(oracle_mod.decode(codes | np.uint8(0xA0), "e2m1"), ref)
+
+
+def test_ue4m3_decode_exhaustive(oracle_mod):
+    codes = np.arange(128, dtype=np.uint8)
+    ours = oracle_mod.decode(codes, "ue4m3")
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert _same(ours, ref)                      # 0x7F (exponent and mantissa all ones) is NaN
+    assert float(oracle_mod.decode(np.array([0x38], np.uint8), "ue4m3")[0]) == 1.0
+    assert np.all(np.isnan(oracle_mod.decode(np.arange(128, 256, dtype=np.uint8), "ue4m3")))
+
+
+def test_e2m1_encode_is_nearest_ties_to_even(oracle_mod):
+    # brute force: the nearest representable magnitude, on a tie the one with an
+    # even code (mantissa bit 0), beyond 6 the largest (satfinite)
+    rng = np.random.default_rng(4)
+    ties = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 7.0, 1e9]
+    x = np.concatenate([rng.uniform(-8, 8, 20000), rng.standard_normal(20000), ties]).astype(np.float32)
+    x = np.concatenate([x, -x])
+    table = np.array(E2M1_TABLE)
+    a = np.abs(x.astype(np.float64))
+    dist = np.abs(a[:, None] - table[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    cand = dist == best
+    even = cand & (np.arange(8)[None, :] % 2 == 0)
+    code = np.where(even.any(axis=1), np.argmax(even, axis=1), np.argmax(cand, axis=1))
+    code = np.where(a > 6.0, 7, code)
+    expect = code.astype(np.uint8) | (np.signbit(x).astype(np.uint8) << 3)
+    assert np.array_equal(synth.f32_to_e2m1_bits(x), expect)
+    # decode -> encode identity on every code
+    codes = np.arange(16, dtype=np.uint8)
+    assert np.array_equal(synth.f32_to_e2m1_bits(oracle_mod.decode(codes, "e2m1").astype(np.float32)), codes)
+
+
+def test_e2m1_packing():
+    codes = np.arange(16, dtype=np.uint8).reshape(2, 8)
+    packed = synth.pack_e2m1(codes)
+    assert packed.shape == (2, 4)
+    assert packed[0, 0] == 0x10 and packed[0, 3] == 0x76 and packed[1, 0] == 0x98
+    assert np.array_equal(synth.unpack_e2m1(packed), codes)

@@ -156,3 +156,96 @@ def test_rejects_bad_arguments(oracle_mod):
                         block_scaled=True)
     with pytest.raises(ValueError):
         oracle_mod.gemm_entries(a, a, None, 4, 4, 4, "bf16", [4], [0])
+
+
+# ------------------------------------------------------------- 4-bit operands
+# OCP MX FP4 E2M1 magnitudes of codes 0..7 (bit 3 is the sign)
+E2M1_TABLE = [Fraction(0), Fraction(1, 2), Fraction(1), Fraction(3, 2), Fraction(2), Fraction(3),
+              Fraction(4), Fraction(6)]
+
+
+def _e2m1_value(code):
+    v = E2M1_TABLE[int(code) & 7]
+    return -v if int(code) & 8 else v
+
+
+def _scale_values(codes, mode):
+    """Exact scale values: UE8M0 2^(c-127); UE4M3 through torch's float8_e4m3fn."""
+    import torch
+    codes = np.asarray(codes, np.uint8)
+    if mode == 1:
+        return [[Fraction(2) ** (int(c) - 127) for c in row] for row in codes]
+    vals = torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).double().numpy()
+    return [[Fraction(float(v)) for v in row] for row in vals]
+
+
+def _pack_store(codes, row_major_of_logical):
+    """Logical (R, C) codes -> packed storage: rows of C when row_major, else rows of R."""
+    s = codes if row_major_of_logical else np.ascontiguousarray(codes.T)
+    return synth.pack_e2m1(s)
+
+
+@pytest.mark.parametrize("mode,K", [(1, 72), (2, 72), (2, 32)])
+@pytest.mark.parametrize("a_rm,b_rm", [(True, False), (True, True), (False, False), (False, True)])
+def test_e2m1_block_scaled_exact_rationals(oracle_mod, mode, K, a_rm, b_rm):
+    # every product and partial sum is a short dyadic (or, with UE4M3 scales,
+    # a short multiple of 2^-20) rational: compare with exact arithmetic
+    rng = np.random.default_rng(11 + mode + K)
+    M, N = 6, 4                                                # even, so column-wise packing works
+    blk = 32 if mode == 1 else 16
+    sfk = -(-K // blk)
+    a = rng.integers(0, 16, (M, K)).astype(np.uint8)           # logical a[i][k]
+    b = rng.integers(0, 16, (K, N)).astype(np.uint8)           # logical b[k][j]
+    if mode == 1:
+        sfa = rng.integers(122, 133, (M, sfk)).astype(np.uint8)
+        sfb = rng.integers(122, 133, (N, sfk)).astype(np.uint8)
+    else:
+        sfa = synth.ue4m3_codes(3, 3, M * sfk).reshape(M, sfk)
+        sfb = synth.ue4m3_codes(3, 4, N * sfk).reshape(N, sfk)
+    c = synth.normal(9, 2, M * N).reshape(M, N)
+    A = _pack_store(a, a_rm)                                   # (M, K/2) or (K, M/2)
+    B = _pack_store(b, b_rm)                                   # (K, N/2) or (N, K/2)
+    D, S = oracle_mod.gemm(A, B, c, M, N, K, "e2m1", a_row_major=a_rm, b_row_major=b_rm,
+                           SFA=sfa, SFB=sfb, block_scaled=mode)
+    sa, sb = _scale_values(sfa, mode), _scale_values(sfb, mode)
+    for i in range(M):
+        for j in range(N):
+            terms = [_e2m1_value(a[i, k]) * sa[i][k // blk] * _e2m1_value(b[k, j]) * sb[j][k // blk]
+                     for k in range(K)]
+            exact = Fraction(float(c[i, j])) + sum(terms)
+            sabs = sum(abs(t) for t in terms)
+            assert abs(Fraction(D[i, j]) - exact) <= Fraction(2.0 ** -50) * (sabs + abs(Fraction(float(c[i, j]))))
+            assert abs(Fraction(S[i, j]) - sabs) <= Fraction(2.0 ** -50) * sabs
+
+
+def test_e2m1_low_nibble_is_the_even_element(oracle_mod):
+    # A row 0 = [0, 1, 0, 0, ...]: only element k = 1 (high nibble of byte 0) is set
+    M, N, K = 2, 2, 32
+    a = np.zeros((M, K), np.uint8)
+    a[0, 1] = 0x2                                              # 1.0
+    b = np.zeros((K, N), np.uint8)
+    b[0, 0], b[1, 0] = 0x4, 0x5                                # b[0][0] = 2, b[1][0] = 3
+    one = np.full((M, 1), 127, np.uint8), np.full((N, 1), 127, np.uint8)
+    D, _ = oracle_mod.gemm(synth.pack_e2m1(a), synth.pack_e2m1(np.ascontiguousarray(b.T)), None, M, N, K,
+                           "e2m1", SFA=one[0], SFB=one[1], block_scaled=1)
+    assert D[0, 0] == 3.0 and D[1, 0] == 0.0
+
+
+@pytest.mark.parametrize("mode,unit", [(1, 127), (2, 0x38)])
+def test_e2m1_unit_scales_give_unscaled_product(oracle_mod, mode, unit):
+    w = synth.scaled(synth.WORKLOADS["nvf4e2m1_8192x8192x8192_c0_f32out"], 20, 12, 96, c="normal")
+    x = synth.make_inputs(w)
+    sfk = 96 // (32 if mode == 1 else 16)
+    D1, S1 = oracle_mod.gemm(x["A"], x["B"], x["C"], 20, 12, 96, "e2m1", SFA=np.full((20, sfk), unit, np.uint8),
+                             SFB=np.full((12, sfk), unit, np.uint8), block_scaled=mode)
+    D0, S0 = oracle_mod.gemm(x["A"], x["B"], x["C"], 20, 12, 96, "e2m1")
+    assert np.array_equal(D0, D1) and np.array_equal(S0, S1)
+
+
+def test_scale_mode_pairing_is_checked(oracle_mod):
+    a = np.zeros((4, 32), np.uint8)
+    sf = np.zeros((4, 2), np.uint8)
+    with pytest.raises(ValueError):                            # UE4M3 scales are for 4-bit operands only
+        oracle_mod.gemm(a, a, None, 4, 4, 32, "e4m3", SFA=sf, SFB=sf, block_scaled=2)
+    with pytest.raises(ValueError):                            # packed sizes: K/2 bytes per row
+        oracle_mod.gemm(a, a, None, 4, 4, 32, "e2m1", SFA=sf[:, :1], SFB=sf[:, :1], block_scaled=1)

@@ -99,3 +99,26 @@ def test_workload_table():
     w = synth.WORKLOADS[synth.HEADLINE]
     assert (w.M, w.N, w.K, w.ab, w.d, w.seed) == (8192, 8192, 8192, "bf16", "bf16", 3)
     assert w.flops == 2 * 8192 ** 3
+
+
+def test_ue4m3_codes():
+    c = synth.ue4m3_codes(5, 3, 1 << 18)
+    e, m = c >> 3, c & 7
+    assert c.max() < 0x80                                      # no sign bit
+    assert e.min() == 3 and e.max() == 11                      # 2^-4 .. 2^4
+    assert np.all(np.abs(np.bincount(e, minlength=16)[3:12] / c.size - 1.0 / 9) < 0.01)
+    assert np.all(np.abs(np.bincount(m, minlength=8) / c.size - 1.0 / 8) < 0.01)
+
+
+def test_make_inputs_e2m1():
+    w = synth.scaled(synth.WORKLOADS["nvf4e2m1_8192x8192x8192_c0_f32out"], 64, 48, 96)
+    x = synth.make_inputs(w)
+    assert x["A"].shape == (64, 48) and x["A"].dtype == np.uint8      # K/2 bytes per row
+    assert x["B"].shape == (48, 48)
+    assert x["SFA"].shape == (64, 6) and x["SFB"].shape == (48, 6)    # one scale per 16 K
+    codes = synth.unpack_e2m1(x["A"])
+    # N(0, 1) rounded to E2M1: zero is the most common code, 6 the saturated tail
+    assert set(np.unique(codes & 7)) <= set(range(8)) and (codes & 7).max() >= 5
+    w1 = synth.scaled(synth.WORKLOADS["mxf4e2m1_8192x8192x8192_c0_f32out"], 64, 48, 96)
+    x1 = synth.make_inputs(w1)
+    assert x1["SFA"].shape == (64, 3) and 123 <= x1["SFA"].min() and x1["SFA"].max() <= 131
