@@ -49,7 +49,16 @@ MEASURED_TRAFFIC = {
 KERNEL_SOURCES = {
     "f16": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_f16.cu"],
     "mxf8": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_mxf8.cu"],
+    "mxf4": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_mxf4.cu"],
+    "nvf4": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_nvf4.cu"],
 }
+
+
+def kernel_family(workload_name: str) -> str:
+    for fam in ("mxf8", "mxf4", "nvf4"):
+        if workload_name.startswith(fam):
+            return fam
+    return "f16"
 
 
 def kernel_source_hash(family: str = "f16") -> str:
@@ -65,12 +74,12 @@ def kernel_source_hash(family: str = "f16") -> str:
 
 def measured_traffic(workload_name: str):
     t = MEASURED_TRAFFIC.get(workload_name)
-    family = "mxf8" if workload_name.startswith("mxf8") else "f16"
-    if t is None or t["src"] != kernel_source_hash(family):
+    if t is None or t["src"] != kernel_source_hash(kernel_family(workload_name)):
         return None, None
     return t["bytes"], t["ncu"]
-# dense tensor-core rate of e4m3 relative to bf16 (nominal 4.5 vs 2.25 PFLOP/s)
-FP8_OVER_BF16 = 2.0
+# dense tensor-core rate of each operand type relative to bf16 (nominal GB300 figures:
+# bf16/fp16 2.25, fp8 4.5, fp4 13.5 PFLOP/s)
+OVER_BF16 = {"bf16": 1.0, "f16": 1.0, "e4m3": 2.0, "e2m1": 6.0}
 
 
 def load_peaks():
@@ -284,16 +293,17 @@ def run_ours(args, rank, world, local_rank):
 
     peaks, source = load_peaks()
     traffic, traffic_src = (args.traffic, "--traffic") if args.traffic is not None else measured_traffic(w.name)
-    peak = peaks["bf16_tflops"] * (FP8_OVER_BF16 if w.ab == "e4m3" else 1.0)
+    ratio = OVER_BF16[w.ab]
+    peak = peaks["bf16_tflops"] * ratio
     achieved = w.flops / (kernel_ms / 1e3) / 1e12
+    sf_bytes = x["SFA"].nbytes + x["SFB"].nbytes if w.block_scaled else 0
     roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_source": traffic_src,
-                "algorithmic_bytes": int(x["A"].nbytes + x["B"].nbytes + x["C"].nbytes +
+                "algorithmic_bytes": int(x["A"].nbytes + x["B"].nbytes + x["C"].nbytes + sf_bytes +
                                          w.M * w.N * (2 if w.d == "bf16" else 4)),
                 "peak_source": f"{source} bf16 burst (cuBLAS bf16 8192^3)" +
-                               (" x2 nominal fp8/bf16" if w.ab == "e4m3" else ""),
-                "frac_of_sustained": round(achieved / (peaks.get("bf16_tflops_sustained", peak) *
-                                                      (FP8_OVER_BF16 if w.ab == "e4m3" else 1.0)), 4),
+                               (f" x{ratio:g} nominal {w.ab}/bf16" if ratio != 1.0 else ""),
+                "frac_of_sustained": round(achieved / (peaks.get("bf16_tflops_sustained", peak) * ratio), 4),
                 "kernel": "gemm_tc_kernel",
                 "kernel_ms": round(kernel_ms, 5)}
 

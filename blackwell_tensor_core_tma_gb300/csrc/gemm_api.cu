@@ -44,12 +44,14 @@ struct gemm_plan {
     uint64_t timeout_ns;
     int fault;
     int *status;              // device word
-    int family;               // 0: fp16/bf16 kernel, 1: block-scaled e4m3 kernel
+    int family;               // GemmKind of the kernel: fp16/bf16, or block-scaled e4m3 / e2m1
     int splits;               // K slices per tile (1 = no split-K)
     int capacity;             // work units the persistent grid runs at once (CTAs or CTA pairs)
     int split_request;        // 0 = choose automatically, n >= 1 = asked for
     int tile_n;
+    int tile_k;               // K elements per stage
     int num_kb;
+    int sfa_stage_bytes, sfb_stage_bytes;   // block-scaled: packed scales per stage (per CTA)
     uint8_t *ws_a, *ws_b;     // block-scaled: packed scale factors (workspace)
     // device buffers of gemm_run_host (allocated on first use)
     void *hA, *hB, *hC, *hD;
@@ -77,7 +79,20 @@ bool encoder() {
     return g_encode != nullptr;
 }
 
-int elem_bytes(gemm_dtype t) { return t == GEMM_E4M3 ? 1 : (t == GEMM_F32 ? 4 : 2); }
+int elem_bits(gemm_dtype t) { return t == GEMM_E2M1 ? 4 : t == GEMM_E4M3 ? 8 : (t == GEMM_F32 ? 32 : 16); }
+
+// bytes of n elements of type t (4-bit elements are packed two per byte)
+size_t bytes_of(gemm_dtype t, int64_t n) { return (size_t)((n * elem_bits(t) + 7) / 8); }
+
+// the family's scale-format 1.0: pads the packed scales outside the matrices
+uint8_t unit_scale(int family) { return family == KIND_NVF4 ? 0x38 : 127; }
+
+// K elements sharing one scale
+int scale_block(int family) { return family == KIND_NVF4 ? 16 : 32; }
+
+const ScaledFamily &scaled_family(int family) {
+    return family == KIND_MXF4 ? family_mxf4() : (family == KIND_NVF4 ? family_nvf4() : family_mxf8());
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -106,16 +121,19 @@ gemm_status encode_maps(gemm_plan *p, const void *A, const void *B, const void *
     if (p->maps_valid && A == p->lastA && B == p->lastB && C == p->lastC && D == p->lastD) return GEMM_OK;
     if (!encoder()) return GEMM_ERR_CUDA;
     std::memset(p->maps, 0, 4 * sizeof(CUtensorMap));     // the scale-factor maps stay
-    const int eb = elem_bytes(p->ab);
-    const uint32_t bk = 128u / (uint32_t)eb;                       // K elements in a 128-byte row
+    // 4-bit operands are mapped as bytes (two K elements each, K-major only)
+    const bool fp4 = p->ab == GEMM_E2M1;
+    const int eb = fp4 ? 1 : elem_bits(p->ab) / 8;
+    const uint64_t k_units = fp4 ? (uint64_t)p->K / 2 : (uint64_t)p->K;
+    const uint32_t bk = 128u / (uint32_t)eb;                       // tensor-map elements in a 128-byte row
     const uint32_t b_rows = (uint32_t)(p->tile_n / p->cta_group);
     // K-major operand: [rows][K], box of bk x rows; MN-major operand: [K][rows], box one
     // 128-byte atom (atom elements) wide along the rows and bk deep along K
     const uint32_t atom = 128u / (uint32_t)eb;
     bool ok = (p->a_mn ? encode_2d(&p->maps[0], tma_dtype(p->ab), eb, A, p->M, p->K, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B)
-                       : encode_2d(&p->maps[0], tma_dtype(p->ab), eb, A, p->K, p->M, bk, TILE_M, CU_TENSOR_MAP_SWIZZLE_128B)) &&
+                       : encode_2d(&p->maps[0], tma_dtype(p->ab), eb, A, k_units, p->M, bk, TILE_M, CU_TENSOR_MAP_SWIZZLE_128B)) &&
               (p->b_mn ? encode_2d(&p->maps[1], tma_dtype(p->ab), eb, B, p->N, p->K, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B)
-                       : encode_2d(&p->maps[1], tma_dtype(p->ab), eb, B, p->K, p->N, bk, b_rows, CU_TENSOR_MAP_SWIZZLE_128B));
+                       : encode_2d(&p->maps[1], tma_dtype(p->ab), eb, B, k_units, p->N, bk, b_rows, CU_TENSOR_MAP_SWIZZLE_128B));
     if (ok && C)
         ok = encode_2d(&p->maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, p->N, p->M, EPI_COLS, 32,
                        CU_TENSOR_MAP_SWIZZLE_128B);
@@ -150,8 +168,8 @@ gemm_status configure_f16(gemm_plan *p) {
     p->cta_group = cg;
     p->stages = f16_stages(cg);
     p->smem = f16_smem_bytes(cg);
-    p->family = 0;
     p->tile_n = TILE_N;
+    p->tile_k = TILE_K16;
     p->num_kb = (int)((p->K + TILE_K16 - 1) / TILE_K16);
     p->tiles_m = (int)((p->M + TILE_M * cg - 1) / (TILE_M * cg));
     p->tiles_n = (int)((p->N + TILE_N - 1) / TILE_N);
@@ -167,39 +185,43 @@ gemm_status configure_f16(gemm_plan *p) {
     return GEMM_OK;
 }
 
-gemm_status configure_mxf8(gemm_plan *p) {
+gemm_status configure_scaled(gemm_plan *p) {
+    const ScaledFamily &fam = scaled_family(p->family);
     int cg = (p->M >= 1024 && p->N >= 1024) ? 2 : 1;
     if (p->flags & GEMM_FLAG_FORCE_1CTA) cg = 1;
     if (p->flags & GEMM_FLAG_FORCE_2CTA) cg = 2;
-    // single-CTA tiles hold 224 rows of B, not a whole number of 128-element atoms:
+    // single-CTA e4m3 tiles hold 224 rows of B, not a whole number of 128-element atoms:
     // an N-contiguous B needs CTA pairs (128 rows each)
     if (p->b_mn && cg == 1) {
         if (p->flags & GEMM_FLAG_FORCE_1CTA) return GEMM_ERR_UNSUPPORTED;
         cg = 2;
     }
     const int bf = p->d == GEMM_BF16;
-    if (mxf8_prepare(cg, bf) != cudaSuccess) return GEMM_ERR_CUDA;
-    p->family = 1;
+    if (fam.prepare(cg, bf) != cudaSuccess) return GEMM_ERR_CUDA;
+    const ScaledShape sh = fam.shape(cg);
     p->cta_group = cg;
-    p->tile_n = mxf8_tile_n(cg);
-    p->stages = mxf8_stages(cg);
-    p->smem = mxf8_smem_bytes(cg);
-    p->num_kb = (int)((p->K + 127) / 128);
+    p->tile_n = sh.tile_n;
+    p->stages = sh.stages;
+    p->smem = sh.smem;
+    p->tile_k = sh.bk;
+    p->sfa_stage_bytes = sh.sfa_bytes;
+    p->sfb_stage_bytes = sh.sfb_bytes;
+    p->num_kb = (int)((p->K + sh.bk - 1) / sh.bk);
     p->tiles_m = (int)((p->M + TILE_M * cg - 1) / (TILE_M * cg));
     p->tiles_n = (int)((p->N + p->tile_n - 1) / p->tile_n);
     p->tiles = p->tiles_m * p->tiles_n;
     int units = p->sm_count / cg;
     if (cg == 2) {
         int clusters = 0;
-        if (mxf8_max_active_clusters(cg, bf, &clusters) == cudaSuccess && clusters > 0) units = clusters;
+        if (fam.max_active_clusters(cg, bf, &clusters) == cudaSuccess && clusters > 0) units = clusters;
     }
     p->capacity = units;
     p->grid = cg * (p->tiles < units ? p->tiles : units);
     p->group_m = cg == 2 ? GB300_GROUP_M_PAIRS : GB300_GROUP_M_SINGLE;
-    // workspace: one 512-byte SFA block per (128 rows, 128 K), one SFB block per (tile column, 128 K)
+    // workspace: the packed SFA of every (128 rows, stage), the packed SFB of every (tile column, stage)
     const int row_blocks = p->tiles_m * cg;
-    const size_t a_bytes = mxf8_workspace_a(row_blocks, p->num_kb);
-    const size_t b_bytes = mxf8_workspace_b(p->tiles_n, p->num_kb);
+    const size_t a_bytes = (size_t)row_blocks * p->num_kb * sh.sfa_bytes;
+    const size_t b_bytes = (size_t)p->tiles_n * p->num_kb * sh.sfb_bytes;
     if (cudaMalloc(&p->ws_a, a_bytes) != cudaSuccess || cudaMalloc(&p->ws_b, b_bytes) != cudaSuccess) {
         cudaFree(p->ws_a);
         cudaFree(p->ws_b);
@@ -207,11 +229,10 @@ gemm_status configure_mxf8(gemm_plan *p) {
         return GEMM_ERR_CUDA;
     }
     if (!encoder()) return GEMM_ERR_CUDA;
-    const uint32_t b_block_rows = (uint32_t)(mxf8_sfb_block_bytes() / 128);
-    if (!encode_2d(&p->maps[4], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p->ws_a, 128, a_bytes / 128, 128, 4,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_2d(&p->maps[5], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p->ws_b, 128, b_bytes / 128, 128, b_block_rows,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_2d(&p->maps[4], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p->ws_a, 128, a_bytes / 128, 128,
+                   (uint32_t)(sh.sfa_bytes / 128), CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&p->maps[5], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p->ws_b, 128, b_bytes / 128, 128,
+                   (uint32_t)(sh.sfb_bytes / 128), CU_TENSOR_MAP_SWIZZLE_NONE))
         return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
@@ -257,16 +278,31 @@ gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K, 
                              gemm_dtype d, int a_row_major, int b_row_major, int block_scaled, unsigned flags) {
     if (!out || M <= 0 || N <= 0 || K <= 0) return GEMM_ERR_INVALID_ARG;
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_ARG;
-    if ((unsigned)ab > GEMM_F32 || (unsigned)c > GEMM_F32 || (unsigned)d > GEMM_F32) return GEMM_ERR_INVALID_ARG;
+    if ((unsigned)ab > GEMM_E2M1 || (unsigned)c > GEMM_E2M1 || (unsigned)d > GEMM_E2M1) return GEMM_ERR_INVALID_ARG;
+    if (block_scaled < GEMM_SCALE_NONE || block_scaled > GEMM_SCALE_UE4M3_16) return GEMM_ERR_INVALID_ARG;
     if ((flags & GEMM_FLAG_FORCE_1CTA) && (flags & GEMM_FLAG_FORCE_2CTA)) return GEMM_ERR_INVALID_ARG;
     if (c != GEMM_F32 || (d != GEMM_F32 && d != GEMM_BF16)) return GEMM_ERR_UNSUPPORTED;
-    if (block_scaled ? ab != GEMM_E4M3 : (ab != GEMM_F16 && ab != GEMM_BF16)) return GEMM_ERR_UNSUPPORTED;
+    // operand type and scale mode: fp16/bf16 unscaled, e4m3 with UE8M0 / 32, e2m1 with
+    // UE8M0 / 32 or UE4M3 / 16
+    int family;
+    if ((ab == GEMM_F16 || ab == GEMM_BF16) && block_scaled == GEMM_SCALE_NONE)
+        family = KIND_F16;
+    else if (ab == GEMM_E4M3 && block_scaled == GEMM_SCALE_UE8M0_32)
+        family = KIND_MXF8;
+    else if (ab == GEMM_E2M1 && block_scaled == GEMM_SCALE_UE8M0_32)
+        family = KIND_MXF4;
+    else if (ab == GEMM_E2M1 && block_scaled == GEMM_SCALE_UE4M3_16)
+        family = KIND_NVF4;
+    else
+        return GEMM_ERR_UNSUPPORTED;
+    // 4-bit operands: K-major only (the tensor core reads packed 4-bit data K-major)
+    if (ab == GEMM_E2M1 && (!a_row_major || b_row_major)) return GEMM_ERR_UNSUPPORTED;
 
     // 16-byte row strides (the copy engine's stride rule): A rows hold K (row-major) or M
     // (column-major) elements, B rows K (column-major) or N (row-major), C and D rows N
     const int64_t a_row = a_row_major ? K : M, b_row = b_row_major ? N : K;
-    if ((a_row * elem_bytes(ab)) % 16 != 0 || (b_row * elem_bytes(ab)) % 16 != 0 || (N * 4) % 16 != 0 ||
-        (N * elem_bytes(d)) % 16 != 0)
+    if ((a_row * elem_bits(ab)) % 128 != 0 || (b_row * elem_bits(ab)) % 128 != 0 || (N * 32) % 128 != 0 ||
+        (N * elem_bits(d)) % 128 != 0)
         return GEMM_ERR_ALIGNMENT;
 
     int dev = 0;
@@ -284,13 +320,14 @@ gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K, 
     p->c = c;
     p->d = d;
     p->block_scaled = block_scaled;
+    p->family = family;
     p->a_mn = !a_row_major;
     p->b_mn = b_row_major != 0;
     p->flags = flags;
     p->device = dev;
     p->sm_count = prop.multiProcessorCount;
     p->timeout_ns = 1000000000ull;
-    gemm_status st = block_scaled ? configure_mxf8(p) : configure_f16(p);
+    gemm_status st = family == KIND_F16 ? configure_f16(p) : configure_scaled(p);
     if (st != GEMM_OK) {
         cudaFree(p->ws_a);
         cudaFree(p->ws_b);
@@ -314,7 +351,7 @@ gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K, 
 gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C, void *D, const uint8_t *SFA,
                      const uint8_t *SFB, void *cuda_stream) {
     if (!p || !A || !B || !D) return GEMM_ERR_INVALID_ARG;
-    if (p->family == 1 && (!SFA || !SFB)) return GEMM_ERR_INVALID_ARG;
+    if (p->family != KIND_F16 && (!SFA || !SFB)) return GEMM_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (C && !aligned16(C))) return GEMM_ERR_ALIGNMENT;
     gemm_status st = encode_maps(p, A, B, C, D);
     if (st != GEMM_OK) return st;
@@ -343,15 +380,20 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
     kp.timeout_ns = p->timeout_ns;
     kp.fault = p->fault;
     LaunchShape shape{p->grid, p->cta_group, p->smem};
-    if (p->family == 1) {
-        kp.idesc = idesc_mxf8((uint32_t)(TILE_M * p->cta_group), (uint32_t)p->tile_n, 0, 0) |
-                   ((uint32_t)p->a_mn << 15) | ((uint32_t)p->b_mn << 16);
+    if (p->family != KIND_F16) {
+        const uint32_t tm = (uint32_t)(TILE_M * p->cta_group), tn = (uint32_t)p->tile_n;
+        kp.idesc = p->family == KIND_MXF8
+                       ? idesc_mxf8(tm, tn, 0, 0) | ((uint32_t)p->a_mn << 15) | ((uint32_t)p->b_mn << 16)
+                       : idesc_mxf4(tm, tn, p->family == KIND_NVF4);
         kp.sfa = p->ws_a;
         kp.sfb = p->ws_b;
-        if (mxf8_pack(SFA, SFB, p->ws_a, p->ws_b, kp.M, kp.N, kp.K, p->tiles_m * p->cta_group, p->tiles_n, p->tile_n,
-                      p->num_kb, p->sm_count, stream) != cudaSuccess)
+        const int sfk = (int)((p->K + scale_block(p->family) - 1) / scale_block(p->family));
+        const int n_wg = p->num_kb * (p->sfa_stage_bytes / 512);
+        if (sf_pack(SFA, SFB, p->ws_a, p->ws_b, kp.M, kp.N, sfk, p->tiles_m * p->cta_group, p->tiles_n, p->tile_n,
+                    n_wg, unit_scale(p->family), stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
-        if (mxf8_launch(p->cta_group, p->d == GEMM_BF16, shape, p->maps, kp, stream) != cudaSuccess)
+        if (scaled_family(p->family).launch(p->cta_group, p->d == GEMM_BF16, shape, p->maps, kp, stream) !=
+            cudaSuccess)
             return GEMM_ERR_CUDA;
     } else {
         kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * p->cta_group), (uint32_t)TILE_N) |
@@ -369,10 +411,10 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
 gemm_status gemm_run_host(gemm_plan_t p, const void *A, const void *B, const void *C, void *D, const uint8_t *SFA,
                           const uint8_t *SFB, void *cuda_stream) {
     if (!p || !A || !B || !D) return GEMM_ERR_INVALID_ARG;
-    const size_t a_bytes = (size_t)p->M * p->K * elem_bytes(p->ab);
-    const size_t b_bytes = (size_t)p->K * p->N * elem_bytes(p->ab);
+    const size_t a_bytes = bytes_of(p->ab, p->M * p->K);
+    const size_t b_bytes = bytes_of(p->ab, p->K * p->N);
     const size_t c_bytes = (size_t)p->M * p->N * 4;
-    const size_t d_bytes = (size_t)p->M * p->N * elem_bytes(p->d);
+    const size_t d_bytes = bytes_of(p->d, p->M * p->N);
     if (!p->hA) {
         if (cudaMalloc(&p->hA, a_bytes) != cudaSuccess || cudaMalloc(&p->hB, b_bytes) != cudaSuccess ||
             cudaMalloc(&p->hC, c_bytes) != cudaSuccess || cudaMalloc(&p->hD, d_bytes) != cudaSuccess)
@@ -383,9 +425,9 @@ gemm_status gemm_run_host(gemm_plan_t p, const void *A, const void *B, const voi
         cudaMemcpyAsync(p->hB, B, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     if (C && cudaMemcpyAsync(p->hC, C, c_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GEMM_ERR_CUDA;
-    if (p->family == 1) {
+    if (p->family != KIND_F16) {
         if (!SFA || !SFB) return GEMM_ERR_INVALID_ARG;
-        const size_t sfk = (size_t)((p->K + 31) / 32);
+        const size_t sfk = (size_t)((p->K + scale_block(p->family) - 1) / scale_block(p->family));
         if (!p->hSFA && (cudaMalloc(&p->hSFA, (size_t)p->M * sfk) != cudaSuccess ||
                          cudaMalloc(&p->hSFB, (size_t)p->N * sfk) != cudaSuccess))
             return GEMM_ERR_CUDA;
@@ -417,12 +459,12 @@ gemm_status gemm_plan_get_info(gemm_plan_t p, gemm_plan_info *info) {
     info->cta_group = p->cta_group;
     info->tile_m = TILE_M * p->cta_group;
     info->tile_n = p->tile_n;
-    info->tile_k = 128 / elem_bytes(p->ab);
+    info->tile_k = p->tile_k;
     info->stages = p->stages;
     info->grid = p->grid;
     info->tiles = p->tiles;
     info->smem_bytes = p->smem;
-    info->launches_per_run = (p->family == 1 ? 2 : 1) + (p->splits > 1 ? 1 : 0);
+    info->launches_per_run = (p->family != KIND_F16 ? 2 : 1) + (p->splits > 1 ? 1 : 0);
     info->splits = p->splits;
     info->sm_count = p->sm_count;
     return GEMM_OK;

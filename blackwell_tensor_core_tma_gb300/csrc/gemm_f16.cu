@@ -16,7 +16,7 @@ namespace gb300 {
 namespace {
 
 template <int CG, bool OUT_BF16>
-using F16Cfg = TileCfg<CG, OUT_BF16, false, TILE_N, CG == 1 ? GB300_F16_CG1_STAGES : GB300_F16_CG2_STAGES>;
+using F16Cfg = TileCfg<CG, OUT_BF16, KIND_F16, TILE_N, CG == 1 ? GB300_F16_CG1_STAGES : GB300_F16_CG2_STAGES>;
 
 // D = C (or 0): the starting value split-K slices add their partial products to
 __global__ void init_d_kernel(float4 *__restrict__ D, const float4 *__restrict__ C, size_t n4) {

@@ -51,19 +51,41 @@ cudaError_t f16_launch(const F16Config &cfg, const LaunchShape &shape, const CUt
 // split-K preparation (gemm_f16.cu): D = C, or D = 0 without C (fp32, n elements, n % 4 == 0)
 cudaError_t init_d_launch(float *D, const float *C, size_t n, int sm_count, cudaStream_t stream);
 
-// block-scaled e4m3 kernel family (gemm_mxf8.cu)
-int mxf8_tile_n(int cta_group);
-int mxf8_stages(int cta_group);
-int mxf8_smem_bytes(int cta_group);
-size_t mxf8_workspace_a(int row_blocks, int num_kb);
-size_t mxf8_workspace_b(int tiles_n, int num_kb);
-int mxf8_sfb_block_bytes();
-cudaError_t mxf8_prepare(int cta_group, int out_bf16);
-cudaError_t mxf8_max_active_clusters(int cta_group, int out_bf16, int *clusters);
-cudaError_t mxf8_pack(const uint8_t *sfa, const uint8_t *sfb, uint8_t *out_a, uint8_t *out_b, int M, int N, int K,
-                      int row_blocks, int tiles_n, int tile_n, int num_kb, int sm_count, cudaStream_t stream);
-cudaError_t mxf8_launch(int cta_group, int out_bf16, const LaunchShape &shape, const CUtensorMap *maps,
-                        const KParams &p, cudaStream_t stream);
+// Operand kinds of the tensor-core kernel (tcgen05.mma kinds):
+//   KIND_F16   fp16 / bf16, kind::f16
+//   KIND_MXF8  e4m3 with a UE8M0 scale per 32 K, kind::mxf8f6f4 scale_vec::1X
+//   KIND_MXF4  e2m1 with a UE8M0 scale per 32 K, kind::mxf4 scale_vec::2X
+//   KIND_NVF4  e2m1 with a UE4M3 scale per 16 K, kind::mxf4nvf4 scale_vec::4X
+enum GemmKind { KIND_F16 = 0, KIND_MXF8 = 1, KIND_MXF4 = 2, KIND_NVF4 = 3 };
+
+// Static shape of a block-scaled kernel instance (per CTA group)
+struct ScaledShape {
+    int tile_n;      // columns of D per tile
+    int stages;      // ring depth
+    int smem;        // dynamic shared memory per CTA
+    int bk;          // K elements per stage
+    int sfa_bytes;   // packed SFA bytes per stage (one 512-byte block per 4 scales of 128 rows)
+    int sfb_bytes;   // packed SFB bytes per stage (every column of the tile)
+};
+
+// A block-scaled kernel family: its four instances (CTA group 1 / 2 x D fp32 / bf16)
+struct ScaledFamily {
+    ScaledShape (*shape)(int cta_group);
+    cudaError_t (*prepare)(int cta_group, int out_bf16);      // set the kernel's shared-memory limit
+    cudaError_t (*max_active_clusters)(int cta_group, int out_bf16, int *clusters);
+    cudaError_t (*launch)(int cta_group, int out_bf16, const LaunchShape &shape, const CUtensorMap *maps,
+                          const KParams &p, cudaStream_t stream);
+};
+const ScaledFamily &family_mxf8();   // gemm_mxf8.cu
+const ScaledFamily &family_mxf4();   // gemm_mxf4.cu
+const ScaledFamily &family_nvf4();   // gemm_nvf4.cu
+
+// Pack row-major scale factors SFA (M x sfk) and SFB (N x sfk) into the kernels'
+// 512-byte TMEM-order blocks (gemm_sfpack.cu).  n_wg: groups of four scale columns
+// per row of the packed layout (stages x scale words per stage); scales outside the
+// matrices read as `pad` (the format's 1.0).
+cudaError_t sf_pack(const uint8_t *sfa, const uint8_t *sfb, uint8_t *out_a, uint8_t *out_b, int M, int N, int sfk,
+                    int row_blocks, int tiles_n, int tile_n, int n_wg, uint8_t pad, cudaStream_t stream);
 
 constexpr int TILE_M = 128;   // rows of D per CTA
 constexpr int TILE_N = 256;   // columns of D per CTA (and per CTA pair)

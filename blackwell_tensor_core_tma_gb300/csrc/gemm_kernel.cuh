@@ -1,6 +1,6 @@
 // Persistent, warp-specialised tensor-core GEMM for sm_103a (shared by the
-// fp16/bf16 and the block-scaled e4m3 kernels):
-//   D = A·B + C, A (M x K) and B (K x N) K-major, fp32 accumulation in tensor
+// fp16/bf16 kernels and the block-scaled e4m3 and e2m1 kernels):
+//   D = A·B + C, A (M x K) and B (K x N), fp32 accumulation in tensor
 //   memory, C fp32, D fp32 or bf16.
 //
 // One CTA (cta_group::1) or one CTA pair (cta_group::2) owns a 128 x BN or
@@ -43,7 +43,8 @@ namespace gb300 {
 // Compile-time shape of one kernel instance.
 //   CG      1 = single CTA per tile, 2 = CTA pair (cta_group::2)
 //   OUT_BF16  D is bf16 (else fp32)
-//   SCALED  block-scaled e4m3 operands (kind::mxf8f6f4, scale_vec::1X)
+//   KIND    operand kind (GemmKind): fp16/bf16, or block-scaled e4m3 (1X),
+//           e2m1 with UE8M0 per 32 (2X) or e2m1 with UE4M3 per 16 (4X)
 //   BN      tile columns (MMA N)
 //   ACC_BUFS  TMEM accumulators: 2 = the epilogue drains one while the MMA fills
 //             the other; 1 = the epilogue copies the accumulator to registers
@@ -51,11 +52,12 @@ namespace gb300 {
 //             for scale slots at N = 256)
 //   EPI_WARPS epilogue warps: 4 (one per TMEM lane window) or 8 (two per window,
 //             each taking half of the tile's columns)
-template <int CG_, bool OUT_BF16_, bool SCALED_, int BN_, int STAGES_, int ACC_BUFS_ = 2, int EPI_WARPS_ = 4>
+template <int CG_, bool OUT_BF16_, int KIND_, int BN_, int STAGES_, int ACC_BUFS_ = 2, int EPI_WARPS_ = 4>
 struct TileCfg {
     static constexpr int CG = CG_;
     static constexpr bool OUT_BF16 = OUT_BF16_;
-    static constexpr bool SCALED = SCALED_;
+    static constexpr int KIND = KIND_;
+    static constexpr bool SCALED = KIND != KIND_F16;
     static constexpr int BN = BN_;
     static constexpr int STAGES = STAGES_;
     static constexpr int ACC_BUFS = ACC_BUFS_;
@@ -66,19 +68,30 @@ struct TileCfg {
     static_assert(ACC_BUFS == 1 || ACC_BUFS == 2, "accumulator buffers");
     static_assert(EPI_WARPS == 4 || EPI_WARPS == 8, "epilogue warps");
     static_assert(WCOLS % EPI_COLS == 0, "epilogue columns per warp");
-    static constexpr int ELEM = SCALED ? 1 : 2;                 // operand bytes
-    static constexpr int BK = 128 / ELEM;                       // K elements per stage: one 128-byte row
-    static constexpr int MMA_K = 32 / ELEM;                     // K per instruction: 32 bytes
-    // MN-major operands: boxes one 128-byte swizzle atom wide along M (or N) and BK rows of K
-    static constexpr int ATOM_MN = 128 / ELEM;                  // M/N elements of one atom
+    static constexpr int ELEM_BITS = KIND == KIND_F16 ? 16 : (KIND == KIND_MXF8 ? 8 : 4);
+    static constexpr int BK = 1024 / ELEM_BITS;                 // K elements per stage: one 128-byte row
+    static constexpr int MMA_K = 256 / ELEM_BITS;               // K per instruction: 32 bytes
+    // K extent of an operand box in tensor-map elements (4-bit operands are mapped as bytes)
+    static constexpr int TMA_BK = ELEM_BITS == 4 ? 128 : BK;
+    // MN-major operands (8- and 16-bit kinds): boxes one 128-byte swizzle atom wide along
+    // M (or N) and BK rows of K
+    static constexpr bool MN_OK = ELEM_BITS >= 8;
+    static constexpr int ATOM_MN = 1024 / ELEM_BITS;            // M/N elements of one atom
     static constexpr int ATOM_BYTES = BK * 128;                 // one atom column of a stage
     static constexpr int A_BYTES = TILE_M * 128;                // 16 KiB
     static constexpr int B_ROWS = BN / CG;                      // B rows held by one CTA
     static constexpr int B_BYTES = B_ROWS * 128;
+    // Block scales: SF_BLOCK K elements share a scale; a row's scales of one stage fill
+    // SF_WORDS 32-bit words (four scales each); an MMA step reads SF_PER_MMA of them.
+    static constexpr int SF_BLOCK = KIND == KIND_NVF4 ? 16 : 32;
+    static constexpr int SF_WORDS = SCALED ? BK / SF_BLOCK / 4 : 0;
+    static constexpr int SF_PER_MMA = MMA_K / SF_BLOCK;
+    static constexpr int HALVES = (BN + 127) / 128;             // 128-column groups of the tile
     // scales of one stage in one CTA: SFA of its 128 rows, SFB of all BN columns of the
-    // tile (each CTA of a pair computes every column of its rows); 512 bytes per 128 rows
-    static constexpr int SFA_BYTES = SCALED ? 512 : 0;          // 128 rows x 4 K-blocks of 32
-    static constexpr int SFB_BYTES = SCALED ? 512 * ((BN + 127) / 128) : 0;
+    // tile (each CTA of a pair computes every column of its rows); 512 bytes per word of
+    // 128 rows, SFB words ordered (word, 128-column group)
+    static constexpr int SFA_BYTES = 512 * SF_WORDS;
+    static constexpr int SFB_BYTES = 512 * SF_WORDS * HALVES;
     static constexpr int TX_BYTES = CG * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES);
     static constexpr int EPI_BUF = 32 * EPI_COLS * 4;           // one 32 x 32 fp32 box
     // Every region a swizzled TMA copy or a swizzled MMA descriptor addresses
@@ -96,14 +109,16 @@ struct TileCfg {
     static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 * EPI_WARPS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base slot, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
-    // TMEM columns: accumulators [0, 2*BN), then one scale slot per stage: SFA in
-    // 4 columns, SFB in 4 columns per 128 rows of B.  A slot is reused only when
-    // its stage is refilled, i.e. after the MMAs that read it have completed.
-    static constexpr int SF_SLOT = SCALED ? 4 + 4 * ((BN + 127) / 128) : 0;
+    // TMEM columns: accumulators [0, ACC_BUFS*BN), then one scale slot per stage: SFA
+    // in 4 columns per word, SFB in 4 columns per (word, 128 columns of the tile).  A
+    // slot is reused only when its stage is refilled, i.e. after the MMAs that read it
+    // have completed.
+    static constexpr int SF_SLOT = 4 * SF_WORDS * (1 + HALVES);
     static constexpr int SF_COL0 = ACC_BUFS * BN;
     static_assert(ACC_BUFS * BN + STAGES * SF_SLOT <= 512, "TMEM budget");
     static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
     static_assert(BN % EPI_COLS == 0 && BN % 16 == 0 && BN <= 256, "tile N");
+    static_assert(!SCALED || (SF_WORDS >= 1 && SF_PER_MMA >= 1 && 4 % SF_PER_MMA == 0), "scale vector");
 };
 
 __device__ __forceinline__ void tile_coords(int t, int tiles_m, int group_m, int &tm, int &tn, int tiles_n) {
@@ -253,8 +268,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // an operand tile: K-major, one box of BK x rows; MN-major, rows / ATOM_MN
                     // boxes of ATOM_MN x BK, one per 128-byte atom column
                     auto load_operand = [&](uint32_t dst, const CUtensorMap *m, int row0, int rows, bool mn) {
-                        if (!mn) {
-                            load(dst, m, kb * Cfg::BK, row0);
+                        if (!Cfg::MN_OK || !mn) {
+                            load(dst, m, kb * Cfg::TMA_BK, row0);
                         } else {
                             for (int i = 0; i < rows / Cfg::ATOM_MN; ++i)
                                 load(dst + i * Cfg::ATOM_BYTES, m, row0 + i * Cfg::ATOM_MN, kb * Cfg::BK);
@@ -296,20 +311,28 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint64_t ad = smem_desc(smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES), a_lbo, 1024, SWZ_128B);
                     const uint64_t bd = smem_desc(smem_addr(smem + Cfg::OFF_B + s * Cfg::B_BYTES), b_lbo, 1024, SWZ_128B);
                     if constexpr (Cfg::SCALED) {
-                        // stage s's scales: SFA in 4 columns, SFB in 4 per 128 rows of B,
-                        // each a 32-lane x 16-byte SMEM block replicated to the 4 lane windows
+                        // stage s's scales, each 512-byte SMEM block (32 lanes x 16 bytes: one
+                        // word of 128 rows) replicated to the 4 lane windows: SFA word w in
+                        // columns 4w..4w+3, SFB (word w, column group h) in 4(w*HALVES + h)..
                         const uint32_t sfa_t = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_SLOT;
-                        const uint32_t sfb_t = sfa_t + 4;
+                        const uint32_t sfb_t = sfa_t + 4 * Cfg::SF_WORDS;
                         const uint32_t sf_src = smem_addr(smem + Cfg::OFF_SF + s * (Cfg::SFA_BYTES + Cfg::SFB_BYTES));
-                        tmem_cp_32x128b_warpx4<CG>(sfa_t, smem_desc(sf_src, 512, 128, SWZ_NONE));
 #pragma unroll
-                        for (int h = 0; h < Cfg::SFB_BYTES / 512; ++h)
-                            tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * h,
-                                                       smem_desc(sf_src + Cfg::SFA_BYTES + 512 * h, 512, 128, SWZ_NONE));
+                        for (int i = 0; i < Cfg::SF_WORDS; ++i)
+                            tmem_cp_32x128b_warpx4<CG>(sfa_t + 4 * i, smem_desc(sf_src + 512 * i, 512, 128, SWZ_NONE));
 #pragma unroll
-                        for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k)   // K block k of 32 uses scale byte k
-                            mma_mxf8<CG>(d_tmem, ad + a_step * k, bd + b_step * k, p.idesc | (k << 4) | (k << 29), sfa_t, sfb_t,
-                                         (kb != kb0) | (k != 0));
+                        for (int i = 0; i < Cfg::SF_WORDS * Cfg::HALVES; ++i)
+                            tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * i,
+                                                       smem_desc(sf_src + Cfg::SFA_BYTES + 512 * i, 512, 128, SWZ_NONE));
+                        // MMA step k reads scales k*SF_PER_MMA.. of the stage: word w, from byte id
+                        // (1X: byte k; 2X: half-word 0 or 2; 4X: the whole word, id 0)
+#pragma unroll
+                        for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k) {
+                            const uint32_t w = (uint32_t)(k * Cfg::SF_PER_MMA) / 4u, id = (uint32_t)(k * Cfg::SF_PER_MMA) % 4u;
+                            mma_scaled<Cfg::KIND, CG>(d_tmem, ad + a_step * k, bd + b_step * k,
+                                                      p.idesc | (id << 4) | (id << 29), sfa_t + 4 * w,
+                                                      sfb_t + 4 * Cfg::HALVES * w, (kb != kb0) | (k != 0));
+                        }
                     } else {
 #pragma unroll
                         for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k)   // 32 bytes of K = 2 descriptor units
@@ -510,5 +533,36 @@ cudaError_t max_active_clusters_tc(int *clusters) {
     lc.numAttrs = 1;
     return cudaOccupancyMaxActiveClusters(clusters, reinterpret_cast<const void *>(&gemm_tc_kernel<Cfg>), &lc);
 }
+
+// The four instances (CTA group 1 / 2, D fp32 / bf16) of a block-scaled family
+template <class C1F, class C1B, class C2F, class C2B>
+struct ScaledInstances {
+    static ScaledShape shape(int cta_group) {
+        return cta_group == 1 ? ScaledShape{C1F::BN, C1F::STAGES, C1F::SMEM_BYTES, C1F::BK, C1F::SFA_BYTES, C1F::SFB_BYTES}
+                              : ScaledShape{C2F::BN, C2F::STAGES, C2F::SMEM_BYTES, C2F::BK, C2F::SFA_BYTES, C2F::SFB_BYTES};
+    }
+    static cudaError_t prepare(int cta_group, int out_bf16) {
+        if (cta_group == 1) return out_bf16 ? prepare_tc<C1B>() : prepare_tc<C1F>();
+        return out_bf16 ? prepare_tc<C2B>() : prepare_tc<C2F>();
+    }
+    static cudaError_t max_active_clusters(int cta_group, int out_bf16, int *clusters) {
+        if (cta_group == 1)
+            return out_bf16 ? max_active_clusters_tc<C1B>(clusters) : max_active_clusters_tc<C1F>(clusters);
+        return out_bf16 ? max_active_clusters_tc<C2B>(clusters) : max_active_clusters_tc<C2F>(clusters);
+    }
+    static cudaError_t launch(int cta_group, int out_bf16, const LaunchShape &shape, const CUtensorMap *maps,
+                              const KParams &p, cudaStream_t stream) {
+        if (cta_group == 1)
+            return out_bf16 ? launch_tc<C1B>(shape, maps, p, stream) : launch_tc<C1F>(shape, maps, p, stream);
+        return out_bf16 ? launch_tc<C2B>(shape, maps, p, stream) : launch_tc<C2F>(shape, maps, p, stream);
+    }
+    static const ScaledFamily &family() {
+        static const ScaledFamily f{&shape, &prepare, &max_active_clusters, &launch};
+        return f;
+    }
+    static_assert(C1F::CG == 1 && C1B::CG == 1 && C2F::CG == 2 && C2B::CG == 2, "CTA groups");
+    static_assert(!C1F::OUT_BF16 && C1B::OUT_BF16 && !C2F::OUT_BF16 && C2B::OUT_BF16, "D types");
+    static_assert(C1F::SF_WORDS == C2F::SF_WORDS && C1F::BK == C2F::BK, "one packed scale layout per family");
+};
 
 }  // namespace gb300

@@ -1,0 +1,28 @@
+// Block-scaled 4-bit instances of the tensor-core GEMM (gemm_kernel.cuh):
+// e2m1 operands with one UE8M0 scale per 32 K elements: an MMA step of 64 K
+// reads two scale bytes, half-word 0 or 2 of a four-scale TMEM word (scale_vec::2X,
+// kind::mxf4).
+//
+// Operands are OCP E2M1 values packed two per byte along K (element 2t in the
+// low nibble of byte t), K-major only; a 128-byte shared-memory row holds 256 K
+// elements, so a stage spans 256 K and four MMA steps of 64.  The stage's scales
+// arrive packed by sf_pack (gemm_sfpack.cu) and take 8 SFA + 16 SFB columns of the pair's slot (8 + 8 for single CTAs).
+#include "gemm_kernel.cuh"
+
+namespace gb300 {
+namespace {
+
+// single CTAs: 128 x 128 tiles, two accumulators, five stages, 4 epilogue warps.
+// CTA pairs: 256 x 256 tiles, one 256-column accumulator drained to registers by
+// 8 epilogue warps, four stages (the shared memory the scales leave).
+template <bool OUT_BF16>
+using Cfg1 = TileCfg<1, OUT_BF16, KIND_MXF4, 128, 5, 2, 4>;
+template <bool OUT_BF16>
+using Cfg2 = TileCfg<2, OUT_BF16, KIND_MXF4, 256, 4, 1, 8>;
+using Family = ScaledInstances<Cfg1<false>, Cfg1<true>, Cfg2<false>, Cfg2<true>>;
+
+}  // namespace
+
+const ScaledFamily &family_mxf4() { return Family::family(); }
+
+}  // namespace gb300

@@ -229,26 +229,32 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
             : "memory");
 }
 
-// D[tmem] (+)= (A * SFA) * (B * SFB), e4m3 operands, UE8M0 scales read from TMEM,
-// one scale per 32 K elements (scale_vec::1X)
-template <int CG>
-__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-    if constexpr (CG == 1)
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-                d_tmem),
-            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-            : "memory");
-    else
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
-                d_tmem),
-            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-            : "memory");
+// D[tmem] (+)= (A * SFA) * (B * SFB) with the scales read from TMEM:
+//   KIND 1  e4m3 operands, UE8M0 scale per 32 K (kind::mxf8f6f4, scale_vec::1X)
+//   KIND 2  e2m1 operands, UE8M0 scale per 32 K (kind::mxf4, scale_vec::2X)
+//   KIND 3  e2m1 operands, UE4M3 scale per 16 K (kind::mxf4nvf4, scale_vec::4X)
+#define GB300_MMA_SCALED(CGS, KINDS)                                                                       \
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"                                         \
+                 "tcgen05.mma.cta_group::" CGS ".kind::" KINDS " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"( \
+                     d_tmem),                                                                               \
+                 "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)           \
+                 : "memory")
+template <int KIND, int CG>
+__device__ __forceinline__ void mma_scaled(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    static_assert(KIND >= 1 && KIND <= 3 && (CG == 1 || CG == 2), "block-scaled kind");
+    if constexpr (KIND == 1) {
+        if constexpr (CG == 1) GB300_MMA_SCALED("1", "mxf8f6f4.block_scale.scale_vec::1X");
+        else GB300_MMA_SCALED("2", "mxf8f6f4.block_scale.scale_vec::1X");
+    } else if constexpr (KIND == 2) {
+        if constexpr (CG == 1) GB300_MMA_SCALED("1", "mxf4.block_scale.scale_vec::2X");
+        else GB300_MMA_SCALED("2", "mxf4.block_scale.scale_vec::2X");
+    } else {
+        if constexpr (CG == 1) GB300_MMA_SCALED("1", "mxf4nvf4.block_scale.scale_vec::4X");
+        else GB300_MMA_SCALED("2", "mxf4nvf4.block_scale.scale_vec::4X");
+    }
 }
+#undef GB300_MMA_SCALED
 
 // SMEM -> TMEM copy of 32 lanes x 128 bits, replicated into the four 32-lane
 // windows (.warpx4); source described by a shared-memory matrix descriptor
@@ -341,6 +347,13 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_bf16, uint32_t M, u
 // A scale-factor byte id in bits 29-30.
 __host__ __device__ constexpr uint32_t idesc_mxf8(uint32_t M, uint32_t N, uint32_t sfa_id, uint32_t sfb_id) {
     return (sfb_id << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sfa_id << 29);
+}
+
+// Instruction descriptor, kind::mxf4 / kind::mxf4nvf4: as for kind::mxf8f6f4 with
+// A/B format E2M1 (1 in bits 7-9 / 10-12), both K-major, and the scale format in
+// bit 23: UE8M0 = 1, UE4M3 = 0.
+__host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32_t scale_ue4m3) {
+    return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((scale_ue4m3 ? 0u : 1u) << 23) | ((M >> 4) << 24);
 }
 
 }  // namespace gb300

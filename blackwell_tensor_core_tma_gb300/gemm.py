@@ -14,10 +14,11 @@ import os
 from . import build as _build
 
 GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ALIGNMENT, GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT = range(6)
-GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_F32 = range(4)
+GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_F32, GEMM_E2M1 = range(5)
+GEMM_SCALE_NONE, GEMM_SCALE_UE8M0_32, GEMM_SCALE_UE4M3_16 = range(3)
 GEMM_FLAG_SYNC, GEMM_FLAG_FORCE_1CTA, GEMM_FLAG_FORCE_2CTA, GEMM_FLAG_DETERMINISTIC = 0x1, 0x2, 0x4, 0x8
 
-DTYPE = {"f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM_E4M3, "f32": GEMM_F32}
+DTYPE = {"f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM_E4M3, "f32": GEMM_F32, "e2m1": GEMM_E2M1}
 
 # every symbol include/gb300gemm.h and include/gb300gemm_testing.h declare
 EXPORTS = ["gemm_plan_create", "gemm_run", "gemm_run_host", "gemm_plan_last_status", "gemm_plan_get_info",
@@ -165,10 +166,11 @@ def gemm_run_noalloc(M: int, N: int, K: int, ab, d, A, B, C, D, stream=None, wai
 class Plan:
     """Owning wrapper of a gemm_plan_t (destroyed on close / context exit)."""
 
-    def __init__(self, M, N, K, ab="bf16", d="f32", block_scaled=False, flags=0, c="f32", a_row_major=True,
-                 b_row_major=False):
+    def __init__(self, M, N, K, ab="bf16", d="f32", block_scaled=GEMM_SCALE_NONE, flags=0, c="f32",
+                 a_row_major=True, b_row_major=False):
+        """``block_scaled``: GEMM_SCALE_NONE / GEMM_SCALE_UE8M0_32 (True) / GEMM_SCALE_UE4M3_16."""
         self.M, self.N, self.K, self.ab, self.d = M, N, K, ab, d
-        self.block_scaled = bool(block_scaled)
+        self.block_scaled = int(block_scaled)
         self.handle = None
         self.handle = gemm_plan_create(M, N, K, ab, c, d, int(a_row_major), int(b_row_major), int(block_scaled), flags)
 

@@ -8,14 +8,19 @@
  *
  *     D[i][j] = C[i][j] + sum_k a[i][k] * b[k][j]          (0 <= i < M, 0 <= j < N)
  *
- * Operands a and b are fp16 or bf16 values, or — block scaled — OCP e4m3
- * values each multiplied by a UE8M0 power-of-two scale shared by 32
- * consecutive K elements ("Tensor Core 数据布局的演进", section
- * "Block-Scaled MMA 的 Scale Factors": SFA[m][sfk] scales row m of A in K
- * block sfk, SFB[n][sfk] scales column n of B):
+ * Operands a and b are fp16 or bf16 values, or — block scaled — low-precision
+ * values each multiplied by a scale shared by `blk` consecutive K elements
+ * ("Tensor Core 数据布局的演进", section "Block-Scaled MMA 的 Scale Factors":
+ * SFA[m][sfk] scales row m of A in K block sfk, SFB[n][sfk] scales column n
+ * of B; section "scale_vec 的 Word 内复制": one, two or four scales per row
+ * and MMA step):
  *
- *     a[i][k] = e4m3(A[i][k]) * 2^(SFA[i][k/32] - 127)
- *     b[k][j] = e4m3(B[k][j]) * 2^(SFB[j][k/32] - 127)
+ *     a[i][k] = A[i][k] * sf(SFA[i][k/blk]),   b[k][j] = B[k][j] * sf(SFB[j][k/blk])
+ *
+ *   block_scaled = GEMM_SCALE_UE8M0_32: blk = 32, sf(c) = 2^(c - 127) (UE8M0),
+ *                  A and B OCP e4m3 (scale_vec::1X) or OCP e2m1 (2X);
+ *   block_scaled = GEMM_SCALE_UE4M3_16: blk = 16, sf(c) = the unsigned e4m3
+ *                  value of c (UE4M3, bit 7 zero), A and B OCP e2m1 (4X).
  *
  * Memory layout (all buffers packed; no leading-dimension arguments):
  *   A    M x K, row-major (element (i,k) at A[i*K + k]) or, with
@@ -27,8 +32,10 @@
  *        descriptor's transpose bits).
  *   C    M x N fp32 row-major, or NULL for C = 0.
  *   D    M x N row-major, fp32 or bf16 (round to nearest even).
- *   SFA  M x ceil(K/32) UE8M0 codes, row-major (block-scaled plans only).
- *   SFB  N x ceil(K/32) UE8M0 codes, row-major (block-scaled plans only).
+ *   SFA  M x ceil(K/blk) scale codes, row-major (block-scaled plans only).
+ *   SFB  N x ceil(K/blk) scale codes, row-major (block-scaled plans only).
+ *   e2m1 operands are packed two per byte along K, element 2t in bits 0..3
+ *   of byte t; they must be K-major (A row-major, B column-major).
  *
  * Every global row stride and every base pointer must be a multiple of
  * 16 bytes: the tensor-memory-accelerator copy engine needs one dimension of
@@ -36,8 +43,8 @@
  * Tensor Memory Accelerator（TMA）", section "使用 TMA 处理 remainder tiles
  * 以及 stride 要求": pad the tensor before calling otherwise).  For 16-bit
  * operands the contiguous extent (K, or M / N for column- / row-major A / B)
- * must be a multiple of 8, for e4m3 of 16; for C and fp32 D N % 4 == 0, for
- * bf16 D N % 8 == 0.  M, N and K need not be multiples of
+ * must be a multiple of 8, for e4m3 of 16, for e2m1 (K) of 32; for C and
+ * fp32 D N % 4 == 0, for bf16 D N % 8 == 0.  M, N and K need not be multiples of
  * any tile size: the copy engine predicates the remainder tiles.
  *
  * Ownership: the caller owns every device buffer.  A plan owns host state and
@@ -68,8 +75,14 @@ typedef enum {
     GEMM_F16 = 0,
     GEMM_BF16 = 1,
     GEMM_E4M3 = 2,
-    GEMM_F32 = 3
+    GEMM_F32 = 3,
+    GEMM_E2M1 = 4               /* OCP FP4 E2M1, two elements per byte (block-scaled only) */
 } gemm_dtype;
+
+/* gemm_plan_create block_scaled modes */
+#define GEMM_SCALE_NONE       0  /* fp16 / bf16 operands, no scales */
+#define GEMM_SCALE_UE8M0_32   1  /* UE8M0 scale per 32 K elements: e4m3 or e2m1 operands */
+#define GEMM_SCALE_UE4M3_16   2  /* UE4M3 scale per 16 K elements: e2m1 operands */
 
 /* gemm_plan_create flags */
 #define GEMM_FLAG_SYNC        0x1u  /* gemm_run synchronises its stream and returns the kernel status */
@@ -94,12 +107,16 @@ typedef struct {
 } gemm_plan_info;
 
 /*
- * Validate a problem and choose its kernel.  M, N, K > 0.  ab is GEMM_F16 or
- * GEMM_BF16 (block_scaled = 0) or GEMM_E4M3 (block_scaled = 1).  c must be
- * GEMM_F32; d is GEMM_F32 or GEMM_BF16.  a_row_major and b_row_major choose
- * the storage order of A and B (all four combinations; a block-scaled plan
- * with row-major B needs CTA pairs, so GEMM_FLAG_FORCE_1CTA then returns
- * GEMM_ERR_UNSUPPORTED).  Row-stride alignment (see above) is checked here and
+ * Validate a problem and choose its kernel.  M, N, K > 0.  ab and block_scaled
+ * go together as GEMM_F16 or GEMM_BF16 with GEMM_SCALE_NONE, GEMM_E4M3 with
+ * GEMM_SCALE_UE8M0_32, or GEMM_E2M1 with GEMM_SCALE_UE8M0_32 or
+ * GEMM_SCALE_UE4M3_16 (other pairs: GEMM_ERR_UNSUPPORTED; a block_scaled
+ * value outside 0..2: GEMM_ERR_INVALID_ARG).  c must be GEMM_F32; d is
+ * GEMM_F32 or GEMM_BF16.  a_row_major and b_row_major choose the storage
+ * order of A and B (all four combinations for 16- and 8-bit operands; a
+ * block-scaled e4m3 plan with row-major B needs CTA pairs, so
+ * GEMM_FLAG_FORCE_1CTA then returns GEMM_ERR_UNSUPPORTED; e2m1 operands
+ * must be K-major, a_row_major = 1 and b_row_major = 0).  Row-stride alignment (see above) is checked here and
  * returns GEMM_ERR_ALIGNMENT.  The plan is bound to the CUDA device current
  * at creation, which must be compute capability 10.3.  *out is set only on
  * GEMM_OK.

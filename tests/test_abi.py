@@ -31,6 +31,14 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), name
 
 
+def test_enum_values_match_header():
+    text = open(os.path.join(ROOT, "include", "gb300gemm.h")).read()
+    for name in ("GEMM_F16", "GEMM_BF16", "GEMM_E4M3", "GEMM_F32", "GEMM_E2M1"):
+        assert int(re.search(rf"\b{name} = (\d+)", text).group(1)) == getattr(gemm, name)
+    for name in ("GEMM_SCALE_NONE", "GEMM_SCALE_UE8M0_32", "GEMM_SCALE_UE4M3_16"):
+        assert int(re.search(rf"#define {name}\s+(\d+)", text).group(1)) == getattr(gemm, name)
+
+
 def test_status_strings(lib):
     for s in range(6):
         assert gemm.gemm_status_string(s)
@@ -54,6 +62,8 @@ def test_plan_rejects_unsupported_combinations(lib):
     cases = [
         dict(ab="f32"), dict(c="bf16"), dict(d="f16"),
         dict(ab="e4m3", block_scaled=0), dict(ab="bf16", block_scaled=1),
+        dict(ab="e2m1", block_scaled=0), dict(ab="e4m3", block_scaled=2), dict(ab="bf16", block_scaled=2),
+        dict(ab="e2m1", block_scaled=1, a_row_major=0), dict(ab="e2m1", block_scaled=2, b_row_major=1),
     ]
     for kw in cases:
         with pytest.raises(gemm.GemmError) as e:
@@ -62,6 +72,18 @@ def test_plan_rejects_unsupported_combinations(lib):
     with pytest.raises(gemm.GemmError) as e:
         gemm.gemm_plan_create(256, 256, 256, flags=gemm.GEMM_FLAG_FORCE_1CTA | gemm.GEMM_FLAG_FORCE_2CTA)
     assert e.value.status == gemm.GEMM_ERR_INVALID_ARG
+    for mode in (-1, 3):
+        with pytest.raises(gemm.GemmError) as e:
+            gemm.gemm_plan_create(256, 256, 256, ab="e2m1", block_scaled=mode)
+        assert e.value.status == gemm.GEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("K", [16, 48, 272])
+def test_e2m1_rows_must_hold_16_bytes(lib, K):
+    # packed 4-bit K-major rows of K/2 bytes: K must be a multiple of 32
+    with pytest.raises(gemm.GemmError) as e:
+        gemm.gemm_plan_create(256, 256, K, ab="e2m1", block_scaled=2)
+    assert e.value.status == gemm.GEMM_ERR_ALIGNMENT
 
 
 def test_null_plan_calls(lib):
