@@ -39,10 +39,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture
 # summarised in profiles/; valid only for the kernel sources the capture ran on
 MEASURED_TRAFFIC = {
-    "bf16_8192x8192x8192_bf16out": {"bytes": 1398978816 + 123798272, "src": "ef60784a3f85e76d",
+    "bf16_8192x8192x8192_bf16out": {"bytes": 1399832064 + 126089216, "src": "cc211e9fed2b0208",
                                     "ncu": "profiles/gemm_tc_kernel_bf16_8192x8192x8192_bf16out_launches.md"},
-    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 706623232 + 237450752, "src": "ef763b86e4aea305",
+    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 715286528 + 237443328, "src": "fdf06f21ed91b359",
                                           "ncu": "profiles/gemm_tc_kernel_mxf8_8192x8192x8192_launches.md"},
+    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 501818368 + 218974464, "src": "d7edda8407890a47",
+                                          "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
+    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 516495360 + 220410112, "src": "42e223774c6a4671",
+                                          "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
 }
 
 
