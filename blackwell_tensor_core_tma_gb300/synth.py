@@ -246,6 +246,57 @@ WORKLOADS = {
 HEADLINE = "bf16_8192x8192x8192_bf16out"
 
 
+@dataclasses.dataclass(frozen=True)
+class ChainWorkload:
+    """Two chained products D = C + round(A·B)·E and the recipe of their inputs.
+
+    A is M x K row-major, B is K x N1 column-major (N1 rows of K), E is N1 x N2
+    column-major (N2 rows of N1), C is M x N2 fp32, D is M x N2; ``ab`` ("bf16"
+    or "f16") is the type of A, B, E and of the rounded intermediate.
+    """
+    name: str
+    M: int
+    N1: int
+    N2: int
+    K: int
+    ab: str
+    dist: str
+    sigma: float
+    c: str
+    d: str
+    seed: int
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N1 * (self.K + self.N2)
+
+
+T_E = 5   # stream id of E
+
+CHAIN_WORKLOADS = {
+    w.name: w for w in [
+        ChainWorkload("chain_bf16_32768x4096_256x256_bf16out", 32768, 256, 256, 4096, "bf16", "uniform", 1.0,
+                      "normal", "bf16", 7),
+    ]
+}
+
+
+def scaled_chain(w: ChainWorkload, M: int, N1: int, N2: int, K: int, **kw) -> ChainWorkload:
+    return dataclasses.replace(w, name=f"{w.name}@{M}x{K}_{N1}x{N2}", M=M, N1=N1, N2=N2, K=K, **kw)
+
+
+def make_chain_inputs(w: ChainWorkload) -> dict:
+    """Bit patterns of A (M, K), B (N1, K), E (N2, N1) and fp32 C (M, N2)."""
+    A = _operand(w, T_A, w.M * w.K).reshape(w.M, w.K)
+    B = _operand(w, T_B, w.K * w.N1).reshape(w.N1, w.K)
+    E = _operand(w, T_E, w.N1 * w.N2).reshape(w.N2, w.N1)
+    if w.c == "zero":
+        C = np.zeros((w.M, w.N2), dtype=np.float32)
+    else:
+        C = normal(w.seed, T_C, w.M * w.N2, 1.0).reshape(w.M, w.N2)
+    return {"A": A, "B": B, "E": E, "C": C}
+
+
 def scaled(w: Workload, M: int, N: int, K: int, name: str | None = None, **kw) -> Workload:
     """The same recipe at other sizes (parity cases the oracle finishes quickly)."""
     return dataclasses.replace(w, name=name or f"{w.name}@{M}x{N}x{K}", M=M, N=N, K=K, **kw)

@@ -8,7 +8,10 @@ calls it, and it imports nothing from the CUDA package.
 ``gemm_oracle.c`` (the definition D[i][j] = C[i][j] + sum_k a[i][k] b[k][j]
 from "Tensor Core 数据布局的演进", overview, with the block-scaling rule of its
 section "Block-Scaled MMA 的 Scale Factors": one scale per 32 K elements
-(UE8M0, e4m3 or e2m1 operands) or per 16 (UE4M3, e2m1 operands)).
+(UE8M0, e4m3 or e2m1 operands) or per 16 (UE4M3, e2m1 operands)).  ``chain``
+is the two-product chain D = C + round(A·B)·E whose intermediate a tensor-core
+kernel keeps in tensor memory (same page, section "TMEM 中的累加器": some MMA
+forms read A from TMEM).
 ``layouts`` holds the pages' register-fragment and TMEM layout maps.
 
 Parity pins (tests/test_oracle_*.py): exhaustive format decodes against
@@ -70,6 +73,13 @@ def lib():
                           ("oracle_decode_e2m1", ctypes.c_uint8), ("oracle_decode_ue4m3", ctypes.c_uint8)]:
             f = getattr(L, name)
             f.argtypes = [arg]
+            f.restype = ctypes.c_double
+        L.oracle_chain.argtypes = [i64, i64, i64, i64, ctypes.c_int, vp, vp, vp, vp, i64, vp, dp, dp, dp, dp,
+                                   ctypes.c_int]
+        L.oracle_chain.restype = ctypes.c_int
+        for name in ("oracle_round_bf16", "oracle_round_f16"):
+            f = getattr(L, name)
+            f.argtypes = [ctypes.c_double]
             f.restype = ctypes.c_double
         L.oracle_threads.argtypes = [ctypes.c_int]
         L.oracle_threads.restype = ctypes.c_int
@@ -158,6 +168,42 @@ def gemm_entries(A, B, C, M: int, N: int, K: int, dtype: str, rows, cols, a_row_
     if rc != 0:
         raise ValueError("oracle_gemm_entries rejected its arguments")
     return D, S
+
+
+def round_to(x, dtype: str) -> np.ndarray:
+    """fp64 values rounded to bf16 / f16 (nearest, ties to even; overflow to infinity)."""
+    f = getattr(lib(), "oracle_round_" + dtype)
+    flat = np.asarray(x, dtype=np.float64).ravel()
+    return np.array([f(float(v)) for v in flat], dtype=np.float64).reshape(np.shape(x))
+
+
+def chain(A, B, E, C, M: int, N1: int, N2: int, K: int, dtype: str, rows=None, nthreads: int = 0):
+    """Two chained products: T = A·B, P = round(T) to ``dtype``, D = C + P·E.
+
+    A is (M, K) row-major, B (N1, K) (column-major K x N1), E (N2, N1) (column-major
+    N1 x N2), C (M, N2) fp32 or None.  Returns (T, S1, D, S2) for the listed rows
+    (default: all): T, S1 = sum_k |a b| of shape (rows, N1); D, S2 = sum_j |P e| of
+    shape (rows, N2).
+    """
+    width = np.uint16
+    A = np.ascontiguousarray(A, dtype=width)
+    B = np.ascontiguousarray(B, dtype=width)
+    E = np.ascontiguousarray(E, dtype=width)
+    if A.size != M * K or B.size != K * N1 or E.size != N1 * N2:
+        raise ValueError("operand sizes do not match M, N1, N2, K")
+    if C is not None:
+        C = np.ascontiguousarray(C, dtype=np.float32)
+        if C.size != M * N2:
+            raise ValueError("C size does not match M, N2")
+    rows = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.size
+    T = np.empty((n, N1)); S1 = np.empty((n, N1)); D = np.empty((n, N2)); S2 = np.empty((n, N2))
+    rc = lib().oracle_chain(M, N1, N2, K, DTYPES[dtype], _ptr(A), _ptr(B), _ptr(E), _ptr(C), n,
+                            rows.ctypes.data, T.ctypes.data, S1.ctypes.data, D.ctypes.data, S2.ctypes.data,
+                            nthreads)
+    if rc != 0:
+        raise ValueError("oracle_chain rejected its arguments")
+    return T, S1, D, S2
 
 
 def bf16_ulp(x) -> np.ndarray:

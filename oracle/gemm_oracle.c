@@ -253,3 +253,80 @@ int oracle_gemm_entries(int64_t M, int64_t N, int64_t K, int dtype,
     }
     return 0;
 }
+
+/*
+ * Round x to the nearest value with `p` significant bits and exponent floor
+ * `emin` (IEEE-style format with subnormals), ties to even; magnitudes that
+ * round beyond `maxv` become infinities.  bf16: p = 8, emin = -126,
+ * maxv = (2 - 2^-7) * 2^127; fp16: p = 11, emin = -14, maxv = 65504.
+ * x / q is exact (q a power of two), and rint rounds ties to even in the
+ * default rounding mode.
+ */
+static double round_to_format(double x, int p, int emin, double maxv) {
+    if (x == 0.0 || isnan(x) || isinf(x)) return x;
+    int e;
+    frexp(fabs(x), &e);                    /* |x| = m * 2^e, m in [0.5, 1) */
+    int ex = e - 1 < emin ? emin : e - 1;  /* unbiased exponent of |x|, subnormals share emin */
+    double q = ldexp(1.0, ex - (p - 1));
+    double r = rint(x / q) * q;
+    if (fabs(r) > maxv) return x > 0 ? INFINITY : -INFINITY;
+    return r;
+}
+
+double oracle_round_bf16(double x) { return round_to_format(x, 8, -126, ldexp(255.0, 120)); }
+double oracle_round_f16(double x) { return round_to_format(x, 11, -14, 65504.0); }
+
+/*
+ * Two chained products ("Tensor Core 数据布局的演进", section "TMEM 中的累加器":
+ * some tcgen05.mma forms read A from tensor memory, so a first product's
+ * result can feed a second without leaving the SM):
+ *
+ *     T[i][j] = sum_k a[i][k] * b[k][j]                 (M x N1, K terms)
+ *     P[i][j] = round(T[i][j])                          (to the operand format, RNE)
+ *     D[i][n] = C[i][n] + sum_j P[i][j] * e[j][n]       (M x N2, N1 terms)
+ *
+ * A is M x K row-major, B is K x N1 column-major (B[j*K + k]), E is
+ * N1 x N2 column-major (E[n*N1 + j]), C is M x N2 fp32 row-major or NULL;
+ * dtype is ORACLE_F16 or ORACLE_BF16 (operands and P).  For each listed row
+ * i = rows[r] it writes T, S1 = sum_k |a b| (r x N1), D, S2 = sum_j |P e|
+ * (r x N2), all fp64.  Returns 0, or -1 on a bad argument.
+ */
+int oracle_chain(int64_t M, int64_t N1, int64_t N2, int64_t K, int dtype, const void *A, const void *B,
+                 const void *E, const float *C, int64_t nrows, const int64_t *rows, double *T, double *S1,
+                 double *D, double *S2, int nthreads) {
+    if (M < 0 || N1 < 0 || N2 < 0 || K < 0 || nrows < 0) return -1;
+    if (dtype != ORACLE_F16 && dtype != ORACLE_BF16) return -1;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= M) return -1;
+    problem first, second;
+    if (make_problem(&first, M, N1, K, dtype, A, 1, B, 0, NULL, NULL, SCALE_NONE)) return -1;
+    if (make_problem(&second, M, N2, N1, dtype, NULL, 1, E, 0, NULL, NULL, SCALE_NONE)) return -1;
+    int nt = set_threads(nthreads);
+    #pragma omp parallel for num_threads(nt) schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows[r];
+        double *t = T + r * N1, *s1 = S1 + r * N1, *d = D + r * N2, *s2 = S2 + r * N2;
+        for (int64_t j = 0; j < N1; ++j) {
+            double acc = 0.0, sabs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double prod = a_elem(&first, i, k) * b_elem(&first, k, j);
+                acc += prod;
+                sabs += fabs(prod);
+            }
+            t[j] = acc;
+            s1[j] = sabs;
+        }
+        for (int64_t n = 0; n < N2; ++n) {
+            double acc = 0.0, sabs = 0.0;
+            for (int64_t j = 0; j < N1; ++j) {
+                double pv = dtype == ORACLE_BF16 ? oracle_round_bf16(t[j]) : oracle_round_f16(t[j]);
+                double prod = pv * b_elem(&second, j, n);
+                acc += prod;
+                sabs += fabs(prod);
+            }
+            d[n] = acc + (C ? (double)C[i * N2 + n] : 0.0);
+            s2[n] = sabs;
+        }
+    }
+    return 0;
+}

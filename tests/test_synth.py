@@ -122,3 +122,16 @@ def test_make_inputs_e2m1():
     w1 = synth.scaled(synth.WORKLOADS["mxf4e2m1_8192x8192x8192_c0_f32out"], 64, 48, 96)
     x1 = synth.make_inputs(w1)
     assert x1["SFA"].shape == (64, 3) and 123 <= x1["SFA"].min() and x1["SFA"].max() <= 131
+
+
+def test_chain_inputs():
+    w = synth.CHAIN_WORKLOADS["chain_bf16_32768x4096_256x256_bf16out"]
+    assert (w.M, w.K, w.N1, w.N2, w.ab, w.d) == (32768, 4096, 256, 256, "bf16", "bf16")
+    assert w.flops == 2 * 32768 * 256 * (4096 + 256)
+    s = synth.scaled_chain(w, 100, 24, 16, 64)
+    x = synth.make_chain_inputs(s)
+    assert x["A"].shape == (100, 64) and x["B"].shape == (24, 64) and x["E"].shape == (16, 24)
+    assert x["C"].shape == (100, 16) and x["A"].dtype == np.uint16
+    # E has its own stream: it is not a copy of a slice of A or B
+    assert not np.array_equal(x["E"].ravel(), x["B"].ravel()[:x["E"].size])
+    assert np.array_equal(synth.make_chain_inputs(s)["E"], x["E"])
