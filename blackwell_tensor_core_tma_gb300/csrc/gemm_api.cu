@@ -52,13 +52,16 @@ struct gemm_plan {
     int tile_k;               // K elements per stage
     int num_kb;
     int sfa_stage_bytes, sfb_stage_bytes;   // block-scaled: packed scales per stage (per CTA)
+    int64_t N2;               // chain plans: columns of D (N is the intermediate's N1)
+    const void *lastE;
+    void *hE;
     uint8_t *ws_a, *ws_b;     // block-scaled: packed scale factors (workspace)
     // device buffers of gemm_run_host (allocated on first use)
     void *hA, *hB, *hC, *hD;
     uint8_t *hSFA, *hSFB;
     // tensor maps of the last run, reused while the pointers repeat
     const void *lastA, *lastB, *lastC, *lastD;
-    CUtensorMap maps[NUM_MAPS];   // A, B, C, D, packed SFA, packed SFB
+    CUtensorMap maps[NUM_MAPS];   // A, B, C, D, packed SFA, packed SFB (chain plans: A, B, C, D, E)
     bool maps_valid;
 };
 
@@ -350,7 +353,7 @@ gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K, 
 
 gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C, void *D, const uint8_t *SFA,
                      const uint8_t *SFB, void *cuda_stream) {
-    if (!p || !A || !B || !D) return GEMM_ERR_INVALID_ARG;
+    if (!p || !A || !B || !D || p->family == FAMILY_CHAIN) return GEMM_ERR_INVALID_ARG;
     if (p->family != KIND_F16 && (!SFA || !SFB)) return GEMM_ERR_INVALID_ARG;
     if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (C && !aligned16(C))) return GEMM_ERR_ALIGNMENT;
     gemm_status st = encode_maps(p, A, B, C, D);
@@ -410,7 +413,7 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
 
 gemm_status gemm_run_host(gemm_plan_t p, const void *A, const void *B, const void *C, void *D, const uint8_t *SFA,
                           const uint8_t *SFB, void *cuda_stream) {
-    if (!p || !A || !B || !D) return GEMM_ERR_INVALID_ARG;
+    if (!p || !A || !B || !D || p->family == FAMILY_CHAIN) return GEMM_ERR_INVALID_ARG;
     const size_t a_bytes = bytes_of(p->ab, p->M * p->K);
     const size_t b_bytes = bytes_of(p->ab, p->K * p->N);
     const size_t c_bytes = (size_t)p->M * p->N * 4;
@@ -464,7 +467,9 @@ gemm_status gemm_plan_get_info(gemm_plan_t p, gemm_plan_info *info) {
     info->grid = p->grid;
     info->tiles = p->tiles;
     info->smem_bytes = p->smem;
-    info->launches_per_run = (p->family != KIND_F16 ? 2 : 1) + (p->splits > 1 ? 1 : 0);
+    // block-scaled plans also launch the scale-packing kernel, split-K plans the D = C kernel
+    const bool scaled = p->family != KIND_F16 && p->family != FAMILY_CHAIN;
+    info->launches_per_run = (scaled ? 2 : 1) + (p->splits > 1 ? 1 : 0);
     info->splits = p->splits;
     info->sm_count = p->sm_count;
     return GEMM_OK;
@@ -478,6 +483,7 @@ gemm_status gemm_plan_set_timeout(gemm_plan_t p, uint64_t ns) {
 
 gemm_status gemm_plan_set_split_k(gemm_plan_t p, int splits) {
     if (!p || splits < 0) return GEMM_ERR_INVALID_ARG;
+    if (p->family == FAMILY_CHAIN) return splits > 1 ? GEMM_ERR_UNSUPPORTED : GEMM_OK;
     if (splits > 1 && (p->d != GEMM_F32 || (p->flags & GEMM_FLAG_DETERMINISTIC))) return GEMM_ERR_UNSUPPORTED;
     p->split_request = splits;
     choose_splits(p);
@@ -493,10 +499,170 @@ gemm_status gemm_plan_destroy(gemm_plan_t p) {
     cudaFree(p->hD);
     cudaFree(p->hSFA);
     cudaFree(p->hSFB);
+    cudaFree(p->hE);
     cudaFree(p->ws_a);
     cudaFree(p->ws_b);
     delete p;
     return GEMM_OK;
+}
+
+// ------------------------------------------------------------ two-product chain
+
+gemm_status gemm_chain_plan_create(gemm_plan_t *out, int64_t M, int64_t N1, int64_t N2, int64_t K, gemm_dtype ab,
+                                   gemm_dtype d, unsigned flags) {
+    if (!out || M <= 0 || N1 <= 0 || N2 <= 0 || K <= 0) return GEMM_ERR_INVALID_ARG;
+    if (M > INT32_MAX || K > INT32_MAX) return GEMM_ERR_INVALID_ARG;
+    if ((unsigned)ab > GEMM_E2M1 || (unsigned)d > GEMM_E2M1) return GEMM_ERR_INVALID_ARG;
+    if ((flags & GEMM_FLAG_FORCE_1CTA) && (flags & GEMM_FLAG_FORCE_2CTA)) return GEMM_ERR_INVALID_ARG;
+    if ((ab != GEMM_F16 && ab != GEMM_BF16) || (d != GEMM_F32 && d != GEMM_BF16)) return GEMM_ERR_UNSUPPORTED;
+    // both products' accumulators share the 512 tensor-memory columns of one SM; single CTAs only
+    if (N1 > CHAIN_MAX_N || N2 > CHAIN_MAX_N || (flags & GEMM_FLAG_FORCE_2CTA)) return GEMM_ERR_UNSUPPORTED;
+    // 16-byte rows: A and B hold K elements, E N1, C N2 fp32, D N2
+    if ((K * 2) % 16 != 0 || (N1 * 2) % 16 != 0 || (N2 * 4) % 16 != 0 || (N2 * elem_bits(d) / 8) % 16 != 0)
+        return GEMM_ERR_ALIGNMENT;
+
+    int dev = 0;
+    cudaDeviceProp prop;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return GEMM_ERR_UNSUPPORTED;
+    if (chain_prepare(d == GEMM_BF16) != cudaSuccess) return GEMM_ERR_CUDA;
+
+    gemm_plan *p = new (std::nothrow) gemm_plan();
+    if (!p) return GEMM_ERR_CUDA;
+    p->M = M;
+    p->N = N1;
+    p->N2 = N2;
+    p->K = K;
+    p->ab = ab;
+    p->c = GEMM_F32;
+    p->d = d;
+    p->a_mn = p->b_mn = 0;
+    p->flags = flags;
+    p->device = dev;
+    p->sm_count = prop.multiProcessorCount;
+    p->timeout_ns = 1000000000ull;
+    p->family = FAMILY_CHAIN;
+    p->cta_group = 1;
+    p->stages = 4;
+    p->smem = chain_smem_bytes();
+    p->tile_n = (int)((N2 + 15) / 16 * 16);
+    p->tile_k = TILE_K16;
+    p->num_kb = (int)((K + TILE_K16 - 1) / TILE_K16);
+    p->tiles_m = (int)((M + TILE_M - 1) / TILE_M);
+    p->tiles_n = 1;
+    p->tiles = p->tiles_m;
+    p->capacity = p->sm_count;
+    p->grid = p->tiles < p->sm_count ? p->tiles : p->sm_count;
+    p->splits = 1;
+    if (cudaMalloc(&p->status, sizeof(int)) != cudaSuccess) {
+        delete p;
+        return GEMM_ERR_CUDA;
+    }
+    if (cudaMemset(p->status, 0, sizeof(int)) != cudaSuccess) {
+        cudaFree(p->status);
+        delete p;
+        return GEMM_ERR_CUDA;
+    }
+    *out = p;
+    return GEMM_OK;
+}
+
+namespace {
+
+gemm_status encode_chain_maps(gemm_plan *p, const void *A, const void *B, const void *E, const void *C, void *D) {
+    if (p->maps_valid && A == p->lastA && B == p->lastB && E == p->lastE && C == p->lastC && D == p->lastD)
+        return GEMM_OK;
+    if (!encoder()) return GEMM_ERR_CUDA;
+    std::memset(p->maps, 0, sizeof p->maps);
+    const CUtensorMapDataType dt = tma_dtype(p->ab);
+    const uint32_t n1p = (uint32_t)((p->N + 15) / 16 * 16), n2p = (uint32_t)p->tile_n;
+    bool ok = encode_2d(&p->maps[0], dt, 2, A, p->K, p->M, TILE_K16, TILE_M, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode_2d(&p->maps[1], dt, 2, B, p->K, p->N, TILE_K16, n1p, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode_2d(&p->maps[4], dt, 2, E, p->N, p->N2, TILE_K16, n2p, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (ok && C)
+        ok = encode_2d(&p->maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, p->N2, p->M, EPI_COLS, 32,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+    if (ok)
+        ok = p->d == GEMM_BF16 ? encode_2d(&p->maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, p->N2, p->M, EPI_COLS,
+                                           32, CU_TENSOR_MAP_SWIZZLE_64B)
+                               : encode_2d(&p->maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, p->N2, p->M, EPI_COLS,
+                                           32, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) {
+        p->maps_valid = false;
+        return GEMM_ERR_CUDA;
+    }
+    p->lastA = A;
+    p->lastB = B;
+    p->lastE = E;
+    p->lastC = C;
+    p->lastD = D;
+    p->maps_valid = true;
+    return GEMM_OK;
+}
+
+}  // namespace
+
+gemm_status gemm_chain_run(gemm_plan_t p, const void *A, const void *B, const void *E, const void *C, void *D,
+                           void *cuda_stream) {
+    if (!p || !A || !B || !E || !D || p->family != FAMILY_CHAIN) return GEMM_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(E) || !aligned16(D) || (C && !aligned16(C)))
+        return GEMM_ERR_ALIGNMENT;
+    gemm_status st = encode_chain_maps(p, A, B, E, C, D);
+    if (st != GEMM_OK) return st;
+    ChainParams cp{};
+    cp.M = (int)p->M;
+    cp.K = (int)p->K;
+    cp.N1 = (int)p->N;
+    cp.N2 = (int)p->N2;
+    cp.n1p = (int)((p->N + 15) / 16 * 16);
+    cp.n2p = p->tile_n;
+    cp.num_kb1 = p->num_kb;
+    cp.num_kb2 = (cp.n1p + TILE_K16 - 1) / TILE_K16;
+    cp.tiles = p->tiles;
+    cp.has_c = C != nullptr;
+    cp.f16 = p->ab == GEMM_F16;
+    const uint32_t bf = p->ab == GEMM_BF16 ? 1u : 0u;
+    cp.idesc1 = idesc_f16(bf, (uint32_t)TILE_M, (uint32_t)cp.n1p);
+    cp.idesc2 = idesc_f16(bf, (uint32_t)TILE_M, (uint32_t)cp.n2p);
+    cp.status = p->status;
+    cp.timeout_ns = p->timeout_ns;
+    cp.fault = p->fault;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
+    if (chain_launch(p->d == GEMM_BF16, p->grid, p->maps, cp, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (p->flags & GEMM_FLAG_SYNC) {
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
+        return gemm_plan_last_status(p);
+    }
+    return GEMM_OK;
+}
+
+gemm_status gemm_chain_run_host(gemm_plan_t p, const void *A, const void *B, const void *E, const void *C, void *D,
+                                void *cuda_stream) {
+    if (!p || !A || !B || !E || !D || p->family != FAMILY_CHAIN) return GEMM_ERR_INVALID_ARG;
+    const size_t a_bytes = (size_t)p->M * p->K * 2, b_bytes = (size_t)p->K * p->N * 2,
+                 e_bytes = (size_t)p->N * p->N2 * 2, c_bytes = (size_t)p->M * p->N2 * 4,
+                 d_bytes = bytes_of(p->d, p->M * p->N2);
+    if (!p->hA) {
+        if (cudaMalloc(&p->hA, a_bytes) != cudaSuccess || cudaMalloc(&p->hB, b_bytes) != cudaSuccess ||
+            cudaMalloc(&p->hE, e_bytes) != cudaSuccess || cudaMalloc(&p->hC, c_bytes) != cudaSuccess ||
+            cudaMalloc(&p->hD, d_bytes) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
+    if (cudaMemcpyAsync(p->hA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(p->hB, B, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+        cudaMemcpyAsync(p->hE, E, e_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (C && cudaMemcpyAsync(p->hC, C, c_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    const unsigned saved = p->flags;
+    p->flags &= ~GEMM_FLAG_SYNC;
+    gemm_status st = gemm_chain_run(p, p->hA, p->hB, p->hE, C ? p->hC : nullptr, p->hD, cuda_stream);
+    p->flags = saved;
+    if (st != GEMM_OK) return st;
+    if (cudaMemcpyAsync(D, p->hD, d_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    return gemm_plan_last_status(p);
 }
 
 // Test hook (declared in include/gb300gemm_testing.h): make the next runs'

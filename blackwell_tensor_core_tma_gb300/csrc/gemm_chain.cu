@@ -1,0 +1,328 @@
+// Two chained tensor-core products with the intermediate kept in tensor memory
+// ("Tensor Core 数据布局的演进", section "TMEM 中的累加器": some tcgen05.mma forms
+// read A from TMEM instead of shared memory):
+//     T = A·B        128 x N1 per tile, fp32 accumulator in TMEM columns [0, 256)
+//     P = round(T)   to the operand type, written back over T's first columns: two
+//                    16-bit elements per 32-bit column, the lower K index in the low half
+//     D = C + P·E    tcgen05.mma with A = P read from TMEM and E from shared memory,
+//                    fp32 accumulator in TMEM columns [256, 512)
+// so the intermediate never leaves the SM.  One CTA owns a 128-row tile at a
+// time and walks the tiles persistently.  Warp roles (192 threads):
+//   warp 0     TMA producer: per tile the K blocks of A and B, then the K blocks
+//              of E, through one STAGES-deep ring (a stage holds A 128 x 64 and
+//              B N1 x 64, or E N2 x 64; 128-byte swizzled rows).
+//   warp 1     allocates the 512 TMEM columns; lane 0 issues both products' MMAs.
+//   warps 2-5  per tile: round T into P (tcgen05.ld, cvt, tcgen05.st), then the D
+//              epilogue (tcgen05.ld, + C, convert, TMA store), each warp in its own
+//              32-lane TMEM window.
+// Every wait is bounded: when one runs out the kernel records GEMM_ERR_TIMEOUT,
+// its roles stop, and it still frees its tensor memory.
+#include "gemm_kernel.cuh"
+
+namespace gb300 {
+namespace {
+
+template <bool OUT_BF16_>
+struct ChainCfg {
+    static constexpr bool OUT_BF16 = OUT_BF16_;
+    static constexpr int THREADS = 192;
+    static constexpr int STAGES = 4;
+    static constexpr int BK = 64;                                     // 16-bit K elements per stage
+    static constexpr int A_BYTES = TILE_M * 128;                      // 16 KiB
+    static constexpr int STAGE_BYTES = A_BYTES + CHAIN_MAX_N * 128;   // 48 KiB: A and B, or E
+    static constexpr int EPI_BUF = 32 * EPI_COLS * 4;                 // one 32 x 32 fp32 box
+    static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
+    static constexpr int OFF_BAR = OFF_EPI + 4 * 2 * EPI_BUF;
+    // full[STAGES], empty[STAGES], tfull, pready, dfull, dempty, cload[4][2], drain
+    static constexpr int NBAR = 2 * STAGES + 4 + 8 + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;               // tmem base slot, abort flag
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;           // + alignment slack
+    static constexpr uint32_t T_COL = 0, D_COL = 256;
+    static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && OFF_EPI % 1024 == 0, "1024-byte aligned");
+    static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
+};
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, 1)
+    chain_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                 const __grid_constant__ CUtensorMap tmE, const ChainParams p) {
+    constexpr int STAGES = Cfg::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + STAGES;
+    uint64_t *tfull = bars + 2 * STAGES;   // first product complete (MMA -> epilogue)
+    uint64_t *pready = tfull + 1;          // P written into TMEM (epilogue -> MMA)
+    uint64_t *dfull = tfull + 2;           // second product complete (MMA -> epilogue, MMA)
+    uint64_t *dempty = tfull + 3;          // D read out of TMEM (epilogue -> MMA)
+    uint64_t *cload = tfull + 4;
+    uint64_t *drain = cload + 8;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 4);
+    const Waiter W{abort_flag, p.status, p.timeout_ns};
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmE);
+        prefetch_tensormap(&tmD);
+        if (p.has_c) prefetch_tensormap(&tmC);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(tfull, 1);
+        mbar_init(pready, 4);
+        mbar_init(dfull, 1);
+        mbar_init(dempty, 4);
+        for (int i = 0; i < 8; ++i) mbar_init(&cload[i], 1);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc<1>(smem_addr(tmem_slot), 512);
+        tmem_relinquish<1>();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+                const int m0 = t * TILE_M;
+                for (int kb = 0; kb < p.num_kb1 + p.num_kb2; ++kb) {
+                    if (!W.wait(&empty[s], ph ^ 1u)) { ok = false; break; }
+                    const bool withhold = p.fault == 1 && t == (int)blockIdx.x && kb == 0;
+                    uint8_t *st = smem + s * Cfg::STAGE_BYTES;
+                    const uint32_t fb = smem_addr(&full[s]);
+                    if (kb < p.num_kb1) {         // A rows m0.., B rows 0..n1p of K block kb
+                        if (!withhold) mbar_arrive_expect_tx(&full[s], Cfg::A_BYTES + p.n1p * 128);
+                        tma_load_2d(smem_addr(st), &tmA, fb, kb * Cfg::BK, m0);
+                        tma_load_2d(smem_addr(st + Cfg::A_BYTES), &tmB, fb, kb * Cfg::BK, 0);
+                    } else {                      // E rows 0..n2p of K block kb - num_kb1
+                        mbar_arrive_expect_tx(&full[s], p.n2p * 128);
+                        tma_load_2d(smem_addr(st), &tmE, fb, (kb - p.num_kb1) * Cfg::BK, 0);
+                    }
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            const uint32_t t_tmem = tmem_base + Cfg::T_COL;
+            const uint32_t d_tmem = tmem_base + Cfg::D_COL;
+            int s = 0;
+            uint32_t ph = 0, it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x, ++it) {
+                // T's columns are free once the previous tile's second product (which read
+                // P from them) has completed
+                if (it > 0 && !W.wait(dfull, (it - 1) & 1u)) break;
+                tc_fence_after_sync();
+                for (int kb = 0; kb < p.num_kb1; ++kb) {
+                    if (!W.wait(&full[s], ph)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    const uint32_t st = smem_addr(smem + s * Cfg::STAGE_BYTES);
+                    const uint64_t ad = smem_desc(st, 16, 1024, SWZ_128B);
+                    const uint64_t bd = smem_desc(st + Cfg::A_BYTES, 16, 1024, SWZ_128B);
+#pragma unroll
+                    for (int k = 0; k < Cfg::BK / 16; ++k)   // 32 bytes of K = 2 descriptor units
+                        mma_f16<1>(t_tmem, ad + 2 * k, bd + 2 * k, p.idesc1, (kb != 0) | (k != 0));
+                    tc_commit<1>(smem_addr(&empty[s]));
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit<1>(smem_addr(tfull));
+                // P is in TMEM, and the previous tile's D has been read out
+                if (!W.wait(pready, it & 1u) || !W.wait(dempty, (it & 1u) ^ 1u)) break;
+                tc_fence_after_sync();
+                for (int j = 0; j < p.num_kb2; ++j) {
+                    if (!W.wait(&full[s], ph)) { ok = false; break; }
+                    tc_fence_after_sync();
+                    const uint64_t ed = smem_desc(smem_addr(smem + s * Cfg::STAGE_BYTES), 16, 1024, SWZ_128B);
+#pragma unroll
+                    for (int k = 0; k < Cfg::BK / 16; ++k) {
+                        const int kk = j * Cfg::BK + 16 * k;   // K index of the second product
+                        if (kk < p.n1p) mma_f16_ts(d_tmem, t_tmem + kk / 2, ed + 2 * k, p.idesc2, kk != 0);
+                    }
+                    tc_commit<1>(smem_addr(&empty[s]));
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit<1>(smem_addr(dfull));
+            }
+            // every MMA this thread issued has finished before teardown
+            tc_commit<1>(smem_addr(drain));
+            W.wait(drain, 0, false);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int e = warp - 2;                           // epilogue warp index
+        const int q = warp & 3;                           // TMEM lane window of this warp
+        const uint32_t lanes = (uint32_t)(32 * q) << 16;
+        uint8_t *ebuf = smem + Cfg::OFF_EPI + e * 2 * Cfg::EPI_BUF;
+        uint64_t *cb = cload + 2 * e;
+        const uint64_t stream_pol = l2_policy_evict_first();
+        const int t_chunks = (p.n1p + 31) / 32;
+        const int d_chunks = (p.n2p + EPI_COLS - 1) / EPI_COLS;
+        // ec counts the 32 x 32 boxes this warp has stored; box ec uses staging buffer
+        // ec % 2, and its C load is that buffer's (ec / 2)-th
+        uint32_t it = 0, ec = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x, ++it) {
+            const int m_warp = t * TILE_M + 32 * q;
+            // P = round(T): chunk c of 32 fp32 columns becomes 16 columns of packed pairs at
+            // column 16c, over columns whose T values this warp has already read
+            if (!__all_sync(0xffffffffu, W.wait(tfull, it & 1u))) break;
+            tc_fence_after_sync();
+            for (int c = 0; c < t_chunks; ++c) {
+                uint32_t acc[32];
+                tmem_ld_32x32b_x32(tmem_base + lanes + Cfg::T_COL + 32 * c, acc);
+                tmem_ld_wait(acc);
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float lo = __uint_as_float(acc[2 * i]), hi = __uint_as_float(acc[2 * i + 1]);
+                    pk[i] = p.f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+                }
+                tmem_st_32x32b_x16(tmem_base + lanes + Cfg::T_COL + 16 * c, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pready);
+
+            // D = C + P·E: 32 x 32 boxes that lie wholly outside D are neither loaded nor stored
+            const int chunks_in = m_warp < p.M ? (p.N2 + EPI_COLS - 1) / EPI_COLS : 0;
+            const bool use_c = p.has_c && chunks_in > 0;
+            if (use_c && lane == 0) {      // the first C box loads while the second product runs
+                bulk_wait_group_read0();
+                mbar_arrive_expect_tx(&cb[ec & 1u], Cfg::EPI_BUF);
+                tma_load_2d_hint(smem_addr(ebuf + (ec & 1u) * Cfg::EPI_BUF), &tmC, smem_addr(&cb[ec & 1u]), 0, m_warp,
+                                 stream_pol);
+            }
+            if (!__all_sync(0xffffffffu, W.wait(dfull, it & 1u))) break;
+            tc_fence_after_sync();
+            for (int j = 0; j < d_chunks && ok; ++j) {
+                uint32_t acc[32];
+                tmem_ld_32x32b_x32(tmem_base + lanes + Cfg::D_COL + EPI_COLS * j, acc);
+                tmem_ld_wait(acc);
+                if (j == d_chunks - 1) {      // D's columns are free once every chunk is in registers
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(dempty);
+                }
+                if (j >= chunks_in) continue;
+                const uint32_t cur = ec & 1u;
+                uint8_t *buf = ebuf + cur * Cfg::EPI_BUF;
+                if (use_c && j + 1 < chunks_in && lane == 0) {
+                    const uint32_t nx = cur ^ 1u;
+                    bulk_wait_group_read0();                  // the store from buffer nx has read it
+                    mbar_arrive_expect_tx(&cb[nx], Cfg::EPI_BUF);
+                    tma_load_2d_hint(smem_addr(ebuf + nx * Cfg::EPI_BUF), &tmC, smem_addr(&cb[nx]), EPI_COLS * (j + 1),
+                                     m_warp, stream_pol);
+                }
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
+                if (use_c) {
+                    if (!__all_sync(0xffffffffu, W.wait(&cb[cur], (ec >> 1) & 1u))) { ok = false; break; }
+                    // row `lane` of the 128-byte-swizzled fp32 box: 16-byte chunk c at (c ^ (row % 8))
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float4 cv = *reinterpret_cast<const float4 *>(buf + lane * 128 + ((c ^ (lane & 7)) << 4));
+                        v[4 * c + 0] += cv.x;
+                        v[4 * c + 1] += cv.y;
+                        v[4 * c + 2] += cv.z;
+                        v[4 * c + 3] += cv.w;
+                    }
+                } else if (lane == 0) {
+                    bulk_wait_group_read1();                  // the store two boxes back has read this buffer
+                }
+                __syncwarp();
+                if constexpr (Cfg::OUT_BF16) {
+                    // 64-byte rows, 64-byte swizzle: chunk c at (c ^ ((row / 2) % 4))
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 w;
+                        w.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
+                        w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+                        w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+                        w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+                        *reinterpret_cast<uint4 *>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = w;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<float4 *>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                            make_float4(v[4 * c + 0], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d_hint(&tmD, smem_addr(buf), EPI_COLS * j, m_warp, stream_pol);
+                    bulk_commit_group();
+                }
+                ++ec;
+            }
+        }
+        if (lane == 0) bulk_wait_group0();
+    }
+
+    // ----------------------------------------------------------------- teardown
+    __syncwarp();
+    if (*abort_flag) {
+        // give copies that were already in flight time to land before the
+        // shared memory they target is released
+        for (int i = 0; i < 64; ++i) __nanosleep(1000);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc<1>(tmem_base, 512);
+    }
+}
+
+template <bool OUT_BF16>
+cudaError_t launch_chain(int grid, const CUtensorMap *maps, const ChainParams &p, cudaStream_t stream) {
+    using Cfg = ChainCfg<OUT_BF16>;
+    chain_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int chain_smem_bytes() { return ChainCfg<false>::SMEM_BYTES; }
+
+cudaError_t chain_prepare(int out_bf16) {
+    const void *fn = out_bf16 ? reinterpret_cast<const void *>(&chain_kernel<ChainCfg<true>>)
+                              : reinterpret_cast<const void *>(&chain_kernel<ChainCfg<false>>);
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem_bytes());
+}
+
+cudaError_t chain_launch(int out_bf16, int grid, const CUtensorMap *maps, const ChainParams &p, cudaStream_t stream) {
+    return out_bf16 ? launch_chain<true>(grid, maps, p, stream) : launch_chain<false>(grid, maps, p, stream);
+}
+
+}  // namespace gb300

@@ -58,6 +58,9 @@ cudaError_t init_d_launch(float *D, const float *C, size_t n, int sm_count, cuda
 //   KIND_NVF4  e2m1 with a UE4M3 scale per 16 K, kind::mxf4nvf4 scale_vec::4X
 enum GemmKind { KIND_F16 = 0, KIND_MXF8 = 1, KIND_MXF4 = 2, KIND_NVF4 = 3 };
 
+// plan family of the two-product chain (gemm_chain.cu)
+constexpr int FAMILY_CHAIN = 4;
+
 // Static shape of a block-scaled kernel instance (per CTA group)
 struct ScaledShape {
     int tile_n;      // columns of D per tile
@@ -86,6 +89,25 @@ const ScaledFamily &family_nvf4();   // gemm_nvf4.cu
 // matrices read as `pad` (the format's 1.0).
 cudaError_t sf_pack(const uint8_t *sfa, const uint8_t *sfb, uint8_t *out_a, uint8_t *out_b, int M, int N, int sfk,
                     int row_blocks, int tiles_n, int tile_n, int n_wg, uint8_t pad, cudaStream_t stream);
+
+// Two chained products D = C + round(A·B)·E (gemm_chain.cu): parameters of one launch
+struct ChainParams {
+    int M, K, N1, N2;
+    int n1p, n2p;        // N1 and N2 rounded up to the MMA's N granule (16)
+    int num_kb1;         // 64-element K blocks of the first product
+    int num_kb2;         // 64-element K blocks of the second product (over n1p)
+    int tiles;           // 128-row tiles of D
+    int has_c;
+    int f16;             // operands (and the rounded intermediate) fp16, else bf16
+    uint32_t idesc1, idesc2;
+    int *status;
+    uint64_t timeout_ns;
+    int fault;
+};
+constexpr int CHAIN_MAX_N = 256;   // N1 and N2 limits: both products' accumulators share 512 TMEM columns
+int chain_smem_bytes();
+cudaError_t chain_prepare(int out_bf16);
+cudaError_t chain_launch(int out_bf16, int grid, const CUtensorMap *maps, const ChainParams &p, cudaStream_t stream);
 
 constexpr int TILE_M = 128;   // rows of D per CTA
 constexpr int TILE_N = 256;   // columns of D per CTA (and per CTA pair)

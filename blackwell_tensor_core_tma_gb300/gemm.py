@@ -23,7 +23,8 @@ DTYPE = {"f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM_E4M3, "f32": GEMM_F32,
 # every symbol include/gb300gemm.h and include/gb300gemm_testing.h declare
 EXPORTS = ["gemm_plan_create", "gemm_run", "gemm_run_host", "gemm_plan_last_status", "gemm_plan_get_info",
            "gemm_plan_set_timeout", "gemm_plan_destroy", "gemm_status_string", "gemm_testing_set_fault",
-           "gemm_run_noalloc", "gemm_plan_set_split_k"]
+           "gemm_run_noalloc", "gemm_plan_set_split_k", "gemm_chain_plan_create", "gemm_chain_run",
+           "gemm_chain_run_host"]
 
 
 class GemmError(RuntimeError):
@@ -75,6 +76,12 @@ def lib():
         L.gemm_plan_set_split_k.restype = st
         L.gemm_run_noalloc.argtypes = [i64, i64, i64, st, st, vp, vp, vp, vp, vp, st]
         L.gemm_run_noalloc.restype = st
+        L.gemm_chain_plan_create.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i64, st, st, ctypes.c_uint]
+        L.gemm_chain_plan_create.restype = st
+        for name in ("gemm_chain_run", "gemm_chain_run_host"):
+            f = getattr(L, name)
+            f.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+            f.restype = st
         _lib = L
     return _lib
 
@@ -126,6 +133,25 @@ def gemm_run(plan: int, A, B, C, D, SFA=None, SFB=None, stream=None) -> int:
 def gemm_run_host(plan: int, A, B, C, D, SFA=None, SFB=None, stream=None) -> int:
     st = lib().gemm_run_host(plan, _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(SFA), _ptr(SFB), _stream(stream))
     _check(st, "gemm_run_host")
+    return st
+
+
+def gemm_chain_plan_create(M: int, N1: int, N2: int, K: int, ab="bf16", d="f32", flags: int = 0) -> int:
+    out = ctypes.c_void_p()
+    st = lib().gemm_chain_plan_create(ctypes.byref(out), M, N1, N2, K, DTYPE.get(ab, ab), DTYPE.get(d, d), flags)
+    _check(st, "gemm_chain_plan_create")
+    return out.value
+
+
+def gemm_chain_run(plan: int, A, B, E, C, D, stream=None) -> int:
+    st = lib().gemm_chain_run(plan, _ptr(A), _ptr(B), _ptr(E), _ptr(C), _ptr(D), _stream(stream))
+    _check(st, "gemm_chain_run")
+    return st
+
+
+def gemm_chain_run_host(plan: int, A, B, E, C, D, stream=None) -> int:
+    st = lib().gemm_chain_run_host(plan, _ptr(A), _ptr(B), _ptr(E), _ptr(C), _ptr(D), _stream(stream))
+    _check(st, "gemm_chain_run_host")
     return st
 
 
@@ -209,3 +235,18 @@ class Plan:
             self.close()
         except Exception:
             pass
+
+
+class ChainPlan(Plan):
+    """Owning wrapper of a two-product chain plan: D = C + round(A·B)·E."""
+
+    def __init__(self, M, N1, N2, K, ab="bf16", d="f32", flags=0):
+        self.M, self.N1, self.N2, self.K, self.ab, self.d = M, N1, N2, K, ab, d
+        self.handle = None
+        self.handle = gemm_chain_plan_create(M, N1, N2, K, ab, d, flags)
+
+    def run(self, A, B, E, C, D, stream=None):
+        return gemm_chain_run(self.handle, A, B, E, C, D, stream)
+
+    def run_host(self, A, B, E, C, D, stream=None):
+        return gemm_chain_run_host(self.handle, A, B, E, C, D, stream)

@@ -219,6 +219,36 @@ gemm_status gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype ab, gem
                              const void *A, const void *B, const void *C, void *D,
                              void *cuda_stream, int wait);
 
+/*
+ * Two chained products with the intermediate kept on chip ("Tensor Core 数据布局的
+ * 演进", section "TMEM 中的累加器": some tcgen05.mma forms read their A operand from
+ * tensor memory, so a first product's result can feed a second one without a
+ * round trip through global memory):
+ *
+ *     T[i][j] = sum_k a[i][k] * b[k][j]               (fp32 accumulation)
+ *     P[i][j] = T[i][j] rounded to the operand type   (round to nearest even)
+ *     D[i][n] = C[i][n] + sum_j P[i][j] * e[j][n]      (fp32 accumulation)
+ *
+ * A is M x K row-major, B is K x N1 column-major (element (k,j) at B[j*K + k]),
+ * E is N1 x N2 column-major (element (j,n) at E[n*N1 + j]), C is M x N2 fp32
+ * row-major or NULL, D is M x N2 row-major fp32 or bf16.  ab (A, B, E and P) is
+ * GEMM_F16 or GEMM_BF16.  1 <= N1, N2 <= 256 (both products' accumulators share
+ * one SM's 512 tensor-memory columns; otherwise GEMM_ERR_UNSUPPORTED, as is
+ * GEMM_FLAG_FORCE_2CTA); K and N1 multiples of 8, N2 a multiple of 4 (fp32 D)
+ * or 8 (bf16 D), else GEMM_ERR_ALIGNMENT.  The plan works with
+ * gemm_plan_last_status, gemm_plan_get_info, gemm_plan_set_timeout and
+ * gemm_plan_destroy; gemm_run / gemm_run_host reject it (GEMM_ERR_INVALID_ARG),
+ * and gemm_plan_set_split_k accepts only 0 or 1.  Pointers, streams, errors and
+ * GEMM_FLAG_SYNC behave as for gemm_run; gemm_chain_run_host is the host-buffer
+ * form (like gemm_run_host).
+ */
+gemm_status gemm_chain_plan_create(gemm_plan_t *out, int64_t M, int64_t N1, int64_t N2, int64_t K,
+                                   gemm_dtype ab, gemm_dtype d, unsigned flags);
+gemm_status gemm_chain_run(gemm_plan_t p, const void *A, const void *B, const void *E, const void *C,
+                           void *D, void *cuda_stream);
+gemm_status gemm_chain_run_host(gemm_plan_t p, const void *A, const void *B, const void *E, const void *C,
+                                void *D, void *cuda_stream);
+
 /* Static description of a status code. */
 const char *gemm_status_string(gemm_status s);
 

@@ -115,3 +115,62 @@ def _assert_within(w, D, D_ref, S, c, what):
         raise AssertionError(
             f"{w.name} ({what}): {idx.size} of {err.size} entries outside tolerance; worst flat index {k}: "
             f"gpu {D.ravel()[k]!r} ref {D_ref.ravel()[k]!r} tol {tol.ravel()[k]!r}")
+
+
+# ------------------------------------------------------------ two-product chain
+
+def run_chain(w, flags: int = 0, c_none: bool = False, guard: int = 0, inputs=None, reps: int = 1):
+    """Run a ChainWorkload through gemm_chain_run; returns (inputs, D as fp64, plan info, status, guard intact)."""
+    import torch
+    x = inputs if inputs is not None else synth.make_chain_inputs(w)
+    A, B, E = to_device(x["A"]), to_device(x["B"]), to_device(x["E"])
+    C = None if c_none else to_device(x["C"])
+    tdt = torch.bfloat16 if w.d == "bf16" else torch.float32
+    n = w.M * w.N2
+    g = guard
+    buf = torch.full((n + 2 * g,), float("nan"), dtype=tdt, device="cuda")
+    D = buf[g:g + n].view(w.M, w.N2)
+    with gemm.ChainPlan(w.M, w.N1, w.N2, w.K, w.ab, w.d, flags) as plan:
+        for _ in range(reps):
+            plan.run(A, B, E, C, D, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        status = plan.last_status()
+        info = plan.info
+    intact = True
+    if g:
+        intact = bool(torch.isnan(buf[:g]).all().item()) and bool(torch.isnan(buf[g + n:]).all().item())
+    return x, decode_d(D, w.d), info, status, intact
+
+
+def format_ulp(x, dtype: str) -> np.ndarray:
+    """Spacing of the bf16 / fp16 grid at |x| (subnormal spacing below the smallest normal)."""
+    p, emin = (8, -126) if dtype == "bf16" else (11, -14)
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    _, e = np.frexp(a)
+    ex = np.where(a > 0, np.maximum(e - 1, emin), emin)
+    return np.ldexp(1.0, ex - (p - 1))
+
+
+def check_chain(w, x, D, rows=None, c_none=False):
+    """D against the oracle's chain on the listed rows (all by default).
+
+    The intermediate is rounded from the exact sum by the oracle and from an fp32 sum by
+    the GPU, so an element of P may differ by one unit of the format at |T| plus the
+    first product's accumulation error; the bound carries that through E:
+        |dD| <= REL_S * S2 + REL_C * |c| + sum_j (ulp(|T| + REL_S * S1) + REL_S * S1)_ij * |e_jn|
+    (+ one bf16 ulp of D for bf16 D).
+    """
+    rows = np.arange(w.M) if rows is None else np.asarray(rows, dtype=np.int64)
+    C = None if c_none else x["C"]
+    T, S1, D_ref, S2 = oracle.chain(x["A"], x["B"], x["E"], C, w.M, w.N1, w.N2, w.K, w.ab, rows=rows)
+    e_abs = np.abs(oracle.decode(x["E"], w.ab)).T                   # (N1, N2)
+    slack = (format_ulp(np.abs(T) + REL_S * S1, w.ab) + REL_S * S1) @ e_abs
+    c = np.zeros_like(D_ref) if c_none else x["C"][rows].astype(np.float64)
+    tol = REL_S * S2 + REL_C * np.abs(c) + slack
+    if w.d == "bf16":
+        tol = tol + oracle.bf16_ulp(D_ref)
+    err = np.abs(D[rows] - D_ref)
+    bad = ~(err <= tol)
+    assert not bad.any(), (f"{w.name}: {int(bad.sum())} of {bad.size} entries out of tolerance; worst "
+                           f"err/tol {float(np.max(err / np.maximum(tol, 1e-300))):.3g}")
+    return float(np.max(err / np.maximum(tol, 1e-300)))

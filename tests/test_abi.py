@@ -99,3 +99,24 @@ def test_no_cpu_fallback_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(gemm, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU path"):
         gemm.lib()
+
+
+@pytest.mark.parametrize("args,kw,status", [
+    ((0, 64, 64, 64), {}, gemm.GEMM_ERR_INVALID_ARG),
+    ((128, 264, 64, 64), {}, gemm.GEMM_ERR_UNSUPPORTED),                    # N1 > 256
+    ((128, 64, 272, 64), {}, gemm.GEMM_ERR_UNSUPPORTED),                    # N2 > 256
+    ((128, 64, 64, 64), {"ab": "e4m3"}, gemm.GEMM_ERR_UNSUPPORTED),
+    ((128, 64, 64, 64), {"flags": gemm.GEMM_FLAG_FORCE_2CTA}, gemm.GEMM_ERR_UNSUPPORTED),
+    ((128, 64, 64, 60), {}, gemm.GEMM_ERR_ALIGNMENT),                       # K rows of 120 bytes
+    ((128, 60, 64, 64), {}, gemm.GEMM_ERR_ALIGNMENT),                       # E rows of N1 = 60
+    ((128, 64, 12, 64), {"d": "bf16"}, gemm.GEMM_ERR_ALIGNMENT),            # bf16 D rows of 24 bytes
+])
+def test_chain_plan_rejects_before_device(lib, args, kw, status):
+    with pytest.raises(gemm.GemmError) as e:
+        gemm.gemm_chain_plan_create(*args, **kw)
+    assert e.value.status == status
+
+
+def test_chain_calls_reject_null(lib):
+    assert lib.gemm_chain_run(None, None, None, None, None, None, None) == gemm.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_chain_run_host(None, None, None, None, None, None, None) == gemm.GEMM_ERR_INVALID_ARG

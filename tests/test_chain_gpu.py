@@ -1,0 +1,84 @@
+"""GPU parity of the two-product chain D = C + round(A·B)·E, whose intermediate
+stays in tensor memory and feeds the second product as its A operand (the
+tcgen05.mma form that reads A from TMEM), through the C ABI against the
+oracle: ragged M, K, N1 and N2, fp16 and bf16 operands, fp32 and bf16 D, C
+present or absent, repeated runs, the full-size workload on sampled rows, and
+the bounded-wait timeout."""
+import numpy as np
+import pytest
+
+from blackwell_tensor_core_tma_gb300 import gemm, synth
+from tests import gpucase
+
+pytestmark = pytest.mark.gpu
+
+CW = synth.CHAIN_WORKLOADS["chain_bf16_32768x4096_256x256_bf16out"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gemm.lib()
+
+
+@pytest.mark.parametrize("M,K,N1,N2,ab,d", [
+    (128, 64, 16, 8, "bf16", "f32"),          # one tile, one K block, the smallest N1 and N2
+    (300, 520, 200, 136, "bf16", "f32"),      # ragged M and K, N1 and N2 not multiples of 32
+    (1000, 2048, 256, 256, "bf16", "bf16"),   # the full TMEM split, bf16 D
+    (260, 1024, 72, 40, "f16", "f32"),        # fp16 operands and intermediate
+    (512, 136, 248, 256, "f16", "bf16"),      # N1 rounds up to 256 inside the kernel
+])
+def test_chain_parity(M, K, N1, N2, ab, d):
+    w = synth.scaled_chain(CW, M, N1, N2, K, ab=ab, d=d)
+    x, D, info, st, intact = gpucase.run_chain(w, guard=512)
+    assert st == gemm.GEMM_OK and intact
+    assert info["cta_group"] == 1 and info["launches_per_run"] == 1
+    gpucase.check_chain(w, x, D)
+
+
+def test_chain_c_none_and_repeat():
+    w = synth.scaled_chain(CW, 640, 128, 96, 384)
+    x, D, info, st, intact = gpucase.run_chain(w, c_none=True, guard=256, reps=3)
+    assert st == gemm.GEMM_OK and intact
+    gpucase.check_chain(w, x, D, c_none=True)
+
+
+def test_chain_full_size_sampled_rows():
+    w = CW
+    x, D, info, st, intact = gpucase.run_chain(w, guard=1024)
+    assert st == gemm.GEMM_OK and intact
+    rng = np.random.default_rng(0)
+    edges = [r for t in range(0, w.M, 128 * 37) for r in (t, t + 31, t + 32, t + 127) if r < w.M]
+    rows = np.unique(np.concatenate([edges, [w.M - 1], rng.integers(0, w.M, 160)]))
+    gpucase.check_chain(w, x, D, rows=rows)
+
+
+def test_chain_rejected_by_gemm_run():
+    import torch
+    with gemm.ChainPlan(128, 64, 64, 64) as plan:
+        z = torch.zeros(128 * 128, dtype=torch.float32, device="cuda")
+        with pytest.raises(gemm.GemmError) as e:
+            gemm.gemm_run(plan.handle, z, z, None, z)
+        assert e.value.status == gemm.GEMM_ERR_INVALID_ARG
+
+
+def test_chain_timeout_and_recovery():
+    import torch
+    w = synth.scaled_chain(CW, 384, 128, 64, 256)
+    x = synth.make_chain_inputs(w)
+    A, B, E, C = (gpucase.to_device(x[k]) for k in ("A", "B", "E", "C"))
+    D = torch.zeros((w.M, w.N2), dtype=torch.bfloat16, device="cuda")
+    with gemm.ChainPlan(w.M, w.N1, w.N2, w.K, w.ab, w.d) as plan:
+        plan.set_timeout(20_000_000)
+        gemm.gemm_testing_set_fault(plan.handle, 1)
+        plan.run(A, B, E, C, D, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        assert plan.last_status() == gemm.GEMM_ERR_TIMEOUT
+        gemm.gemm_testing_set_fault(plan.handle, 0)
+        plan.set_timeout(1_000_000_000)
+        plan.run(A, B, E, C, D, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        assert plan.last_status() == gemm.GEMM_OK
+    gpucase.check_chain(w, x, gpucase.decode_d(D, w.d))
