@@ -47,6 +47,8 @@ MEASURED_TRAFFIC = {
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
     "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 516495360 + 220410112, "src": "42e223774c6a4671",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
+    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312352000 + 11990528, "src": "c0c10fd3a749e02b",
+                                              "ncu": "profiles/chain_kernel_bf16_32768x4096_256x256_launches.md"},
 }
 
 
@@ -55,11 +57,12 @@ KERNEL_SOURCES = {
     "mxf8": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_mxf8.cu"],
     "mxf4": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_mxf4.cu"],
     "nvf4": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_nvf4.cu"],
+    "chain": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_chain.cu"],
 }
 
 
 def kernel_family(workload_name: str) -> str:
-    for fam in ("mxf8", "mxf4", "nvf4"):
+    for fam in ("mxf8", "mxf4", "nvf4", "chain"):
         if workload_name.startswith(fam):
             return fam
     return "f16"
@@ -197,6 +200,12 @@ def smi_index(local_rank: int) -> int:
 
 def workload(args):
     from blackwell_tensor_core_tma_gb300 import synth
+    if args.workload in synth.CHAIN_WORKLOADS:
+        w = synth.CHAIN_WORKLOADS[args.workload]
+        if args.shape:
+            M, N1, N2, K = (int(v) for v in args.shape.lower().split("x"))
+            w = synth.scaled_chain(w, M, N1, N2, K)
+        return w
     w = synth.WORKLOADS[args.workload]
     if args.shape:
         M, N, K = (int(v) for v in args.shape.lower().split("x"))
@@ -334,6 +343,139 @@ def run_ours(args, rank, world, local_rank):
     return out
 
 
+def run_ours_chain(args, rank, world, local_rank):
+    """The two-product chain D = C + round(A·B)·E through gemm_chain_run."""
+    import numpy as np
+    import torch
+
+    from blackwell_tensor_core_tma_gb300 import gemm, synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = workload(args)
+    x = synth.make_chain_inputs(w)
+
+    def dev_tensor(a):
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    A, B, E, C = (dev_tensor(x[k]) for k in ("A", "B", "E", "C"))
+    d_t = torch.bfloat16 if w.d == "bf16" else torch.float32
+    D = torch.empty((w.M, w.N2), dtype=d_t, device=dev)
+    plan = gemm.ChainPlan(w.M, w.N1, w.N2, w.K, w.ab, w.d)
+    info = plan.info
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        plan.run(A, B, E, C, D, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    if plan.last_status() != gemm.GEMM_OK:
+        raise RuntimeError("kernel reported a timeout during warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(smi_index(local_rank)) as clocks:
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    if plan.last_status() != gemm.GEMM_OK:
+        raise RuntimeError("kernel reported a timeout in the timed region")
+    local_ms = t0.elapsed_time(t1) / args.steps
+    kernel_ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
+    max_ms, flops_per_s = aggregate(local_ms, w.flops, world)
+
+    e2e = None
+    if not args.no_e2e:
+        h = {k: torch.from_numpy(x[k].view(np.int16) if x[k].dtype == np.uint16 else x[k]).pin_memory()
+             for k in ("A", "B", "E", "C")}
+        hD = torch.empty((w.M, w.N2), dtype=d_t).pin_memory()
+        e_steps = max(3, min(args.steps, args.e2e_steps))
+        for _ in range(2):
+            plan.run_host(h["A"], h["B"], h["E"], h["C"], hD, stream)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e_steps):
+            plan.run_host(h["A"], h["B"], h["E"], h["C"], hD, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        _, e2e_flops = aggregate(e0.elapsed_time(e1) / e_steps, w.flops, world)
+        h2d = sum(x[k].nbytes for k in ("A", "B", "E", "C"))
+        e2e = {"value": round(e2e_flops / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(hD.numel() * hD.element_size()), "steps": e_steps}
+
+    # roofline: the bound is whichever of HBM bytes and tensor FLOPs takes longer at the measured peaks
+    peaks, source = load_peaks()
+    alg_bytes = int(sum(x[k].nbytes for k in ("A", "B", "E", "C")) + w.M * w.N2 * (2 if w.d == "bf16" else 4))
+    t_hbm = alg_bytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = w.flops / (peaks["bf16_tflops"] * 1e12)
+    traffic, traffic_src = (args.traffic, "--traffic") if args.traffic is not None else measured_traffic(w.name)
+    if t_hbm >= t_tc:
+        achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(achieved / peaks["hbm_gbs"], 4),
+                    "peak_source": f"{source} HBM copy bandwidth"}
+    else:
+        achieved = w.flops / (kernel_ms / 1e3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_tflops"],
+                    "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                    "peak_source": f"{source} bf16 burst (cuBLAS bf16 8192^3)"}
+    roofline.update({"traffic": traffic, "traffic_source": traffic_src, "algorithmic_bytes": alg_bytes,
+                     "tensor_tflops": round(w.flops / (kernel_ms / 1e3) / 1e12, 2),
+                     "frac_of_tensor_peak": round(w.flops / (kernel_ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
+                     "kernel": "chain_kernel", "kernel_ms": round(kernel_ms, 5)})
+    out = {
+        "metric": "GEMM TFLOP/s and % of GB300 dense tensor peak (bf16 8192^3), vs CPU oracle",
+        "value": round(flops_per_s / 1e12, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(max_ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.ab,
+        "data": "synthetic (seeded splitmix64; recipe of the workload)",
+        "config": {"workload": w.name, "M": w.M, "K": w.K, "N1": w.N1, "N2": w.N2, "ab": w.ab, "c": "fp32",
+                   "d": w.d, "tile": [128, info["tile_n"], info["tile_k"]], "stages": info["stages"],
+                   "grid": info["grid"], "replicas": world,
+                   "l2": "no flush: inputs (A alone) larger than the 129 MB L2"},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": args.steps * info["launches_per_run"],
+        "clocks": clocks.summary(),
+    }
+    plan.close()
+    if rank == 0 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline_chain(w, x, args.cpu_seconds)
+    return out
+
+
+def cpu_baseline_chain(w, x, seconds: float):
+    """The oracle's chain on a bounded number of rows of the same workload."""
+    import numpy as np
+
+    import oracle
+    probe = 64
+    t = time.perf_counter()
+    oracle.chain(x["A"], x["B"], x["E"], x["C"], w.M, w.N1, w.N2, w.K, w.ab, rows=np.arange(probe))
+    per_row = max((time.perf_counter() - t) / probe, 1e-6)
+    R = int(max(1, min(w.M, seconds / per_row)))
+    t = time.perf_counter()
+    oracle.chain(x["A"], x["B"], x["E"], x["C"], w.M, w.N1, w.N2, w.K, w.ab, rows=np.arange(R))
+    dt = time.perf_counter() - t
+    return {"value": round(2.0 * R * w.N1 * (w.K + w.N2) / dt / 1e12, 6), "unit": "TFLOP/s",
+            "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"rows 0..{R - 1} of {w.name} (both products, fp64, incl. operand decode), {dt:.1f} s"}
+
+
 def cpu_baseline(w, x, seconds: float):
     """The oracle's triple loop on a row slab of the same workload (bounded CPU time)."""
     import oracle
@@ -368,6 +510,8 @@ def run_reference(args, rank, world):
     from blackwell_tensor_core_tma_gb300 import synth
 
     w = workload(args)
+    if isinstance(w, synth.ChainWorkload):
+        return run_reference_chain(args, w, world)
     x = synth.make_inputs(w)
     rng = np.random.default_rng(0)
     total_budget = args.reference_seconds
@@ -407,6 +551,45 @@ def run_reference(args, rank, world):
     }
 
 
+def run_reference_chain(args, w, world):
+    """The oracle's chain on random rows of the workload (each row: both products, fp64)."""
+    import numpy as np
+
+    import oracle
+    from blackwell_tensor_core_tma_gb300 import synth
+    x = synth.make_chain_inputs(w)
+    rng = np.random.default_rng(0)
+    per_step = args.reference_seconds / (args.steps + args.warmup)
+
+    def sample(n):
+        t = time.perf_counter()
+        oracle.chain(x["A"], x["B"], x["E"], x["C"], w.M, w.N1, w.N2, w.K, w.ab, rows=rng.integers(0, w.M, n))
+        return time.perf_counter() - t
+
+    rate = 8 / max(sample(8), 1e-6)                  # rows per second
+    n = int(max(1, rate * per_step))
+    for _ in range(args.warmup):
+        sample(n)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        sample(n)
+    dt = (time.perf_counter() - t) / args.steps
+    value = 2.0 * n * w.N1 * (w.K + w.N2) / dt / 1e12
+    desc = f"{n} random rows of {w.name} per step (both products in fp64)"
+    return {
+        "impl": "reference",
+        "metric": "GEMM TFLOP/s and % of GB300 dense tensor peak (bf16 8192^3), vs CPU oracle",
+        "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded splitmix64)",
+        "config": {"workload": w.name, "M": w.M, "K": w.K, "N1": w.N1, "N2": w.N2, "ab": w.ab, "d": w.d},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
 def main(argv=None):
     from blackwell_tensor_core_tma_gb300 import synth
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
@@ -414,8 +597,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--shape", default=None, help="MxNxK: the workload's recipe at other sizes (profiling)")
+    ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS) + sorted(synth.CHAIN_WORKLOADS))
+    ap.add_argument("--shape", default=None, help="MxNxK (chain workloads: MxN1xN2xK): the workload's recipe at "
+                                                  "other sizes (profiling)")
     ap.add_argument("--cta-group", type=int, choices=[0, 1, 2], default=0,
                     help="force single CTAs (1) or CTA pairs (2); 0 = the plan's choice")
     ap.add_argument("--a-col-major", action="store_true", help="store A column-major (M contiguous)")
@@ -442,7 +626,8 @@ def main(argv=None):
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
     try:
-        out = run_ours(args, rank, world, local_rank)
+        runner = run_ours_chain if args.workload in synth.CHAIN_WORKLOADS else run_ours
+        out = runner(args, rank, world, local_rank)
         if rank == 0:
             print(json.dumps(out), flush=True)
     finally:
