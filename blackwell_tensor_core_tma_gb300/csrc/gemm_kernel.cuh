@@ -22,6 +22,9 @@
 //               block scaling it first moves the stage's scales SMEM -> TMEM
 //               with tcgen05.cp (same page: SFA, SFB: GMEM --TMA--> SMEM
 //               --tcgen05.cp--> TMEM --tcgen05.mma-->).
+//   warp 2+EPI  (block-scaled instances with COPIER) issues the stage's scale copies
+//               SMEM -> TMEM ahead of the MMA issuer and signals them on sfull[s], so
+//               that copies and MMAs come from two threads.
 //   warps 2..5  epilogue warpgroup: warp w reads TMEM lanes 32*(w%4)..+31
 //               ("Tensor Memory（TMEM）": each warp of a warpgroup reaches its
 //               own 32-lane window) with tcgen05.ld + tcgen05.wait::ld, adds C
@@ -52,7 +55,10 @@ namespace gb300 {
 //             for scale slots at N = 256)
 //   EPI_WARPS epilogue warps: 4 (one per TMEM lane window) or 8 (two per window,
 //             each taking half of the tile's columns)
-template <int CG_, bool OUT_BF16_, int KIND_, int BN_, int STAGES_, int ACC_BUFS_ = 2, int EPI_WARPS_ = 4>
+//   COPIER  block-scaled: a warp of its own issues the scale-factor copies (the
+//           MMA thread then issues MMAs only)
+template <int CG_, bool OUT_BF16_, int KIND_, int BN_, int STAGES_, int ACC_BUFS_ = 2, int EPI_WARPS_ = 4,
+          bool COPIER_ = false>
 struct TileCfg {
     static constexpr int CG = CG_;
     static constexpr bool OUT_BF16 = OUT_BF16_;
@@ -62,7 +68,9 @@ struct TileCfg {
     static constexpr int STAGES = STAGES_;
     static constexpr int ACC_BUFS = ACC_BUFS_;
     static constexpr int EPI_WARPS = EPI_WARPS_;
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr bool COPIER = COPIER_ && KIND_ != KIND_F16;
+    static constexpr int COPY_WARP = 2 + EPI_WARPS;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS + (COPIER ? 32 : 0);
     static constexpr int WCOLS = BN * 4 / EPI_WARPS;             // columns one epilogue warp handles
     static constexpr int WCHUNKS = WCOLS / EPI_COLS;
     static_assert(ACC_BUFS == 1 || ACC_BUFS == 2, "accumulator buffers");
@@ -105,8 +113,9 @@ struct TileCfg {
     static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF;
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && OFF_B % 1024 == 0, "operand stages 1024-aligned");
     static_assert(OFF_EPI % 1024 == 0 && EPI_BUF % 1024 == 0, "epilogue staging 1024-aligned");
-    // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], cload[EPI_WARPS][2], drain
-    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 * EPI_WARPS + 1;
+    // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], cload[EPI_WARPS][2], drain,
+    // then with COPIER: sfull[STAGES] (the stage's scales are in TMEM), cdrain
+    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 * EPI_WARPS + 1 + (COPIER ? STAGES + 1 : 0);
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base slot, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
     // TMEM columns: accumulators [0, ACC_BUFS*BN), then one scale slot per stage: SFA
@@ -143,6 +152,16 @@ __device__ __forceinline__ void unit_coords(int u, const KParams &p, int &tm, in
     kb1 = (int)((int64_t)(s + 1) * p.num_kb / p.splits);
 }
 
+// K blocks of a unit walk forward in even persistent rounds and backward in odd ones
+// (round = how many units this CTA has taken before), so that a round starts on the
+// A and B slices the previous round read last, which are the likeliest still in L2.
+#ifndef GB300_SERPENTINE_K
+#define GB300_SERPENTINE_K 1
+#endif
+__device__ __forceinline__ int kb_at(int j, int kb0, int kb1, uint32_t round) {
+    return (GB300_SERPENTINE_K && (round & 1u)) ? kb1 - 1 - j : kb0 + j;
+}
+
 struct Waiter {
     volatile int *abort_flag;
     int *status;
@@ -174,6 +193,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// SMEM -> TMEM copies of stage s's scales, each 512-byte SMEM block (32 lanes x 16
+// bytes: one word of 128 rows) replicated to the 4 lane windows: SFA word w in columns
+// sfa_t + 4w.., SFB (word w, column group h) in sfb_t + 4(w*HALVES + h)..
+template <class Cfg>
+__device__ __forceinline__ void copy_scales(uint8_t *smem, int s, uint32_t sfa_t, uint32_t sfb_t) {
+    const uint32_t sf_src = smem_addr(smem + Cfg::OFF_SF + s * (Cfg::SFA_BYTES + Cfg::SFB_BYTES));
+#pragma unroll
+    for (int i = 0; i < Cfg::SF_WORDS; ++i)
+        tmem_cp_32x128b_warpx4<Cfg::CG>(sfa_t + 4 * i, smem_desc(sf_src + 512 * i, 512, 128, SWZ_NONE));
+#pragma unroll
+    for (int i = 0; i < Cfg::SF_WORDS * Cfg::HALVES; ++i)
+        tmem_cp_32x128b_warpx4<Cfg::CG>(sfb_t + 4 * i, smem_desc(sf_src + Cfg::SFA_BYTES + 512 * i, 512, 128, SWZ_NONE));
+}
+
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -198,6 +231,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint64_t *tempty = tfull + 2;
     uint64_t *cload = tempty + 2;
     uint64_t *drain = cload + 2 * Cfg::EPI_WARPS;
+    uint64_t *sfull = drain + 1;                          // COPIER only
+    uint64_t *cdrain = sfull + STAGES;                    // COPIER only
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 4);
     const Waiter W{abort_flag, p.status, p.timeout_ns};
@@ -221,6 +256,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         for (int i = 0; i < 2 * Cfg::EPI_WARPS; ++i) mbar_init(&cload[i], 1);
         mbar_init(drain, 1);
+        if constexpr (Cfg::COPIER) {
+            for (int i = 0; i < STAGES; ++i) mbar_init(&sfull[i], 1);
+            mbar_init(cdrain, 1);
+        }
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -242,14 +281,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step) {
+            uint32_t round = 0;
+            for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step, ++round) {
                 int tm, tn, kb0, kb1;
                 unit_coords(u, p, tm, tn, kb0, kb1);
                 const int m0 = tm * TILE_M * CG + (int)rank * TILE_M;
                 const int n0 = tn * BN + (int)rank * Cfg::B_ROWS;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int j = 0; j < kb1 - kb0; ++j) {
+                    const int kb = kb_at(j, kb0, kb1, round);
                     if (!W.wait(&empty[s], ph ^ 1u)) { ok = false; break; }
-                    const bool withhold = p.fault == 1 && u == tile0 && kb == kb0;
+                    const bool withhold = p.fault == 1 && u == tile0 && j == 0;
                     if (rank == 0 && !withhold) mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
                     const uint32_t a_dst = smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES);
                     const uint32_t b_dst = smem_addr(smem + Cfg::OFF_B + s * Cfg::B_BYTES);
@@ -305,25 +346,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (!W.wait(&tempty[b], aph ^ 1u)) { ok = false; break; }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * BN;
-                for (int kb = kb0; kb < kb1; ++kb) {
+                for (int j = 0; j < kb1 - kb0; ++j) {
                     if (!W.wait(&full[s], ph)) { ok = false; break; }
+                    if (Cfg::COPIER && !W.wait(&sfull[s], ph)) { ok = false; break; }
                     tc_fence_after_sync();
                     const uint64_t ad = smem_desc(smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES), a_lbo, 1024, SWZ_128B);
                     const uint64_t bd = smem_desc(smem_addr(smem + Cfg::OFF_B + s * Cfg::B_BYTES), b_lbo, 1024, SWZ_128B);
                     if constexpr (Cfg::SCALED) {
-                        // stage s's scales, each 512-byte SMEM block (32 lanes x 16 bytes: one
-                        // word of 128 rows) replicated to the 4 lane windows: SFA word w in
-                        // columns 4w..4w+3, SFB (word w, column group h) in 4(w*HALVES + h)..
+                        // stage s's scale slot (filled here, or by the copier warp before sfull[s])
                         const uint32_t sfa_t = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_SLOT;
                         const uint32_t sfb_t = sfa_t + 4 * Cfg::SF_WORDS;
-                        const uint32_t sf_src = smem_addr(smem + Cfg::OFF_SF + s * (Cfg::SFA_BYTES + Cfg::SFB_BYTES));
-#pragma unroll
-                        for (int i = 0; i < Cfg::SF_WORDS; ++i)
-                            tmem_cp_32x128b_warpx4<CG>(sfa_t + 4 * i, smem_desc(sf_src + 512 * i, 512, 128, SWZ_NONE));
-#pragma unroll
-                        for (int i = 0; i < Cfg::SF_WORDS * Cfg::HALVES; ++i)
-                            tmem_cp_32x128b_warpx4<CG>(sfb_t + 4 * i,
-                                                       smem_desc(sf_src + Cfg::SFA_BYTES + 512 * i, 512, 128, SWZ_NONE));
+                        if constexpr (!Cfg::COPIER) copy_scales<Cfg>(smem, s, sfa_t, sfb_t);
                         // MMA step k reads scales k*SF_PER_MMA.. of the stage: word w, from byte id
                         // (1X: byte k; 2X: half-word 0 or 2; 4X: the whole word, id 0)
 #pragma unroll
@@ -331,12 +364,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                             const uint32_t w = (uint32_t)(k * Cfg::SF_PER_MMA) / 4u, id = (uint32_t)(k * Cfg::SF_PER_MMA) % 4u;
                             mma_scaled<Cfg::KIND, CG>(d_tmem, ad + a_step * k, bd + b_step * k,
                                                       p.idesc | (id << 4) | (id << 29), sfa_t + 4 * w,
-                                                      sfb_t + 4 * Cfg::HALVES * w, (kb != kb0) | (k != 0));
+                                                      sfb_t + 4 * Cfg::HALVES * w, (j != 0) | (k != 0));
                         }
                     } else {
 #pragma unroll
                         for (int k = 0; k < Cfg::BK / Cfg::MMA_K; ++k)   // 32 bytes of K = 2 descriptor units
-                            mma_f16<CG>(d_tmem, ad + a_step * k, bd + b_step * k, p.idesc, (kb != kb0) | (k != 0));
+                            mma_f16<CG>(d_tmem, ad + a_step * k, bd + b_step * k, p.idesc, (j != 0) | (k != 0));
                     }
                     if constexpr (CG == 1) tc_commit<1>(smem_addr(&empty[s]));
                     else tc_commit_pair(smem_addr(&empty[s]), 0x3);
@@ -350,6 +383,34 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // after an abort: this wait is bounded by time only)
             tc_commit<CG>(smem_addr(drain));
             W.wait(drain, 0, false);
+        }
+    } else if (Cfg::COPIER && warp == Cfg::COPY_WARP) {
+        // ---------------------------------------------------------- scale copies
+        if constexpr (Cfg::COPIER) {
+            if (rank == 0 && lane == 0) {
+                // stage s's slot is rewritten only after full[s] of the next round, i.e. after
+                // the producer saw empty[s]: the MMAs that read the slot have completed
+                int s = 0;
+                uint32_t ph = 0;
+                bool ok = true;
+                for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step) {
+                    int tm, tn, kb0, kb1;
+                    unit_coords(u, p, tm, tn, kb0, kb1);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!W.wait(&full[s], ph)) { ok = false; break; }
+                        tc_fence_after_sync();
+                        const uint32_t sfa_t = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_SLOT;
+                        copy_scales<Cfg>(smem, s, sfa_t, sfa_t + 4 * Cfg::SF_WORDS);
+                        if constexpr (CG == 1) tc_commit<1>(smem_addr(&sfull[s]));
+                        else tc_commit_pair(smem_addr(&sfull[s]), 0x1);
+                        if (++s == STAGES) { s = 0; ph ^= 1u; }
+                    }
+                }
+                // every copy this thread issued has finished before teardown
+                if constexpr (CG == 1) tc_commit<1>(smem_addr(cdrain));
+                else tc_commit_pair(smem_addr(cdrain), 0x1);
+                W.wait(cdrain, 0, false);
+            }
         }
     } else {
         // ------------------------------------------------------------ epilogue

@@ -13,11 +13,13 @@ namespace {
 
 // single CTAs: 128 x 128 tiles, two accumulators, five stages, 4 epilogue warps.
 // CTA pairs: 256 x 256 tiles, one 256-column accumulator drained to registers by
-// 8 epilogue warps, four stages (the shared memory the scales leave).
+// 8 epilogue warps, four stages (the shared memory the scales leave), and a copier
+// warp that issues the scale copies so that they overlap the MMAs (measured on
+// 8192^3: +6 % with two scales per step, +19 % with four).
 template <bool OUT_BF16>
 using Cfg1 = TileCfg<1, OUT_BF16, KIND_NVF4, 128, 5, 2, 4>;
 template <bool OUT_BF16>
-using Cfg2 = TileCfg<2, OUT_BF16, KIND_NVF4, 256, 4, 1, 8>;
+using Cfg2 = TileCfg<2, OUT_BF16, KIND_NVF4, 256, 4, 1, 8, true>;
 using Family = ScaledInstances<Cfg1<false>, Cfg1<true>, Cfg2<false>, Cfg2<true>>;
 
 }  // namespace
