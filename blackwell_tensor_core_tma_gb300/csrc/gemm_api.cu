@@ -48,6 +48,12 @@ struct gemm_plan {
     int splits;               // K slices per tile (1 = no split-K)
     int capacity;             // work units the persistent grid runs at once (CTAs or CTA pairs)
     int split_request;        // 0 = choose automatically, n >= 1 = asked for
+    int sk_request;           // stream-K: 1 = where it balances the waves (default), 0 = never
+    int sk;                   // stream-K chosen
+    int sk_dp_tiles;          // stream-K: tiles the units take whole before their spans
+    float *ws_p;              // stream-K: partial-sum slots (units x CG x 128 rows x tile_n fp32)
+    int *sk_flags;            // stream-K: one flag per (slot, CTA of the group)
+    uint32_t epoch;           // stream-K: runs so far (the value a run's flags carry)
     int tile_n;
     int tile_k;               // K elements per stage
     int num_kb;
@@ -123,7 +129,7 @@ CUtensorMapDataType tma_dtype(gemm_dtype t) {
 gemm_status encode_maps(gemm_plan *p, const void *A, const void *B, const void *C, void *D) {
     if (p->maps_valid && A == p->lastA && B == p->lastB && C == p->lastC && D == p->lastD) return GEMM_OK;
     if (!encoder()) return GEMM_ERR_CUDA;
-    std::memset(p->maps, 0, 4 * sizeof(CUtensorMap));     // the scale-factor maps stay
+    std::memset(p->maps, 0, 4 * sizeof(CUtensorMap));     // the scale-factor and partial-sum maps stay
     // 4-bit operands are mapped as bytes (two K elements each, K-major only)
     const bool fp4 = p->ab == GEMM_E2M1;
     const int eb = fp4 ? 1 : elem_bits(p->ab) / 8;
@@ -243,7 +249,11 @@ gemm_status configure_scaled(gemm_plan *p) {
 // Split-K: when the output tiles cannot fill the GPU, cut each tile's K range into
 // slices that run as separate work units and add their partial products into D
 // (fp32 only: rounding every partial sum to bf16 would cost accuracy).
-void choose_splits(gemm_plan *p) {
+// Stream-K: when there are more tiles than units but not a whole number of waves, the
+// last one to two waves' worth of tiles is shared out as equal spans of k-blocks, so
+// that every unit finishes at about the same time (deterministic: every tile is summed
+// in a fixed order).
+gemm_status choose_splits(gemm_plan *p) {
     const int units = p->capacity;
     int s = 1;
     if (p->split_request >= 1) {
@@ -259,6 +269,37 @@ void choose_splits(gemm_plan *p) {
     // more work units than tiles: the persistent grid may grow up to the machine
     const int work = p->tiles * s;
     p->grid = p->cta_group * (work < units ? work : units);
+    // measured on GB300: worth it with long tiles (>= 64 k-blocks: the cut pieces' extra
+    // epilogue work stays small) and few waves (below 8 the idle part of the last wave is
+    // a large share; above, the power the idle SMs leave lets the busy ones clock higher)
+    p->sk = s == 1 && p->sk_request && p->tiles >= units && p->tiles % units != 0 && p->num_kb >= 64 &&
+            p->tiles < 8 * units;
+    if (p->sk) {
+        p->sk_dp_tiles = (p->tiles / units - 1) * units;
+        p->grid = p->cta_group * units;
+        // flags always; the partial-sum workspace only for bf16 D (fp32 partial sums go into D)
+        if (!p->sk_flags) {
+            const size_t ws = (size_t)units * p->cta_group * TILE_M * p->tile_n * sizeof(float);
+            const size_t fl = (size_t)units * p->cta_group * sizeof(int);
+            const bool need_ws = p->d == GEMM_BF16;
+            if ((need_ws && cudaMalloc(&p->ws_p, ws) != cudaSuccess) || cudaMalloc(&p->sk_flags, fl) != cudaSuccess ||
+                cudaMemset(p->sk_flags, 0, fl) != cudaSuccess) {
+                cudaFree(p->ws_p);
+                cudaFree(p->sk_flags);
+                p->ws_p = nullptr;
+                p->sk_flags = nullptr;
+                p->sk = 0;
+                return GEMM_ERR_CUDA;
+            }
+            if (need_ws && (!encoder() || !encode_2d(&p->maps[6], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->ws_p,
+                                                     p->tile_n, (uint64_t)units * p->cta_group * TILE_M, EPI_COLS,
+                                                     32, CU_TENSOR_MAP_SWIZZLE_128B))) {
+                p->sk = 0;
+                return GEMM_ERR_CUDA;
+            }
+        }
+    }
+    return GEMM_OK;
 }
 
 }  // namespace
@@ -337,8 +378,12 @@ gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K, 
         delete p;
         return st;
     }
-    choose_splits(p);
-    if (cudaMalloc(&p->status, sizeof(int)) != cudaSuccess) {
+    p->sk_request = 1;
+    if (choose_splits(p) != GEMM_OK || cudaMalloc(&p->status, sizeof(int)) != cudaSuccess) {
+        cudaFree(p->ws_a);
+        cudaFree(p->ws_b);
+        cudaFree(p->ws_p);
+        cudaFree(p->sk_flags);
         delete p;
         return GEMM_ERR_CUDA;
     }
@@ -382,6 +427,15 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
     kp.status = p->status;
     kp.timeout_ns = p->timeout_ns;
     kp.fault = p->fault;
+    if (p->sk) {
+        kp.sk = 1;
+        kp.sk_dp_tiles = p->sk_dp_tiles;
+        kp.sk_units = p->grid / p->cta_group;
+        kp.epoch = (int)(++p->epoch & 0x7FFFFFFF);
+        if (kp.epoch == 0) kp.epoch = p->epoch = 1;
+        kp.sk_flags = p->sk_flags;
+        kp.sk_ws = p->ws_p;
+    }
     LaunchShape shape{p->grid, p->cta_group, p->smem};
     if (p->family != KIND_F16) {
         const uint32_t tm = (uint32_t)(TILE_M * p->cta_group), tn = (uint32_t)p->tile_n;
@@ -471,6 +525,7 @@ gemm_status gemm_plan_get_info(gemm_plan_t p, gemm_plan_info *info) {
     const bool scaled = p->family != KIND_F16 && p->family != FAMILY_CHAIN;
     info->launches_per_run = (scaled ? 2 : 1) + (p->splits > 1 ? 1 : 0);
     info->splits = p->splits;
+    info->stream_k = p->sk;
     info->sm_count = p->sm_count;
     return GEMM_OK;
 }
@@ -486,8 +541,14 @@ gemm_status gemm_plan_set_split_k(gemm_plan_t p, int splits) {
     if (p->family == FAMILY_CHAIN) return splits > 1 ? GEMM_ERR_UNSUPPORTED : GEMM_OK;
     if (splits > 1 && (p->d != GEMM_F32 || (p->flags & GEMM_FLAG_DETERMINISTIC))) return GEMM_ERR_UNSUPPORTED;
     p->split_request = splits;
-    choose_splits(p);
-    return GEMM_OK;
+    return choose_splits(p);
+}
+
+gemm_status gemm_plan_set_stream_k(gemm_plan_t p, int enable) {
+    if (!p || enable < 0 || enable > 1) return GEMM_ERR_INVALID_ARG;
+    if (p->family == FAMILY_CHAIN) return GEMM_OK;
+    p->sk_request = enable;
+    return choose_splits(p);
 }
 
 gemm_status gemm_plan_destroy(gemm_plan_t p) {
@@ -502,6 +563,8 @@ gemm_status gemm_plan_destroy(gemm_plan_t p) {
     cudaFree(p->hE);
     cudaFree(p->ws_a);
     cudaFree(p->ws_b);
+    cudaFree(p->ws_p);
+    cudaFree(p->sk_flags);
     delete p;
     return GEMM_OK;
 }

@@ -114,8 +114,8 @@ struct TileCfg {
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && OFF_B % 1024 == 0, "operand stages 1024-aligned");
     static_assert(OFF_EPI % 1024 == 0 && EPI_BUF % 1024 == 0, "epilogue staging 1024-aligned");
     // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], cload[EPI_WARPS][2], drain,
-    // then with COPIER: sfull[STAGES] (the stage's scales are in TMEM), cdrain
-    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 * EPI_WARPS + 1 + (COPIER ? STAGES + 1 : 0);
+    // epi_sync, then with COPIER: sfull[STAGES] (the stage's scales are in TMEM), cdrain
+    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 * EPI_WARPS + 2 + (COPIER ? STAGES + 1 : 0);
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base slot, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
     // TMEM columns: accumulators [0, ACC_BUFS*BN), then one scale slot per stage: SFA
@@ -162,6 +162,65 @@ __device__ __forceinline__ int kb_at(int j, int kb0, int kb1, uint32_t round) {
     return (GB300_SERPENTINE_K && (round & 1u)) ? kb1 - 1 - j : kb0 + j;
 }
 
+// A piece of work: K blocks [kb0, kb1) of tile (tm, tn).  ROLE_TILE pieces cover a
+// whole tile (or, with split-K, one slice); stream-K pieces that cover only part of a
+// tile are ROLE_EARLY (ends the tile, starts a span: stores a partial sum in workspace
+// slot `slot`) or ROLE_FINAL (starts the tile, ends a span: adds that partial).
+enum : int { ROLE_TILE = 0, ROLE_EARLY = 1, ROLE_FINAL = 2 };
+struct Work {
+    int tm, tn, kb0, kb1, role, slot;
+};
+
+// The pieces one unit (CTA or CTA pair) processes, in order; every role of the kernel
+// walks the same sequence.  Without stream-K: units tile0, tile0 + step, ... of the
+// (tile x split) list.  With stream-K: first the whole tiles tile0, tile0 + step, ...
+// below sk_dp_tiles, then the unit's span of the remaining tiles' k-blocks.
+struct WorkIter {
+    int unit, step, u;
+    int64_t g, g_end;
+    __device__ __forceinline__ WorkIter(const KParams &p, int unit0, int step0) : unit(unit0), step(step0), u(unit0) {
+        g = g_end = 0;
+        if (p.sk) {
+            const int64_t base = (int64_t)p.sk_dp_tiles * p.num_kb;
+            const int64_t total = (int64_t)(p.num_tiles - p.sk_dp_tiles) * p.num_kb;
+            g = base + (int64_t)unit0 * total / p.sk_units;
+            g_end = base + (int64_t)(unit0 + 1) * total / p.sk_units;
+        }
+    }
+    __device__ __forceinline__ bool next(const KParams &p, Work &w) {
+        if (!p.sk) {
+            if (u >= p.num_tiles * p.splits) return false;
+            unit_coords(u, p, w.tm, w.tn, w.kb0, w.kb1);
+            w.role = ROLE_TILE;
+            w.slot = 0;
+            u += step;
+            return true;
+        }
+        if (u < p.sk_dp_tiles) {
+            tile_coords(u, p.tiles_m, p.group_m, w.tm, w.tn, p.tiles_n);
+            w.kb0 = 0;
+            w.kb1 = p.num_kb;
+            w.role = ROLE_TILE;
+            w.slot = 0;
+            u += step;
+            return true;
+        }
+        if (g >= g_end) return false;
+        const int t = (int)(g / p.num_kb);
+        const int k0 = (int)(g - (int64_t)t * p.num_kb);
+        const int k1 = (int)min((int64_t)p.num_kb, (int64_t)k0 + (g_end - g));
+        tile_coords(t, p.tiles_m, p.group_m, w.tm, w.tn, p.tiles_n);
+        w.kb0 = k0;
+        w.kb1 = k1;
+        // a span is at least one tile long, so only its first piece can start inside a tile
+        // (the next span's boundary: this unit's slot) and only its last can end inside one
+        w.role = (k0 == 0 && k1 == p.num_kb) ? ROLE_TILE : (k0 > 0 ? ROLE_EARLY : ROLE_FINAL);
+        w.slot = k0 > 0 ? unit : unit + 1;
+        g += k1 - k0;
+        return true;
+    }
+};
+
 struct Waiter {
     volatile int *abort_flag;
     int *status;
@@ -177,6 +236,24 @@ struct Waiter {
             if (mbar_try_wait(a, parity)) return true;
             if ((it & 15) == 0) {
                 if (honor_abort && *abort_flag) return false;
+                if (globaltimer_ns() - t0 > timeout_ns) {
+                    *abort_flag = 1;
+                    atomicExch(status, (int)GEMM_ERR_TIMEOUT);
+                    return false;
+                }
+            }
+        }
+    }
+
+    // wait until the global flag *f holds v (acquire); false if the kernel is giving up
+    __device__ __forceinline__ bool wait_flag(const int *f, int v) const {
+        if (ld_acquire_gpu(f) == v) return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t it = 1;; ++it) {
+            __nanosleep(64);
+            if (ld_acquire_gpu(f) == v) return true;
+            if ((it & 15) == 0) {
+                if (*abort_flag) return false;
                 if (globaltimer_ns() - t0 > timeout_ns) {
                     *abort_flag = 1;
                     atomicExch(status, (int)GEMM_ERR_TIMEOUT);
@@ -212,7 +289,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                    const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                   const KParams p) {
+                   const __grid_constant__ CUtensorMap tmP, const KParams p) {
     constexpr int CG = Cfg::CG;
     constexpr int STAGES = Cfg::STAGES;
     constexpr int BN = Cfg::BN;
@@ -231,7 +308,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint64_t *tempty = tfull + 2;
     uint64_t *cload = tempty + 2;
     uint64_t *drain = cload + 2 * Cfg::EPI_WARPS;
-    uint64_t *sfull = drain + 1;                          // COPIER only
+    uint64_t *epi_sync = drain + 1;                       // every epilogue warp stored its part of a partial sum
+    uint64_t *sfull = epi_sync + 1;                       // COPIER only
     uint64_t *cdrain = sfull + STAGES;                    // COPIER only
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 4);
@@ -242,6 +320,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         prefetch_tensormap(&tmB);
         if (p.has_c) prefetch_tensormap(&tmC);
         prefetch_tensormap(&tmD);
+        if (Cfg::OUT_BF16 && p.sk) prefetch_tensormap(&tmP);   // the partial-sum map exists for bf16 D only
         if constexpr (Cfg::SCALED) {
             prefetch_tensormap(&tmSFA);
             prefetch_tensormap(&tmSFB);
@@ -256,6 +335,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
         for (int i = 0; i < 2 * Cfg::EPI_WARPS; ++i) mbar_init(&cload[i], 1);
         mbar_init(drain, 1);
+        mbar_init(epi_sync, Cfg::EPI_WARPS);
         if constexpr (Cfg::COPIER) {
             for (int i = 0; i < STAGES; ++i) mbar_init(&sfull[i], 1);
             mbar_init(cdrain, 1);
@@ -282,15 +362,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             uint32_t ph = 0;
             bool ok = true;
             uint32_t round = 0;
-            for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step, ++round) {
-                int tm, tn, kb0, kb1;
-                unit_coords(u, p, tm, tn, kb0, kb1);
+            WorkIter it(p, tile0, tile_step);
+            Work wk;
+            for (; ok && it.next(p, wk); ++round) {
+                const int tm = wk.tm, tn = wk.tn, kb0 = wk.kb0, kb1 = wk.kb1;
                 const int m0 = tm * TILE_M * CG + (int)rank * TILE_M;
                 const int n0 = tn * BN + (int)rank * Cfg::B_ROWS;
                 for (int j = 0; j < kb1 - kb0; ++j) {
                     const int kb = kb_at(j, kb0, kb1, round);
                     if (!W.wait(&empty[s], ph ^ 1u)) { ok = false; break; }
-                    const bool withhold = p.fault == 1 && u == tile0 && j == 0;
+                    const bool withhold = p.fault == 1 && round == 0 && j == 0;
                     if (rank == 0 && !withhold) mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
                     const uint32_t a_dst = smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES);
                     const uint32_t b_dst = smem_addr(smem + Cfg::OFF_B + s * Cfg::B_BYTES);
@@ -338,9 +419,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int s = 0;
             uint32_t ph = 0, acc_it = 0;
             bool ok = true;
-            for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step, ++acc_it) {
-                int tm, tn, kb0, kb1;
-                unit_coords(u, p, tm, tn, kb0, kb1);
+            WorkIter it(p, tile0, tile_step);
+            Work wk;
+            for (; ok && it.next(p, wk); ++acc_it) {
+                const int kb0 = wk.kb0, kb1 = wk.kb1;
                 const uint32_t b = Cfg::ACC_BUFS == 2 ? (acc_it & 1u) : 0u;
                 const uint32_t aph = Cfg::ACC_BUFS == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
                 if (!W.wait(&tempty[b], aph ^ 1u)) { ok = false; break; }
@@ -393,10 +475,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 int s = 0;
                 uint32_t ph = 0;
                 bool ok = true;
-                for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step) {
-                    int tm, tn, kb0, kb1;
-                    unit_coords(u, p, tm, tn, kb0, kb1);
-                    for (int kb = kb0; kb < kb1; ++kb) {
+                WorkIter it(p, tile0, tile_step);
+                Work wk;
+                while (ok && it.next(p, wk)) {
+                    for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
                         if (!W.wait(&full[s], ph)) { ok = false; break; }
                         tc_fence_after_sync();
                         const uint32_t sfa_t = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_SLOT;
@@ -421,70 +503,114 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         uint64_t *cb = cload + 2 * e;
         // C is read once and D written once: let them leave L2 before the operand tiles
         const uint64_t stream_pol = l2_policy_evict_first();
-        // ec counts the 32 x 32 boxes this warp has stored; box ec uses staging
-        // buffer ec % 2, and its C load is that buffer's (ec / 2)-th
-        uint32_t acc_it = 0, ec = 0;
+        // ec counts the 32 x 32 boxes this warp has stored (box ec is staged in buffer ec % 2);
+        // lc[i] counts the loads issued into buffer i (the phases of cb[i]); n_early counts the
+        // stream-K partial sums this CTA has published (the phases of epi_sync)
+        uint32_t acc_it = 0, ec = 0, n_early = 0;
+        uint32_t lc0 = 0, lc1 = 0;                    // the lc[i] of the comment, kept in registers
         bool ok = true;
-        for (int u = tile0; ok && u < p.num_tiles * p.splits; u += tile_step, ++acc_it) {
-            int tm, tn, kb0, kb1;
-            unit_coords(u, p, tm, tn, kb0, kb1);
+        // a TMA load of one 32 x 32 fp32 box into staging buffer i (issued by lane 0, counted by all)
+        auto issue = [&](uint32_t i, const CUtensorMap *m, int c0, int c1) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&cb[i], Cfg::EPI_BUF);
+                tma_load_2d_hint(smem_addr(ebuf + i * Cfg::EPI_BUF), m, smem_addr(&cb[i]), c0, c1, stream_pol);
+            }
+            if (i) ++lc1; else ++lc0;
+        };
+        auto landed = [&](uint32_t i) -> bool {
+            return __all_sync(0xffffffffu, W.wait(&cb[i], ((i ? lc1 : lc0) - 1u) & 1u));
+        };
+        // add the fp32 box in staging buffer i (row `lane`, 128-byte swizzle: 16-byte chunk c at c ^ (row % 8))
+        auto add_box = [&](uint32_t i, float (&v)[32]) {
+            const uint8_t *bb = ebuf + i * Cfg::EPI_BUF;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 cv = *reinterpret_cast<const float4 *>(bb + lane * 128 + ((c ^ (lane & 7)) << 4));
+                v[4 * c + 0] += cv.x;
+                v[4 * c + 1] += cv.y;
+                v[4 * c + 2] += cv.z;
+                v[4 * c + 3] += cv.w;
+            }
+        };
+        // hand accumulator bb back to the MMA (all 32 lanes have read it)
+        auto release = [&](uint32_t bb) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (CG == 1) mbar_arrive(&tempty[bb]);
+                else mbar_arrive_remote(mapa_shared(smem_addr(&tempty[bb]), 0));
+            }
+        };
+        WorkIter it(p, tile0, tile_step);
+        Work wk;
+        for (; ok && it.next(p, wk); ++acc_it) {
             const uint32_t b = Cfg::ACC_BUFS == 2 ? (acc_it & 1u) : 0u;
             const uint32_t aph = Cfg::ACC_BUFS == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
-            const int m_warp = tm * TILE_M * CG + (int)rank * TILE_M + 32 * q;
-            const int n_warp = tn * BN + h * Cfg::WCOLS;
+            const int m_warp = wk.tm * TILE_M * CG + (int)rank * TILE_M + 32 * q;
+            const int n_warp = wk.tn * BN + h * Cfg::WCOLS;
+            // this warp's rows and columns of a stream-K partial sum in the workspace
+            const int ws_row = (wk.slot * CG + (int)rank) * TILE_M + 32 * q;
+            const int ws_col = h * Cfg::WCOLS;
             // 32 x 32 boxes that lie wholly outside D are neither loaded nor stored
             const int chunks_in = m_warp < p.M ? max(0, min(Cfg::WCHUNKS, (p.N - n_warp + EPI_COLS - 1) / EPI_COLS)) : 0;
-            const bool use_c = p.has_c && chunks_in > 0;
-            if (use_c && lane == 0) {      // the tile's first C box loads while its accumulator is computed
-                bulk_wait_group_read0();
-                mbar_arrive_expect_tx(&cb[ec & 1u], Cfg::EPI_BUF);
-                tma_load_2d_hint(smem_addr(ebuf + (ec & 1u) * Cfg::EPI_BUF), &tmC, smem_addr(&cb[ec & 1u]), n_warp,
-                                 m_warp, stream_pol);
+            // every piece but a partial sum (ROLE_EARLY) adds C, loaded box by box
+            const bool use_c = wk.role != ROLE_EARLY && p.has_c && chunks_in > 0;
+            if (use_c) {                   // the piece's first C box loads while its accumulator is computed
+                if (lane == 0) bulk_wait_group_read0();
+                issue(ec & 1u, &tmC, n_warp, m_warp);
             }
             if (!__all_sync(0xffffffffu, W.wait(&tfull[b], aph))) break;
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + b * BN + h * Cfg::WCOLS;
 
-            auto release_accumulator = [&]() {
-                // the accumulator is free once all 32 lanes have read it
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) {
-                    if constexpr (CG == 1) mbar_arrive(&tempty[b]);
-                    else mbar_arrive_remote(mapa_shared(smem_addr(&tempty[b]), 0));
-                }
+            auto release_accumulator = [&]() { release(b); };
+            // a stream-K piece that starts its tile waits for its tile's other piece to have
+            // published (the flag carries this run's epoch): with fp32 D that piece has stored
+            // its partial sum into D and this one adds into it; with bf16 D the partial sum is
+            // in the workspace and this one reads it
+            auto await_partial = [&]() -> bool {
+                if (wk.role != ROLE_FINAL) return true;
+                const bool got = W.wait_flag(p.sk_flags + wk.slot * CG + (int)rank, p.epoch);
+                if (got && lane == 0) fence_proxy_async_global();   // the flag before TMA traffic to D
+                return __all_sync(0xffffffffu, got);
             };
-            // one 32 x 32 box: add C, convert, stage in shared memory, TMA-store
+            // one 32 x 32 box: add C (and a partial sum), convert, stage in shared memory, then
+            // TMA-store it to D (reduce-add for split-K slices and for fp32 stream-K finals), or
+            // a partial sum to D (fp32) or the workspace (bf16 D)
             auto store_box = [&](int j, const uint32_t (&acc)[32]) -> bool {
                 const uint32_t cur = ec & 1u;
                 uint8_t *buf = ebuf + cur * Cfg::EPI_BUF;
-                if (use_c && j + 1 < chunks_in && lane == 0) {
-                    const uint32_t nx = cur ^ 1u;
-                    bulk_wait_group_read0();              // the store from buffer nx has read it
-                    mbar_arrive_expect_tx(&cb[nx], Cfg::EPI_BUF);
-                    tma_load_2d_hint(smem_addr(ebuf + nx * Cfg::EPI_BUF), &tmC, smem_addr(&cb[nx]),
-                                     n_warp + EPI_COLS * (j + 1), m_warp, stream_pol);
+                if (use_c && j + 1 < chunks_in) {
+                    if (lane == 0) bulk_wait_group_read0();   // the store from the other buffer has read it
+                    issue(cur ^ 1u, &tmC, n_warp + EPI_COLS * (j + 1), m_warp);
                 }
                 if (j >= chunks_in) return true;
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
-                if (use_c) {
-                    if (!__all_sync(0xffffffffu, W.wait(&cb[cur], (ec >> 1) & 1u))) return false;
-                    // row `lane` of the 128-byte-swizzled fp32 box: 16-byte chunk c at (c ^ (row % 8))
+                if constexpr (Cfg::OUT_BF16) {
+                    if (wk.role == ROLE_FINAL) {
+                        // row `lane` of this box of the partial sum (row-major fp32 workspace, L2)
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            p.sk_ws + (size_t)(ws_row + lane) * BN + ws_col + EPI_COLS * j);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float4 cv = *reinterpret_cast<const float4 *>(buf + lane * 128 + ((c ^ (lane & 7)) << 4));
-                        v[4 * c + 0] += cv.x;
-                        v[4 * c + 1] += cv.y;
-                        v[4 * c + 2] += cv.z;
-                        v[4 * c + 3] += cv.w;
+                        for (int c = 0; c < 8; ++c) {
+                            const float4 pv = __ldcg(src + c);
+                            v[4 * c + 0] += pv.x;
+                            v[4 * c + 1] += pv.y;
+                            v[4 * c + 2] += pv.z;
+                            v[4 * c + 3] += pv.w;
+                        }
                     }
+                }
+                if (use_c) {
+                    if (!landed(cur)) return false;
+                    add_box(cur, v);
                 } else if (lane == 0) {
-                    bulk_wait_group_read1();              // the store two boxes back has read this buffer
+                    bulk_wait_group_read1();                  // the store two boxes back has read this buffer
                 }
                 __syncwarp();
-                if constexpr (Cfg::OUT_BF16) {
+                if (Cfg::OUT_BF16 && wk.role != ROLE_EARLY) {
                     // 64-byte rows, 64-byte swizzle: chunk c at (c ^ ((row / 2) % 4))
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -504,8 +630,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    if (p.splits > 1) tma_reduce_add_2d(&tmD, smem_addr(buf), n_warp + EPI_COLS * j, m_warp);
-                    else tma_store_2d_hint(&tmD, smem_addr(buf), n_warp + EPI_COLS * j, m_warp, stream_pol);
+                    const int dx = n_warp + EPI_COLS * j;
+                    if (wk.role == ROLE_EARLY) {
+                        if (Cfg::OUT_BF16) tma_store_2d(&tmP, smem_addr(buf), ws_col + EPI_COLS * j, ws_row);
+                        else tma_store_2d(&tmD, smem_addr(buf), dx, m_warp);
+                    } else if (p.splits > 1 || (wk.role == ROLE_FINAL && !Cfg::OUT_BF16)) {
+                        tma_reduce_add_2d(&tmD, smem_addr(buf), dx, m_warp);
+                    } else {
+                        tma_store_2d_hint(&tmD, smem_addr(buf), dx, m_warp, stream_pol);
+                    }
                     bulk_commit_group();
                 }
                 ++ec;
@@ -522,10 +655,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < Cfg::WCHUNKS; ++j) tie_registers(acc[j]);
                 release_accumulator();
+                if (!await_partial()) { ok = false; break; }
 #pragma unroll
                 for (int j = 0; j < Cfg::WCHUNKS; ++j)
                     if (ok) ok = store_box(j, acc[j]);
             } else {
+                if (!await_partial()) { ok = false; break; }
                 for (int j = 0; j < Cfg::WCHUNKS && ok; ++j) {
                     uint32_t acc[32];
                     tmem_ld_32x32b_x32(taddr + EPI_COLS * j, acc);
@@ -533,6 +668,22 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     if (j == Cfg::WCHUNKS - 1) release_accumulator();
                     ok = store_box(j, acc);
                 }
+            }
+            if (ok && wk.role == ROLE_EARLY) {
+                // publish the partial sum once every epilogue warp's stores have completed
+                if (lane == 0) {
+                    bulk_wait_group0();
+                    fence_proxy_async_global();
+                    mbar_arrive(epi_sync);
+                }
+                if (e == 0) {
+                    ok = __all_sync(0xffffffffu, W.wait(epi_sync, n_early & 1u));
+                    if (ok && lane == 0) {
+                        __threadfence();
+                        st_release_gpu(p.sk_flags + wk.slot * CG + (int)rank, p.epoch);
+                    }
+                }
+                ++n_early;
             }
         }
         if (lane == 0) bulk_wait_group0();
@@ -568,8 +719,8 @@ cudaError_t launch_tc(const LaunchShape &shape, const CUtensorMap *maps, const K
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    void *args[7] = {(void *)&maps[0], (void *)&maps[1], (void *)&maps[2], (void *)&maps[3],
-                     (void *)&maps[4], (void *)&maps[5], (void *)&p};
+    void *args[8] = {(void *)&maps[0], (void *)&maps[1], (void *)&maps[2], (void *)&maps[3],
+                     (void *)&maps[4], (void *)&maps[5], (void *)&maps[6], (void *)&p};
     return cudaLaunchKernelExC(&lc, reinterpret_cast<const void *>(&gemm_tc_kernel<Cfg>), args);
 }
 

@@ -24,7 +24,7 @@ DTYPE = {"f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM_E4M3, "f32": GEMM_F32,
 EXPORTS = ["gemm_plan_create", "gemm_run", "gemm_run_host", "gemm_plan_last_status", "gemm_plan_get_info",
            "gemm_plan_set_timeout", "gemm_plan_destroy", "gemm_status_string", "gemm_testing_set_fault",
            "gemm_run_noalloc", "gemm_plan_set_split_k", "gemm_chain_plan_create", "gemm_chain_run",
-           "gemm_chain_run_host"]
+           "gemm_chain_run_host", "gemm_plan_set_stream_k"]
 
 
 class GemmError(RuntimeError):
@@ -35,7 +35,8 @@ class GemmError(RuntimeError):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "grid", "tiles",
-                                            "smem_bytes", "launches_per_run", "sm_count", "splits")]
+                                            "smem_bytes", "launches_per_run", "sm_count", "splits",
+                                            "stream_k")]
 
 
 _lib = None
@@ -74,6 +75,8 @@ def lib():
         L.gemm_testing_set_fault.restype = st
         L.gemm_plan_set_split_k.argtypes = [vp, st]
         L.gemm_plan_set_split_k.restype = st
+        L.gemm_plan_set_stream_k.argtypes = [vp, st]
+        L.gemm_plan_set_stream_k.restype = st
         L.gemm_run_noalloc.argtypes = [i64, i64, i64, st, st, vp, vp, vp, vp, vp, st]
         L.gemm_run_noalloc.restype = st
         L.gemm_chain_plan_create.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i64, st, st, ctypes.c_uint]
@@ -173,6 +176,10 @@ def gemm_plan_set_split_k(plan: int, splits: int):
     _check(lib().gemm_plan_set_split_k(plan, splits), "gemm_plan_set_split_k")
 
 
+def gemm_plan_set_stream_k(plan: int, enable: int):
+    _check(lib().gemm_plan_set_stream_k(plan, int(enable)), "gemm_plan_set_stream_k")
+
+
 def gemm_plan_destroy(plan: int):
     _check(lib().gemm_plan_destroy(plan), "gemm_plan_destroy")
 
@@ -218,6 +225,9 @@ class Plan:
 
     def set_split_k(self, splits: int):
         gemm_plan_set_split_k(self.handle, splits)
+
+    def set_stream_k(self, enable: bool):
+        gemm_plan_set_stream_k(self.handle, int(enable))
 
     def close(self):
         if self.handle:
