@@ -21,11 +21,14 @@ using namespace gb300;
 
 // M tiles per rasterisation group (tuning knobs)
 #ifndef GB300_GROUP_M_PAIRS
-#define GB300_GROUP_M_PAIRS 8
+#define GB300_GROUP_M_PAIRS 12
 #endif
 #ifndef GB300_GROUP_M_SINGLE
 #define GB300_GROUP_M_SINGLE 16
 #endif
+
+// gemm_run_host splits a product into at most this many row chunks
+constexpr int HOST_CHUNKS = 8;
 
 struct gemm_plan {
     int64_t M, N, K;
@@ -64,6 +67,10 @@ struct gemm_plan {
     uint8_t *ws_a, *ws_b;     // block-scaled: packed scale factors (workspace)
     // device buffers of gemm_run_host (allocated on first use)
     void *hA, *hB, *hC, *hD;
+    // gemm_run_host's pipeline: copy-in, compute and copy-out streams and their events
+    bool pipe_ready;
+    cudaStream_t pipe_in, pipe_comp, pipe_out;
+    cudaEvent_t pipe_entry, pipe_in_done[HOST_CHUNKS], pipe_k_done[HOST_CHUNKS];
     uint8_t *hSFA, *hSFB;
     // tensor maps of the last run, reused while the pointers repeat
     const void *lastA, *lastB, *lastC, *lastD;
@@ -108,6 +115,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // 2-D row-major tensor [outer][inner] with a box of box_outer x box_inner elements
 bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, int ebytes, const void *ptr, uint64_t inner, uint64_t outer,
                uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    if (!encoder()) return false;      // the driver's encoder is looked up on first use
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * (uint64_t)ebytes};
     cuuint32_t box[2] = {box_inner, box_outer};
@@ -126,10 +134,10 @@ CUtensorMapDataType tma_dtype(gemm_dtype t) {
     }
 }
 
-gemm_status encode_maps(gemm_plan *p, const void *A, const void *B, const void *C, void *D) {
-    if (p->maps_valid && A == p->lastA && B == p->lastB && C == p->lastC && D == p->lastD) return GEMM_OK;
-    if (!encoder()) return GEMM_ERR_CUDA;
-    std::memset(p->maps, 0, 4 * sizeof(CUtensorMap));     // the scale-factor and partial-sum maps stay
+// Tensor maps of A, B, C and D for the plan's operands with M rows (maps[0..3])
+bool encode_operand_maps(const gemm_plan *p, CUtensorMap *maps, const void *A, const void *B, const void *C, void *D,
+                         int64_t M) {
+    std::memset(maps, 0, 4 * sizeof(CUtensorMap));
     // 4-bit operands are mapped as bytes (two K elements each, K-major only)
     const bool fp4 = p->ab == GEMM_E2M1;
     const int eb = fp4 ? 1 : elem_bits(p->ab) / 8;
@@ -139,22 +147,28 @@ gemm_status encode_maps(gemm_plan *p, const void *A, const void *B, const void *
     // K-major operand: [rows][K], box of bk x rows; MN-major operand: [K][rows], box one
     // 128-byte atom (atom elements) wide along the rows and bk deep along K
     const uint32_t atom = 128u / (uint32_t)eb;
-    bool ok = (p->a_mn ? encode_2d(&p->maps[0], tma_dtype(p->ab), eb, A, p->M, p->K, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B)
-                       : encode_2d(&p->maps[0], tma_dtype(p->ab), eb, A, k_units, p->M, bk, TILE_M, CU_TENSOR_MAP_SWIZZLE_128B)) &&
-              (p->b_mn ? encode_2d(&p->maps[1], tma_dtype(p->ab), eb, B, p->N, p->K, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B)
-                       : encode_2d(&p->maps[1], tma_dtype(p->ab), eb, B, k_units, p->N, bk, b_rows, CU_TENSOR_MAP_SWIZZLE_128B));
+    bool ok = (p->a_mn ? encode_2d(&maps[0], tma_dtype(p->ab), eb, A, M, p->K, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B)
+                       : encode_2d(&maps[0], tma_dtype(p->ab), eb, A, k_units, M, bk, TILE_M, CU_TENSOR_MAP_SWIZZLE_128B)) &&
+              (p->b_mn ? encode_2d(&maps[1], tma_dtype(p->ab), eb, B, p->N, p->K, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B)
+                       : encode_2d(&maps[1], tma_dtype(p->ab), eb, B, k_units, p->N, bk, b_rows, CU_TENSOR_MAP_SWIZZLE_128B));
     if (ok && C)
-        ok = encode_2d(&p->maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, p->N, p->M, EPI_COLS, 32,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
+        ok = encode_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, p->N, M, EPI_COLS, 32, CU_TENSOR_MAP_SWIZZLE_128B);
     if (ok) {
         if (p->d == GEMM_BF16)
-            ok = encode_2d(&p->maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, p->N, p->M, EPI_COLS, 32,
+            ok = encode_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, p->N, M, EPI_COLS, 32,
                            CU_TENSOR_MAP_SWIZZLE_64B);
         else
-            ok = encode_2d(&p->maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, p->N, p->M, EPI_COLS, 32,
+            ok = encode_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, p->N, M, EPI_COLS, 32,
                            CU_TENSOR_MAP_SWIZZLE_128B);
     }
-    if (!ok) {
+    return ok;
+}
+
+gemm_status encode_maps(gemm_plan *p, const void *A, const void *B, const void *C, void *D) {
+    if (p->maps_valid && A == p->lastA && B == p->lastB && C == p->lastC && D == p->lastD) return GEMM_OK;
+    if (!encoder()) return GEMM_ERR_CUDA;
+    // maps 4..6 (scale factors, partial sums) belong to the plan and stay
+    if (!encode_operand_maps(p, p->maps, A, B, C, D, p->M)) {
         p->maps_valid = false;
         return GEMM_ERR_CUDA;
     }
@@ -465,6 +479,110 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
     return GEMM_OK;
 }
 
+namespace {
+
+gemm_status pipe_setup(gemm_plan *p) {
+    if (p->pipe_ready) return GEMM_OK;
+    bool ok = cudaStreamCreateWithFlags(&p->pipe_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p->pipe_comp, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&p->pipe_out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p->pipe_entry, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < HOST_CHUNKS; ++i)
+        ok = cudaEventCreateWithFlags(&p->pipe_in_done[i], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&p->pipe_k_done[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) return GEMM_ERR_CUDA;
+    p->pipe_ready = true;
+    return GEMM_OK;
+}
+
+void pipe_destroy(gemm_plan *p) {
+    if (!p->pipe_ready) return;
+    cudaStreamDestroy(p->pipe_in);
+    cudaStreamDestroy(p->pipe_comp);
+    cudaStreamDestroy(p->pipe_out);
+    cudaEventDestroy(p->pipe_entry);
+    for (int i = 0; i < HOST_CHUNKS; ++i) {
+        cudaEventDestroy(p->pipe_in_done[i]);
+        cudaEventDestroy(p->pipe_k_done[i]);
+    }
+}
+
+// The fp16/bf16 kernel on rows [0, rows) of device operands A, C, D (whole tiles, no split-K)
+gemm_status launch_rows(gemm_plan *p, const void *A, const void *B, const void *C, void *D, int64_t rows,
+                        cudaStream_t stream) {
+    CUtensorMap maps[NUM_MAPS];
+    std::memset(maps, 0, sizeof maps);
+    if (!encode_operand_maps(p, maps, A, B, C, D, rows)) return GEMM_ERR_CUDA;
+    const int cg = p->cta_group;
+    KParams kp{};
+    kp.M = (int)rows;
+    kp.N = (int)p->N;
+    kp.K = (int)p->K;
+    kp.tiles_m = (int)((rows + TILE_M * cg - 1) / (TILE_M * cg));
+    kp.tiles_n = p->tiles_n;
+    kp.num_tiles = kp.tiles_m * kp.tiles_n;
+    kp.num_kb = p->num_kb;
+    kp.group_m = p->group_m;
+    kp.has_c = C != nullptr;
+    kp.a_mn = p->a_mn;
+    kp.b_mn = p->b_mn;
+    kp.splits = 1;
+    kp.status = p->status;
+    kp.timeout_ns = p->timeout_ns;
+    kp.fault = p->fault;
+    kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * cg), (uint32_t)TILE_N) |
+               ((uint32_t)p->b_mn << 16);
+    const int units = kp.num_tiles < p->capacity ? kp.num_tiles : p->capacity;
+    LaunchShape shape{cg * units, cg, p->smem};
+    F16Config cfg{cg, p->d == GEMM_BF16};
+    return f16_launch(cfg, shape, maps, kp, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// Host-buffer run as a pipeline over row chunks (fp16/bf16, row-major A, no split-K):
+// B first, then each chunk's rows of A and C go up on one stream, its product runs on a
+// second as soon as they have landed, and its rows of D come back on a third, so that
+// transfers in both directions and the kernels overlap.
+gemm_status run_host_pipelined(gemm_plan *p, const void *A, const void *B, const void *C, void *D, int64_t chunk,
+                               cudaStream_t stream) {
+    if (pipe_setup(p) != GEMM_OK) return GEMM_ERR_CUDA;
+    const size_t a_row = bytes_of(p->ab, p->K), c_row = (size_t)p->N * 4, d_row = bytes_of(p->d, p->N);
+    const size_t b_bytes = bytes_of(p->ab, p->K * p->N);
+    const char *hA = static_cast<const char *>(A), *hC = static_cast<const char *>(C);
+    char *hD = static_cast<char *>(D);
+    char *dA = static_cast<char *>(p->hA), *dC = static_cast<char *>(p->hC), *dD = static_cast<char *>(p->hD);
+    // the pipeline starts after the work already queued on the caller's stream
+    if (cudaEventRecord(p->pipe_entry, stream) != cudaSuccess ||
+        cudaStreamWaitEvent(p->pipe_in, p->pipe_entry, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(p->pipe_comp, p->pipe_entry, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(p->pipe_out, p->pipe_entry, 0) != cudaSuccess ||
+        cudaMemcpyAsync(p->hB, B, b_bytes, cudaMemcpyHostToDevice, p->pipe_in) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    int i = 0;
+    for (int64_t r0 = 0; r0 < p->M; r0 += chunk, ++i) {
+        const int64_t rows = p->M - r0 < chunk ? p->M - r0 : chunk;
+        if (cudaMemcpyAsync(dA + r0 * a_row, hA + r0 * a_row, rows * a_row, cudaMemcpyHostToDevice, p->pipe_in) !=
+                cudaSuccess ||
+            (C && cudaMemcpyAsync(dC + r0 * c_row, hC + r0 * c_row, rows * c_row, cudaMemcpyHostToDevice,
+                                  p->pipe_in) != cudaSuccess) ||
+            cudaEventRecord(p->pipe_in_done[i], p->pipe_in) != cudaSuccess ||
+            cudaStreamWaitEvent(p->pipe_comp, p->pipe_in_done[i], 0) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        const gemm_status st = launch_rows(p, dA + r0 * a_row, p->hB, C ? dC + r0 * c_row : nullptr, dD + r0 * d_row,
+                                           rows, p->pipe_comp);
+        if (st != GEMM_OK) return st;
+        if (cudaEventRecord(p->pipe_k_done[i], p->pipe_comp) != cudaSuccess ||
+            cudaStreamWaitEvent(p->pipe_out, p->pipe_k_done[i], 0) != cudaSuccess ||
+            cudaMemcpyAsync(hD + r0 * d_row, dD + r0 * d_row, rows * d_row, cudaMemcpyDeviceToHost, p->pipe_out) !=
+                cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    // D's last rows are home once the copy-out stream drains (it waited for every kernel)
+    if (cudaStreamSynchronize(p->pipe_out) != cudaSuccess) return GEMM_ERR_CUDA;
+    return gemm_plan_last_status(p);
+}
+
+}  // namespace
+
 gemm_status gemm_run_host(gemm_plan_t p, const void *A, const void *B, const void *C, void *D, const uint8_t *SFA,
                           const uint8_t *SFB, void *cuda_stream) {
     if (!p || !A || !B || !D || p->family == FAMILY_CHAIN) return GEMM_ERR_INVALID_ARG;
@@ -478,6 +596,15 @@ gemm_status gemm_run_host(gemm_plan_t p, const void *A, const void *B, const voi
             return GEMM_ERR_CUDA;
     }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
+    // fp16/bf16 with row-major A (contiguous row chunks) and room for two or more chunks of
+    // at least 1024 rows: the pipelined form
+    if (p->family == KIND_F16 && !p->a_mn && p->splits == 1) {
+        const int64_t tile = (int64_t)TILE_M * p->cta_group;
+        int64_t chunk = (p->M + HOST_CHUNKS - 1) / HOST_CHUNKS;
+        chunk = (chunk + tile - 1) / tile * tile;
+        if (chunk < 1024) chunk = 1024;
+        if (p->M >= 2 * chunk) return run_host_pipelined(p, A, B, C, D, chunk, stream);
+    }
     if (cudaMemcpyAsync(p->hA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
         cudaMemcpyAsync(p->hB, B, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
@@ -561,6 +688,7 @@ gemm_status gemm_plan_destroy(gemm_plan_t p) {
     cudaFree(p->hSFA);
     cudaFree(p->hSFB);
     cudaFree(p->hE);
+    pipe_destroy(p);
     cudaFree(p->ws_a);
     cudaFree(p->ws_b);
     cudaFree(p->ws_p);

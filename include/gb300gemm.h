@@ -142,7 +142,12 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
  * The same product with HOST buffers (any host memory; page-locked memory
  * copies fastest): copies A, B, C (and SFA, SFB) to device buffers the plan
  * owns (allocated on first use, freed by gemm_plan_destroy), runs the kernel,
- * copies D back and waits for the stream.  Returns the kernel's status.
+ * copies D back and waits for it.  Returns the kernel's status.  For fp16/bf16
+ * plans with row-major A and at least two chunks of 1024 rows, the product runs
+ * as a pipeline over up to 8 row chunks on three plan-owned streams (after the
+ * work already queued on cuda_stream): B and then each chunk's rows of A and C
+ * are copied up, each chunk's product starts as soon as its rows have landed,
+ * and its rows of D are copied back while the next chunks are copied up.
  */
 gemm_status gemm_run_host(gemm_plan_t p, const void *A, const void *B, const void *C, void *D,
                           const uint8_t *SFA, const uint8_t *SFB, void *cuda_stream);
