@@ -54,7 +54,6 @@ struct gemm_plan {
     int sk_request;           // stream-K: 1 = where it balances the waves (default), 0 = never
     int sk;                   // stream-K chosen
     int sk_dp_tiles;          // stream-K: tiles the units take whole before their spans
-    float *ws_p;              // stream-K: partial-sum slots (units x CG x 128 rows x tile_n fp32)
     int *sk_flags;            // stream-K: one flag per (slot, CTA of the group)
     uint32_t epoch;           // stream-K: runs so far (the value a run's flags carry)
     int tile_n;
@@ -167,7 +166,7 @@ bool encode_operand_maps(const gemm_plan *p, CUtensorMap *maps, const void *A, c
 gemm_status encode_maps(gemm_plan *p, const void *A, const void *B, const void *C, void *D) {
     if (p->maps_valid && A == p->lastA && B == p->lastB && C == p->lastC && D == p->lastD) return GEMM_OK;
     if (!encoder()) return GEMM_ERR_CUDA;
-    // maps 4..6 (scale factors, partial sums) belong to the plan and stay
+    // maps 4 and 5 (scale factors) belong to the plan and stay
     if (!encode_operand_maps(p, p->maps, A, B, C, D, p->M)) {
         p->maps_valid = false;
         return GEMM_ERR_CUDA;
@@ -283,31 +282,20 @@ gemm_status choose_splits(gemm_plan *p) {
     // more work units than tiles: the persistent grid may grow up to the machine
     const int work = p->tiles * s;
     p->grid = p->cta_group * (work < units ? work : units);
-    // measured on GB300: worth it with long tiles (>= 64 k-blocks: the cut pieces' extra
-    // epilogue work stays small) and few waves (below 8 the idle part of the last wave is
-    // a large share; above, the power the idle SMs leave lets the busy ones clock higher)
-    p->sk = s == 1 && p->sk_request && p->tiles >= units && p->tiles % units != 0 && p->num_kb >= 64 &&
-            p->tiles < 8 * units;
+    // fp32 D only (the partial sums meet in D itself), and as measured on GB300 only with
+    // long tiles (>= 64 k-blocks: the cut pieces' extra epilogue work stays small) and few
+    // waves (below 4 the idle part of the last wave is a large share; above, the power the
+    // idle SMs leave lets the busy ones clock higher)
+    p->sk = s == 1 && p->sk_request && p->d == GEMM_F32 && p->tiles >= units && p->tiles % units != 0 &&
+            p->num_kb >= 64 && p->tiles < 4 * units;
     if (p->sk) {
         p->sk_dp_tiles = (p->tiles / units - 1) * units;
         p->grid = p->cta_group * units;
-        // flags always; the partial-sum workspace only for bf16 D (fp32 partial sums go into D)
         if (!p->sk_flags) {
-            const size_t ws = (size_t)units * p->cta_group * TILE_M * p->tile_n * sizeof(float);
             const size_t fl = (size_t)units * p->cta_group * sizeof(int);
-            const bool need_ws = p->d == GEMM_BF16;
-            if ((need_ws && cudaMalloc(&p->ws_p, ws) != cudaSuccess) || cudaMalloc(&p->sk_flags, fl) != cudaSuccess ||
-                cudaMemset(p->sk_flags, 0, fl) != cudaSuccess) {
-                cudaFree(p->ws_p);
+            if (cudaMalloc(&p->sk_flags, fl) != cudaSuccess || cudaMemset(p->sk_flags, 0, fl) != cudaSuccess) {
                 cudaFree(p->sk_flags);
-                p->ws_p = nullptr;
                 p->sk_flags = nullptr;
-                p->sk = 0;
-                return GEMM_ERR_CUDA;
-            }
-            if (need_ws && (!encoder() || !encode_2d(&p->maps[6], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p->ws_p,
-                                                     p->tile_n, (uint64_t)units * p->cta_group * TILE_M, EPI_COLS,
-                                                     32, CU_TENSOR_MAP_SWIZZLE_128B))) {
                 p->sk = 0;
                 return GEMM_ERR_CUDA;
             }
@@ -396,7 +384,6 @@ gemm_status gemm_plan_create(gemm_plan_t *out, int64_t M, int64_t N, int64_t K, 
     if (choose_splits(p) != GEMM_OK || cudaMalloc(&p->status, sizeof(int)) != cudaSuccess) {
         cudaFree(p->ws_a);
         cudaFree(p->ws_b);
-        cudaFree(p->ws_p);
         cudaFree(p->sk_flags);
         delete p;
         return GEMM_ERR_CUDA;
@@ -448,7 +435,6 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
         kp.epoch = (int)(++p->epoch & 0x7FFFFFFF);
         if (kp.epoch == 0) kp.epoch = p->epoch = 1;
         kp.sk_flags = p->sk_flags;
-        kp.sk_ws = p->ws_p;
     }
     LaunchShape shape{p->grid, p->cta_group, p->smem};
     if (p->family != KIND_F16) {
@@ -691,7 +677,6 @@ gemm_status gemm_plan_destroy(gemm_plan_t p) {
     pipe_destroy(p);
     cudaFree(p->ws_a);
     cudaFree(p->ws_b);
-    cudaFree(p->ws_p);
     cudaFree(p->sk_flags);
     delete p;
     return GEMM_OK;

@@ -27,20 +27,18 @@ struct KParams {
     // stream-K (sk != 0): the first sk_dp_tiles tiles go to the units whole, round by round;
     // the (tile, k-block) iterations of the remaining tiles are cut into sk_units equal
     // spans, one per unit.  A tile cut between two spans is finished by the unit whose
-    // span covers its first k-block: the other unit stores its partial sum (into D for
-    // fp32 D, which the finishing unit then adds into; into workspace slot `unit` for bf16
-    // D) and publishes `epoch` in sk_flags[unit * CG + rank].
+    // span covers its first k-block: the other unit stores its partial sum into D (fp32)
+    // and publishes `epoch` in sk_flags[unit * CG + rank]; the finishing unit then adds
+    // its own into D.
     int sk;
     int sk_dp_tiles;
     int sk_units;
     int epoch;
     int *sk_flags;
-    const float *sk_ws;  // stream-K with bf16 D: partial sums, row-major [slots x CG x 128][tile columns]
 };
 
-// Tensor maps a kernel takes: A, B, C, D, the packed scale factors (block-scaled only) and
-// the stream-K partial sums (fp32 [slots x CG x 128 rows][tile columns]).
-constexpr int NUM_MAPS = 7;
+// Tensor maps a kernel takes: A, B, C, D, and the packed scale factors (block-scaled only).
+constexpr int NUM_MAPS = 6;
 
 // A launch: grid, cluster width and dynamic shared memory.
 struct LaunchShape {

@@ -164,8 +164,9 @@ __device__ __forceinline__ int kb_at(int j, int kb0, int kb1, uint32_t round) {
 
 // A piece of work: K blocks [kb0, kb1) of tile (tm, tn).  ROLE_TILE pieces cover a
 // whole tile (or, with split-K, one slice); stream-K pieces that cover only part of a
-// tile are ROLE_EARLY (ends the tile, starts a span: stores a partial sum in workspace
-// slot `slot`) or ROLE_FINAL (starts the tile, ends a span: adds that partial).
+// tile are ROLE_EARLY (ends the tile, starts a span: stores its partial sum into D and
+// publishes flag `slot`) or ROLE_FINAL (starts the tile, ends a span: adds into D once
+// flag `slot` is published).
 enum : int { ROLE_TILE = 0, ROLE_EARLY = 1, ROLE_FINAL = 2 };
 struct Work {
     int tm, tn, kb0, kb1, role, slot;
@@ -289,7 +290,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                    const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
-                   const __grid_constant__ CUtensorMap tmP, const KParams p) {
+                   const KParams p) {
     constexpr int CG = Cfg::CG;
     constexpr int STAGES = Cfg::STAGES;
     constexpr int BN = Cfg::BN;
@@ -320,7 +321,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         prefetch_tensormap(&tmB);
         if (p.has_c) prefetch_tensormap(&tmC);
         prefetch_tensormap(&tmD);
-        if (Cfg::OUT_BF16 && p.sk) prefetch_tensormap(&tmP);   // the partial-sum map exists for bf16 D only
         if constexpr (Cfg::SCALED) {
             prefetch_tensormap(&tmSFA);
             prefetch_tensormap(&tmSFB);
@@ -548,9 +548,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint32_t aph = Cfg::ACC_BUFS == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
             const int m_warp = wk.tm * TILE_M * CG + (int)rank * TILE_M + 32 * q;
             const int n_warp = wk.tn * BN + h * Cfg::WCOLS;
-            // this warp's rows and columns of a stream-K partial sum in the workspace
-            const int ws_row = (wk.slot * CG + (int)rank) * TILE_M + 32 * q;
-            const int ws_col = h * Cfg::WCOLS;
             // 32 x 32 boxes that lie wholly outside D are neither loaded nor stored
             const int chunks_in = m_warp < p.M ? max(0, min(Cfg::WCHUNKS, (p.N - n_warp + EPI_COLS - 1) / EPI_COLS)) : 0;
             // every piece but a partial sum (ROLE_EARLY) adds C, loaded box by box
@@ -564,19 +561,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + b * BN + h * Cfg::WCOLS;
 
             auto release_accumulator = [&]() { release(b); };
-            // a stream-K piece that starts its tile waits for its tile's other piece to have
-            // published (the flag carries this run's epoch): with fp32 D that piece has stored
-            // its partial sum into D and this one adds into it; with bf16 D the partial sum is
-            // in the workspace and this one reads it
+            // a stream-K piece that starts its tile waits until its tile's other piece has
+            // stored its partial sum into D and published it (the flag carries this run's
+            // epoch); this one then adds into D
             auto await_partial = [&]() -> bool {
                 if (wk.role != ROLE_FINAL) return true;
                 const bool got = W.wait_flag(p.sk_flags + wk.slot * CG + (int)rank, p.epoch);
                 if (got && lane == 0) fence_proxy_async_global();   // the flag before TMA traffic to D
                 return __all_sync(0xffffffffu, got);
             };
-            // one 32 x 32 box: add C (and a partial sum), convert, stage in shared memory, then
-            // TMA-store it to D (reduce-add for split-K slices and for fp32 stream-K finals), or
-            // a partial sum to D (fp32) or the workspace (bf16 D)
+            // one 32 x 32 box: add C, convert, stage in shared memory, then TMA-store it to D
+            // (reduce-add for split-K slices and for stream-K pieces that finish a tile)
             auto store_box = [&](int j, const uint32_t (&acc)[32]) -> bool {
                 const uint32_t cur = ec & 1u;
                 uint8_t *buf = ebuf + cur * Cfg::EPI_BUF;
@@ -588,21 +583,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
-                if constexpr (Cfg::OUT_BF16) {
-                    if (wk.role == ROLE_FINAL) {
-                        // row `lane` of this box of the partial sum (row-major fp32 workspace, L2)
-                        const float4 *src = reinterpret_cast<const float4 *>(
-                            p.sk_ws + (size_t)(ws_row + lane) * BN + ws_col + EPI_COLS * j);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const float4 pv = __ldcg(src + c);
-                            v[4 * c + 0] += pv.x;
-                            v[4 * c + 1] += pv.y;
-                            v[4 * c + 2] += pv.z;
-                            v[4 * c + 3] += pv.w;
-                        }
-                    }
-                }
                 if (use_c) {
                     if (!landed(cur)) return false;
                     add_box(cur, v);
@@ -610,7 +590,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     bulk_wait_group_read1();                  // the store two boxes back has read this buffer
                 }
                 __syncwarp();
-                if (Cfg::OUT_BF16 && wk.role != ROLE_EARLY) {
+                if constexpr (Cfg::OUT_BF16) {
                     // 64-byte rows, 64-byte swizzle: chunk c at (c ^ ((row / 2) % 4))
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -632,9 +612,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (lane == 0) {
                     const int dx = n_warp + EPI_COLS * j;
                     if (wk.role == ROLE_EARLY) {
-                        if (Cfg::OUT_BF16) tma_store_2d(&tmP, smem_addr(buf), ws_col + EPI_COLS * j, ws_row);
-                        else tma_store_2d(&tmD, smem_addr(buf), dx, m_warp);
-                    } else if (p.splits > 1 || (wk.role == ROLE_FINAL && !Cfg::OUT_BF16)) {
+                        tma_store_2d(&tmD, smem_addr(buf), dx, m_warp);
+                    } else if (p.splits > 1 || wk.role == ROLE_FINAL) {
                         tma_reduce_add_2d(&tmD, smem_addr(buf), dx, m_warp);
                     } else {
                         tma_store_2d_hint(&tmD, smem_addr(buf), dx, m_warp, stream_pol);
@@ -719,8 +698,8 @@ cudaError_t launch_tc(const LaunchShape &shape, const CUtensorMap *maps, const K
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    void *args[8] = {(void *)&maps[0], (void *)&maps[1], (void *)&maps[2], (void *)&maps[3],
-                     (void *)&maps[4], (void *)&maps[5], (void *)&maps[6], (void *)&p};
+    void *args[7] = {(void *)&maps[0], (void *)&maps[1], (void *)&maps[2], (void *)&maps[3],
+                     (void *)&maps[4], (void *)&maps[5], (void *)&p};
     return cudaLaunchKernelExC(&lc, reinterpret_cast<const void *>(&gemm_tc_kernel<Cfg>), args);
 }
 

@@ -190,20 +190,20 @@ gemm_status gemm_plan_set_split_k(gemm_plan_t p, int splits);
 
 /*
  * Stream-K scheduling of the same product (a property of this library; the pages have
- * no counterpart to it, and it does not change what is computed).  When a plan has more
- * output tiles than its persistent grid runs at once but not a whole number of waves,
- * the CTAs (or CTA pairs) first take whole tiles round by round, then share the last one
- * to two waves' worth of tiles out as equal spans of K blocks, so that all of them
- * finish together.  A tile cut between two spans is finished by the span that covers its
- * first K block: the other stores its fp32 partial sum (into D itself for fp32 D, which
- * the finishing CTA then adds into; into a plan-owned workspace of about 20 MB for bf16
- * D) and publishes it with a flag the finishing CTA waits for (a bounded wait:
- * GEMM_ERR_TIMEOUT if it runs out).  Results do
- * not depend on timing (each tile is summed in a fixed order), so the schedule is allowed
- * with GEMM_FLAG_DETERMINISTIC; it is never combined with split-K.  enable = 1 (the
- * default) uses it where it was measured to pay — at least 64 K blocks per tile and
- * fewer than 8 waves — and 0 never; other values return GEMM_ERR_INVALID_ARG.
- * Runs of one stream-K plan must not overlap on the GPU (they share the workspace).
+ * no counterpart to it, and it does not change what is computed).  When an fp32-D plan
+ * has more output tiles than its persistent grid runs at once but not a whole number of
+ * waves, the CTAs (or CTA pairs) first take whole tiles round by round, then share the
+ * last one to two waves' worth of tiles out as equal spans of K blocks, so that all of
+ * them finish together.  A tile cut between two spans is finished by the span that
+ * covers its first K block: the other stores its partial sum into D and publishes it
+ * with a flag (plan-owned, a few hundred bytes); the finishing CTA waits for the flag (a
+ * bounded wait: GEMM_ERR_TIMEOUT if it runs out) and adds its own part and C into D with
+ * a TMA reduce-add.  Results do not depend on timing (each tile is summed in a fixed
+ * order), so the schedule is allowed with GEMM_FLAG_DETERMINISTIC; it is never combined
+ * with split-K.  enable = 1 (the default) uses it where it was measured to pay — fp32 D,
+ * at least 64 K blocks per tile and fewer than 4 waves — and 0 never; other values
+ * return GEMM_ERR_INVALID_ARG.  Runs of one stream-K plan must not overlap on the GPU
+ * (they share the flags).
  */
 gemm_status gemm_plan_set_stream_k(gemm_plan_t p, int enable);
 

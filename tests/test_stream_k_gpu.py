@@ -1,6 +1,7 @@
-"""Stream-K (the last waves' tiles shared out as equal spans of K blocks, cut tiles
-finished from a published fp32 partial sum) against the oracle and against the
-whole-tile schedule, for every kernel family, both CTA modes and both D types."""
+"""Stream-K (the last waves' tiles shared out as equal spans of K blocks; a cut tile's
+first piece stores its partial sum into D and publishes it, the piece that finishes
+the tile adds into D) against the oracle and against the whole-tile schedule, for
+every kernel family and both CTA modes, and the plan's choice of it."""
 import numpy as np
 import pytest
 
@@ -47,8 +48,8 @@ def _run(w, flags, stream_k=True, c_none=False, reps=1):
 @pytest.mark.parametrize("name,M,N,K,d", [
     # 2cta: 8 x 10 = 80 pair tiles over 76 pairs (every tile in a span); 1cta: 160 tiles, 152 CTAs
     ("bf16_4096x4096x4096_f32out", 2048, 2560, 4096, "f32"),
-    # ragged edges, bf16 D, a K tail; 1cta: 16 x 11 = 176 tiles (one whole round, then spans)
-    ("f16_4000x3000x2056_f32out", 2000, 2696, 4104, "bf16"),
+    # ragged edges, a K tail; 1cta: 16 x 11 = 176 tiles (one whole round, then spans)
+    ("f16_4000x3000x2056_f32out", 2000, 2700, 4104, "f32"),
 ])
 def test_stream_k_matches_oracle(variant, name, M, N, K, d):
     w = synth.scaled(W[name], M, N, K, d=d)
@@ -96,11 +97,15 @@ def test_stream_k_c_none():
 
 
 def test_stream_k_rule():
-    # short tiles (16 k-blocks) or many waves: whole tiles only
+    # short tiles (16 k-blocks), many waves or bf16 D: whole tiles only
     with gemm.Plan(2048, 2560, 1024, "bf16", "f32") as plan:
         assert plan.info["stream_k"] == 0
-    with gemm.Plan(8192, 8192, 8192, "bf16", "bf16") as plan:
+    with gemm.Plan(8192, 8192, 8192, "bf16", "f32") as plan:
         assert plan.info["stream_k"] == 0
+    with gemm.Plan(4096, 4096, 4096, "bf16", "bf16") as plan:
+        assert plan.info["stream_k"] == 0
+    with gemm.Plan(4096, 4096, 4096, "bf16", "f32") as plan:
+        assert plan.info["stream_k"] == (1 if plan.info["grid"] == 152 else plan.info["stream_k"])
 
 
 def test_stream_k_not_used_for_whole_waves():
