@@ -57,8 +57,10 @@ namespace gb300 {
 //             each taking half of the tile's columns)
 //   COPIER  block-scaled: a warp of its own issues the scale-factor copies (the
 //           MMA thread then issues MMAs only)
+//   EPI_BUFS  staging buffers per epilogue warp: 2 = the next box's C loads while this
+//             box is stored; 1 = one box at a time (leaves shared memory for a stage)
 template <int CG_, bool OUT_BF16_, int KIND_, int BN_, int STAGES_, int ACC_BUFS_ = 2, int EPI_WARPS_ = 4,
-          bool COPIER_ = false>
+          bool COPIER_ = false, int EPI_BUFS_ = 2>
 struct TileCfg {
     static constexpr int CG = CG_;
     static constexpr bool OUT_BF16 = OUT_BF16_;
@@ -68,6 +70,8 @@ struct TileCfg {
     static constexpr int STAGES = STAGES_;
     static constexpr int ACC_BUFS = ACC_BUFS_;
     static constexpr int EPI_WARPS = EPI_WARPS_;
+    static constexpr int EPI_BUFS = EPI_BUFS_;
+    static_assert(EPI_BUFS == 1 || EPI_BUFS == 2, "epilogue staging buffers");
     static constexpr bool COPIER = COPIER_ && KIND_ != KIND_F16;
     static constexpr int COPY_WARP = 2 + EPI_WARPS;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS + (COPIER ? 32 : 0);
@@ -110,7 +114,7 @@ struct TileCfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_SF = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_EPI = align1k(OFF_SF + STAGES * (SFA_BYTES + SFB_BYTES));
-    static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * 2 * EPI_BUF;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_BUFS * EPI_BUF;
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && OFF_B % 1024 == 0, "operand stages 1024-aligned");
     static_assert(OFF_EPI % 1024 == 0 && EPI_BUF % 1024 == 0, "epilogue staging 1024-aligned");
     // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], cload[EPI_WARPS][2], drain,
@@ -499,11 +503,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int e = warp - 2;                           // epilogue warp index
         const int q = warp & 3;                           // TMEM lane window of this warp
         const int h = e / 4;                              // which WCOLS-wide column slice of the tile
-        uint8_t *ebuf = smem + Cfg::OFF_EPI + e * 2 * Cfg::EPI_BUF;
+        uint8_t *ebuf = smem + Cfg::OFF_EPI + e * Cfg::EPI_BUFS * Cfg::EPI_BUF;
         uint64_t *cb = cload + 2 * e;
         // C is read once and D written once: let them leave L2 before the operand tiles
         const uint64_t stream_pol = l2_policy_evict_first();
-        // ec counts the 32 x 32 boxes this warp has stored (box ec is staged in buffer ec % 2);
+        // ec counts the 32 x 32 boxes this warp has stored (box ec is staged in buffer
+        // ec % EPI_BUFS);
         // lc[i] counts the loads issued into buffer i (the phases of cb[i]); n_early counts the
         // stream-K partial sums this CTA has published (the phases of epi_sync)
         uint32_t acc_it = 0, ec = 0, n_early = 0;
@@ -554,7 +559,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const bool use_c = wk.role != ROLE_EARLY && p.has_c && chunks_in > 0;
             if (use_c) {                   // the piece's first C box loads while its accumulator is computed
                 if (lane == 0) bulk_wait_group_read0();
-                issue(ec & 1u, &tmC, n_warp, m_warp);
+                issue(ec % Cfg::EPI_BUFS, &tmC, n_warp, m_warp);
             }
             if (!__all_sync(0xffffffffu, W.wait(&tfull[b], aph))) break;
             tc_fence_after_sync();
@@ -573,13 +578,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // one 32 x 32 box: add C, convert, stage in shared memory, then TMA-store it to D
             // (reduce-add for split-K slices and for stream-K pieces that finish a tile)
             auto store_box = [&](int j, const uint32_t (&acc)[32]) -> bool {
-                const uint32_t cur = ec & 1u;
+                const uint32_t cur = ec % Cfg::EPI_BUFS;
                 uint8_t *buf = ebuf + cur * Cfg::EPI_BUF;
-                if (use_c && j + 1 < chunks_in) {
+                if (Cfg::EPI_BUFS == 2 && use_c && j + 1 < chunks_in) {
                     if (lane == 0) bulk_wait_group_read0();   // the store from the other buffer has read it
                     issue(cur ^ 1u, &tmC, n_warp + EPI_COLS * (j + 1), m_warp);
                 }
                 if (j >= chunks_in) return true;
+                if (Cfg::EPI_BUFS == 1 && use_c && j > 0) {   // one buffer: this box's C loads now
+                    if (lane == 0) bulk_wait_group_read0();   // the last store has read the buffer
+                    issue(0, &tmC, n_warp + EPI_COLS * j, m_warp);
+                }
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
@@ -587,7 +596,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     if (!landed(cur)) return false;
                     add_box(cur, v);
                 } else if (lane == 0) {
-                    bulk_wait_group_read1();                  // the store two boxes back has read this buffer
+                    // the store that last used this buffer (one or two boxes back) has read it
+                    if (Cfg::EPI_BUFS == 2) bulk_wait_group_read1();
+                    else bulk_wait_group_read0();
                 }
                 __syncwarp();
                 if constexpr (Cfg::OUT_BF16) {
