@@ -105,6 +105,9 @@ struct TileCfg {
     static constexpr int SFA_BYTES = 512 * SF_WORDS;
     static constexpr int SFB_BYTES = 512 * SF_WORDS * HALVES;
     static constexpr int TX_BYTES = CG * (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES);
+    // with a copier warp the scales land on a barrier of their own (sffull), ahead of A and B
+    static constexpr int TX_AB = CG * (A_BYTES + B_BYTES);
+    static constexpr int TX_SF = CG * (SFA_BYTES + SFB_BYTES);
     static constexpr int EPI_BUF = 32 * EPI_COLS * 4;           // one 32 x 32 fp32 box
     // Every region a swizzled TMA copy or a swizzled MMA descriptor addresses
     // starts on a 1024-byte boundary: the 128-byte swizzle permutes 16-byte
@@ -118,8 +121,9 @@ struct TileCfg {
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && OFF_B % 1024 == 0, "operand stages 1024-aligned");
     static_assert(OFF_EPI % 1024 == 0 && EPI_BUF % 1024 == 0, "epilogue staging 1024-aligned");
     // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], cload[EPI_WARPS][2], drain,
-    // epi_sync, then with COPIER: sfull[STAGES] (the stage's scales are in TMEM), cdrain
-    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 * EPI_WARPS + 2 + (COPIER ? STAGES + 1 : 0);
+    // epi_sync, then with COPIER: sfull[STAGES] (the stage's scales are in TMEM), cdrain,
+    // sffull[STAGES] (the stage's scales are in shared memory)
+    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 * EPI_WARPS + 2 + (COPIER ? 2 * STAGES + 1 : 0);
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base slot, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
     // TMEM columns: accumulators [0, ACC_BUFS*BN), then one scale slot per stage: SFA
@@ -316,6 +320,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint64_t *epi_sync = drain + 1;                       // every epilogue warp stored its part of a partial sum
     uint64_t *sfull = epi_sync + 1;                       // COPIER only
     uint64_t *cdrain = sfull + STAGES;                    // COPIER only
+    uint64_t *sffull = cdrain + 1;                        // COPIER only
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 4);
     const Waiter W{abort_flag, p.status, p.timeout_ns};
@@ -341,7 +346,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         mbar_init(drain, 1);
         mbar_init(epi_sync, Cfg::EPI_WARPS);
         if constexpr (Cfg::COPIER) {
-            for (int i = 0; i < STAGES; ++i) mbar_init(&sfull[i], 1);
+            for (int i = 0; i < STAGES; ++i) {
+                mbar_init(&sfull[i], 1);
+                mbar_init(&sffull[i], 1);
+            }
             mbar_init(cdrain, 1);
         }
         *abort_flag = 0;
@@ -376,7 +384,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const int kb = kb_at(j, kb0, kb1, round);
                     if (!W.wait(&empty[s], ph ^ 1u)) { ok = false; break; }
                     const bool withhold = p.fault == 1 && round == 0 && j == 0;
-                    if (rank == 0 && !withhold) mbar_arrive_expect_tx(&full[s], Cfg::TX_BYTES);
+                    if (rank == 0 && Cfg::COPIER) mbar_arrive_expect_tx(&sffull[s], Cfg::TX_SF);
+                    if (rank == 0 && !withhold) mbar_arrive_expect_tx(&full[s], Cfg::COPIER ? Cfg::TX_AB : Cfg::TX_BYTES);
                     const uint32_t a_dst = smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES);
                     const uint32_t b_dst = smem_addr(smem + Cfg::OFF_B + s * Cfg::B_BYTES);
                     const uint32_t fb = smem_addr(&full[s]);
@@ -386,11 +395,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const int sfa_row = ((tm * CG + (int)rank) * p.num_kb + kb) * (Cfg::SFA_BYTES / 128);
                     const int sfb_row = (tn * p.num_kb + kb) * (Cfg::SFB_BYTES / 128);
                     // the completion of every copy of the stage counts on the leader's full[s]
+                    // (the scales' on its sffull[s] when a copier warp moves them)
                     const uint32_t bar = CG == 1 ? fb : mapa_shared(fb, 0);
-                    auto load = [&](uint32_t dst, const CUtensorMap *m, int c0, int c1) {
-                        if constexpr (CG == 1) tma_load_2d(dst, m, bar, c0, c1);
-                        else tma_load_2d_pair(dst, m, bar, c0, c1);
+                    uint32_t sbar = bar;
+                    if constexpr (Cfg::COPIER) {
+                        const uint32_t sfb = smem_addr(&sffull[s]);
+                        sbar = CG == 1 ? sfb : mapa_shared(sfb, 0);
+                    }
+                    auto load_on = [&](uint32_t dst, const CUtensorMap *m, int c0, int c1, uint32_t mb) {
+                        if constexpr (CG == 1) tma_load_2d(dst, m, mb, c0, c1);
+                        else tma_load_2d_pair(dst, m, mb, c0, c1);
                     };
+                    auto load = [&](uint32_t dst, const CUtensorMap *m, int c0, int c1) { load_on(dst, m, c0, c1, bar); };
                     // an operand tile: K-major, one box of BK x rows; MN-major, rows / ATOM_MN
                     // boxes of ATOM_MN x BK, one per 128-byte atom column
                     auto load_operand = [&](uint32_t dst, const CUtensorMap *m, int row0, int rows, bool mn) {
@@ -401,12 +417,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                                 load(dst + i * Cfg::ATOM_BYTES, m, row0 + i * Cfg::ATOM_MN, kb * Cfg::BK);
                         }
                     };
+                    if constexpr (Cfg::SCALED) {    // the scales first: the copier warp starts on them
+                        load_on(sf_dst, &tmSFA, 0, sfa_row, sbar);
+                        load_on(sf_dst + Cfg::SFA_BYTES, &tmSFB, 0, sfb_row, sbar);
+                    }
                     load_operand(a_dst, &tmA, m0, TILE_M, p.a_mn != 0);
                     load_operand(b_dst, &tmB, n0, Cfg::B_ROWS, p.b_mn != 0);
-                    if constexpr (Cfg::SCALED) {
-                        load(sf_dst, &tmSFA, 0, sfa_row);
-                        load(sf_dst + Cfg::SFA_BYTES, &tmSFB, 0, sfb_row);
-                    }
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
             }
@@ -474,7 +490,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // ---------------------------------------------------------- scale copies
         if constexpr (Cfg::COPIER) {
             if (rank == 0 && lane == 0) {
-                // stage s's slot is rewritten only after full[s] of the next round, i.e. after
+                // stage s's slot is rewritten only after sffull[s] of the next round, i.e. after
                 // the producer saw empty[s]: the MMAs that read the slot have completed
                 int s = 0;
                 uint32_t ph = 0;
@@ -483,7 +499,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 Work wk;
                 while (ok && it.next(p, wk)) {
                     for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
-                        if (!W.wait(&full[s], ph)) { ok = false; break; }
+                        if (!W.wait(&sffull[s], ph)) { ok = false; break; }
                         tc_fence_after_sync();
                         const uint32_t sfa_t = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_SLOT;
                         copy_scales<Cfg>(smem, s, sfa_t, sfa_t + 4 * Cfg::SF_WORDS);

@@ -28,7 +28,7 @@ using Mx1 = TileCfg<1, OUT_BF16, KIND_MXF8, 224, 4, 2, 4>;
 #define GB300_MXF8_PAIR_EPI_BUFS 1
 #endif
 template <bool OUT_BF16>
-using Mx2 = TileCfg<2, OUT_BF16, KIND_MXF8, 256, GB300_MXF8_PAIR_STAGES, 1, 8, false, GB300_MXF8_PAIR_EPI_BUFS>;
+using Mx2 = TileCfg<2, OUT_BF16, KIND_MXF8, 256, GB300_MXF8_PAIR_STAGES, 1, 8, true, GB300_MXF8_PAIR_EPI_BUFS>;
 using MxF8 = ScaledInstances<Mx1<false>, Mx1<true>, Mx2<false>, Mx2<true>>;
 
 }  // namespace
