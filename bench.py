@@ -219,6 +219,26 @@ def workload(args):
 
 # --------------------------------------------------------------- our arm
 
+def tensor_rate(w, info, achieved, clock_summary):
+    """Per-clock view of the roofline: the tensor-pipe rate probe (after the timed region)
+    gives the FLOP per SM clock of the plan's MMA shape; the kernel's TFLOP/s is then set
+    against that rate at the maximum SM clock and at the clock sampled while it ran.  The
+    probe's operands are zero, so its own clock (and TFLOP/s) sits above what real data
+    draws under the power limit; the per-clock rate does not depend on the clock."""
+    from blackwell_tensor_core_tma_gb300 import gemm
+    r = gemm.gemm_measure_tensor_rate(w.ab, w.block_scaled, info["cta_group"], 8192)
+    per_clk, sms = r["flop_per_clk_per_sm"], info["sm_count"]
+    max_mhz = clock_summary.get("sm_max_mhz") or 2070.0
+    at_max = sms * per_clk * max_mhz * 1e6 / 1e12
+    run_mhz = clock_summary.get("sm_mhz")
+    at_run = sms * per_clk * run_mhz * 1e6 / 1e12 if run_mhz else None
+    return {"flop_per_clk_per_sm": round(per_clk, 1), "probe_sm_mhz": round(r["sm_mhz"], 1),
+            "probe_tflops": round(r["tflops"], 1), "peak_at_max_clock": round(at_max, 1),
+            "max_mhz": max_mhz, "frac_at_max_clock": round(achieved / at_max, 4),
+            "frac_at_run_clock": round(achieved / at_run, 4) if at_run else None,
+            "run_clock_source": "nvidia-smi median over the timed region"}
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -319,6 +339,9 @@ def run_ours(args, rank, world, local_rank):
                 "frac_of_sustained": round(achieved / (peaks.get("bf16_tflops_sustained", peak) * ratio), 4),
                 "kernel": "gemm_tc_kernel",
                 "kernel_ms": round(kernel_ms, 5)}
+    clock_summary = clocks.summary()
+    if not args.no_probe:
+        roofline["tensor_rate"] = tensor_rate(w, info, achieved, clock_summary)
 
     out = {
         "metric": "GEMM TFLOP/s and % of GB300 dense tensor peak (bf16 8192^3), vs CPU oracle",
@@ -335,7 +358,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": args.steps * info["launches_per_run"],
-        "clocks": clocks.summary(),
+        "clocks": clock_summary,
     }
     plan.close()
     if rank == 0 and not args.no_cpu:
@@ -607,6 +630,7 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-probe", action="store_true", help="skip the tensor-pipe rate probe")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0)
     ap.add_argument("--traffic", type=float, default=None,

@@ -24,7 +24,7 @@ DTYPE = {"f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM_E4M3, "f32": GEMM_F32,
 EXPORTS = ["gemm_plan_create", "gemm_run", "gemm_run_host", "gemm_plan_last_status", "gemm_plan_get_info",
            "gemm_plan_set_timeout", "gemm_plan_destroy", "gemm_status_string", "gemm_testing_set_fault",
            "gemm_run_noalloc", "gemm_plan_set_split_k", "gemm_chain_plan_create", "gemm_chain_run",
-           "gemm_chain_run_host", "gemm_plan_set_stream_k"]
+           "gemm_chain_run_host", "gemm_plan_set_stream_k", "gemm_measure_tensor_rate"]
 
 
 class GemmError(RuntimeError):
@@ -37,6 +37,11 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("cta_group", "tile_m", "tile_n", "tile_k", "stages", "grid", "tiles",
                                             "smem_bytes", "launches_per_run", "sm_count", "splits",
                                             "stream_k")]
+
+
+class TensorRate(ctypes.Structure):
+    _fields_ = [("flop_per_clk_per_sm", ctypes.c_double), ("sm_mhz", ctypes.c_double), ("tflops", ctypes.c_double),
+                ("ms", ctypes.c_double), ("sms", ctypes.c_int)]
 
 
 _lib = None
@@ -79,6 +84,8 @@ def lib():
         L.gemm_plan_set_stream_k.restype = st
         L.gemm_run_noalloc.argtypes = [i64, i64, i64, st, st, vp, vp, vp, vp, vp, st]
         L.gemm_run_noalloc.restype = st
+        L.gemm_measure_tensor_rate.argtypes = [st, st, st, i64, ctypes.POINTER(TensorRate)]
+        L.gemm_measure_tensor_rate.restype = st
         L.gemm_chain_plan_create.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i64, st, st, ctypes.c_uint]
         L.gemm_chain_plan_create.restype = st
         for name in ("gemm_chain_run", "gemm_chain_run_host"):
@@ -194,6 +201,16 @@ def gemm_run_noalloc(M: int, N: int, K: int, ab, d, A, B, C, D, stream=None, wai
                                 _stream(stream), int(wait))
     _check(st, "gemm_run_noalloc")
     return st
+
+
+def gemm_measure_tensor_rate(ab, block_scaled: int = GEMM_SCALE_NONE, cta_group: int = 2,
+                             iters: int = 4096) -> dict:
+    """The tensor-pipe rate probe: FLOP per SM clock of the GEMM's MMA shape, the SM clock
+    during the probe, and the whole-GPU TFLOP/s it reached (blocks until done)."""
+    out = TensorRate()
+    _check(lib().gemm_measure_tensor_rate(DTYPE.get(ab, ab), int(block_scaled), int(cta_group), int(iters),
+                                          ctypes.byref(out)), "gemm_measure_tensor_rate")
+    return {n: getattr(out, n) for n, _ in TensorRate._fields_}
 
 
 class Plan:

@@ -275,6 +275,31 @@ gemm_status gemm_chain_run_host(gemm_plan_t p, const void *A, const void *B, con
                                 void *D, void *cuda_stream);
 
 /* Static description of a status code. */
+/*
+ * Tensor-pipe rate probe (measurement, not part of the GEMM path).  Launches one
+ * CTA (cta_group = 1) or CTA pair (cta_group = 2) per SM; in each, one thread
+ * issues `iters` groups of four back-to-back tcgen05.mma of the GEMM kernels'
+ * instruction shape (M = 128 * cta_group, N = 256, 32 bytes of K per
+ * instruction: K = 16 for f16/bf16, 32 for e4m3, 64 for e2m1) from operands
+ * already in shared memory into one TMEM accumulator, and times the stream
+ * with the SM clock and the globaltimer ("Blackwell Tensor Core": one thread
+ * issues tcgen05.mma, the accumulator lives in TMEM).  ab / block_scaled pick
+ * the kind as for gemm_plan_create.  1 <= iters <= 2^20.  Synchronises the
+ * device first and again before returning; meant for an otherwise idle GPU.
+ * Errors: GEMM_ERR_INVALID_ARG (out NULL, cta_group not 1 or 2, iters out of
+ * range), GEMM_ERR_UNSUPPORTED (another kind or device), GEMM_ERR_CUDA,
+ * GEMM_ERR_TIMEOUT (a CTA's wait ran out).  *out is written only on GEMM_OK.
+ */
+typedef struct {
+    double flop_per_clk_per_sm;  /* dense FLOP per SM clock (median over CTA groups; 2 FLOP per multiply-add) */
+    double sm_mhz;               /* SM clock during the run (median of clocks / globaltimer time) */
+    double tflops;               /* whole-GPU rate: FLOPs of every CTA group / kernel time (CUDA events) */
+    double ms;                   /* kernel time */
+    int sms;                     /* CTAs launched (one per SM) */
+} gemm_tensor_rate;
+gemm_status gemm_measure_tensor_rate(gemm_dtype ab, int block_scaled, int cta_group, int64_t iters,
+                                     gemm_tensor_rate *out);
+
 const char *gemm_status_string(gemm_status s);
 
 #ifdef __cplusplus

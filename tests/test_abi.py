@@ -120,3 +120,19 @@ def test_chain_plan_rejects_before_device(lib, args, kw, status):
 def test_chain_calls_reject_null(lib):
     assert lib.gemm_chain_run(None, None, None, None, None, None, None) == gemm.GEMM_ERR_INVALID_ARG
     assert lib.gemm_chain_run_host(None, None, None, None, None, None, None) == gemm.GEMM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args,status", [
+    ((gemm.GEMM_BF16, 0, 3, 64), gemm.GEMM_ERR_INVALID_ARG),        # cta_group 3
+    ((gemm.GEMM_BF16, 0, 2, 0), gemm.GEMM_ERR_INVALID_ARG),         # no iterations
+    ((gemm.GEMM_BF16, 0, 2, (1 << 20) + 1), gemm.GEMM_ERR_INVALID_ARG),
+    ((gemm.GEMM_BF16, 5, 2, 64), gemm.GEMM_ERR_INVALID_ARG),        # block_scaled out of range
+    ((gemm.GEMM_F32, 0, 2, 64), gemm.GEMM_ERR_UNSUPPORTED),
+    ((gemm.GEMM_E4M3, gemm.GEMM_SCALE_UE4M3_16, 2, 64), gemm.GEMM_ERR_UNSUPPORTED),
+    ((gemm.GEMM_BF16, gemm.GEMM_SCALE_UE8M0_32, 1, 64), gemm.GEMM_ERR_UNSUPPORTED),
+])
+def test_tensor_rate_probe_rejects_before_device(lib, args, status):
+    out = gemm.TensorRate()
+    import ctypes
+    assert lib.gemm_measure_tensor_rate(*args, ctypes.byref(out)) == status
+    assert lib.gemm_measure_tensor_rate(gemm.GEMM_BF16, 0, 2, 64, None) == gemm.GEMM_ERR_INVALID_ARG
