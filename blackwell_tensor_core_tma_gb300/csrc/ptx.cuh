@@ -65,15 +65,22 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
 }
 
 // one probe of phase `parity`; cluster-scope acquire so that arrivals released
-// by the peer CTA of a pair are ordered before what follows
+// by the peer CTA of a pair are ordered before what follows.  The explicit
+// suspend-time hint bounds how long the thread sleeps inside the probe: with the
+// default limit, a thread whose barrier was completed by the cluster (a pair's
+// remote arrivals, a multicast commit) was seen to resume 1.3-1.5 us after the
+// completion, which stalled the MMA issuer at every tile boundary.
+#ifndef GB300_MBAR_SUSPEND_NS
+#define GB300_MBAR_SUSPEND_NS 32
+#endif
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred P;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2, %3;\n\t"
         "selp.b32 %0, 1, 0, P;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"((uint32_t)GB300_MBAR_SUSPEND_NS)
         : "memory");
     return ok != 0;
 }
