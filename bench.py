@@ -39,15 +39,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture
 # summarised in profiles/; valid only for the kernel sources the capture ran on
 MEASURED_TRAFFIC = {
-    "bf16_8192x8192x8192_bf16out": {"bytes": 1147522048 + 125594112, "src": "15c2e75e009b6756",
+    "bf16_8192x8192x8192_bf16out": {"bytes": 1138562560 + 123100928, "src": "15329b193f4e3db4",
                                     "ncu": "profiles/gemm_tc_kernel_bf16_8192x8192x8192_bf16out_launches.md"},
-    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 679223808 + 235662592, "src": "60ee38e52745b1c1",
+    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 676302080 + 235404032, "src": "3b8148c75fd6edc6",
                                           "ncu": "profiles/gemm_tc_kernel_mxf8_8192x8192x8192_launches.md"},
-    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 483979008 + 216036608, "src": "f16436fea5c529c7",
+    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 482768384 + 216126976, "src": "689b7ff473d2e9db",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 495036672 + 218056704, "src": "dbdfc44180f748a6",
+    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 494488320 + 218182912, "src": "a8400e7c5c8f43be",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312179456 + 12005888, "src": "fd152ffb457153a4",
+    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312859136 + 12512000, "src": "77f70f080a2cbc73",
                                               "ncu": "profiles/chain_kernel_bf16_32768x4096_256x256_launches.md"},
 }
 
