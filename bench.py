@@ -39,15 +39,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture
 # summarised in profiles/; valid only for the kernel sources the capture ran on
 MEASURED_TRAFFIC = {
-    "bf16_8192x8192x8192_bf16out": {"bytes": 1138562560 + 123100928, "src": "15329b193f4e3db4",
+    "bf16_8192x8192x8192_bf16out": {"bytes": 1138562560 + 123100928, "src": "a476c8ed04fa1cf9",
                                     "ncu": "profiles/gemm_tc_kernel_bf16_8192x8192x8192_bf16out_launches.md"},
-    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 676302080 + 235404032, "src": "3b8148c75fd6edc6",
+    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 676302080 + 235404032, "src": "078fa9d8bf7a0756",
                                           "ncu": "profiles/gemm_tc_kernel_mxf8_8192x8192x8192_launches.md"},
-    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 482768384 + 216126976, "src": "689b7ff473d2e9db",
+    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 482768384 + 216126976, "src": "d1108a59d87a4cc5",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 494488320 + 218182912, "src": "a8400e7c5c8f43be",
+    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 494488320 + 218182912, "src": "a0e3647d91deb099",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312859136 + 12512000, "src": "77f70f080a2cbc73",
+    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312859136 + 12512000, "src": "625b27984023cb94",
                                               "ncu": "profiles/chain_kernel_bf16_32768x4096_256x256_launches.md"},
 }
 
@@ -68,14 +68,39 @@ def kernel_family(workload_name: str) -> str:
     return "f16"
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and with runs of whitespace collapsed, so that a
+    change to comments alone leaves the kernel's hash (and its recorded traffic) valid."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":                 # a literal: copied up to its closing quote
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(family: str = "f16") -> str:
-    """Hash of the CUDA sources the GEMM kernel of a family is built from."""
+    """Hash of the CUDA sources (comments stripped) the GEMM kernel of a family is built from."""
     import hashlib
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[family]:
         h.update(f.encode())
-        with open(os.path.join(ROOT, "blackwell_tensor_core_tma_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "blackwell_tensor_core_tma_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

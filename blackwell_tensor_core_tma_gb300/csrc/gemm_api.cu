@@ -28,7 +28,14 @@ using namespace gb300;
 #endif
 
 // gemm_run_host splits a product into at most this many row chunks
-constexpr int HOST_CHUNKS = 8;
+#ifndef GB300_HOST_CHUNKS
+#define GB300_HOST_CHUNKS 8
+#endif
+#ifndef GB300_HOST_MIN_ROWS
+#define GB300_HOST_MIN_ROWS 1024
+#endif
+constexpr int HOST_CHUNKS = GB300_HOST_CHUNKS;        // row chunks of the host-buffer pipeline (at most)
+constexpr int HOST_MIN_ROWS = GB300_HOST_MIN_ROWS;    // rows of the smallest chunk
 
 struct gemm_plan {
     int64_t M, N, K;
@@ -588,7 +595,7 @@ gemm_status gemm_run_host(gemm_plan_t p, const void *A, const void *B, const voi
         const int64_t tile = (int64_t)TILE_M * p->cta_group;
         int64_t chunk = (p->M + HOST_CHUNKS - 1) / HOST_CHUNKS;
         chunk = (chunk + tile - 1) / tile * tile;
-        if (chunk < 1024) chunk = 1024;
+        if (chunk < HOST_MIN_ROWS) chunk = HOST_MIN_ROWS;
         if (p->M >= 2 * chunk) return run_host_pipelined(p, A, B, C, D, chunk, stream);
     }
     if (cudaMemcpyAsync(p->hA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||

@@ -5,7 +5,7 @@
 //
 // One CTA (cta_group::1) or one CTA pair (cta_group::2) owns a 128 x BN or
 // 256 x BN output tile at a time and walks the tile list persistently.
-// Warp roles (192 threads):
+// Warp roles (192 threads; 64 + 32 * EPI_WARPS + a copier warp in general):
 //   warp 0      TMA producer: fills a STAGES-deep shared-memory ring of
 //               A (128 rows) and B (BN/CG rows) boxes of 128-byte K rows,
 //               128-byte swizzled, running STAGES k-blocks ahead of the MMA
@@ -13,7 +13,8 @@
 //               prefetch distance fetch_batch = compute_batch + num_stages;
 //               one thread issues each copy, completion is an mbarrier
 //               transaction count).  Block-scaled kernels also copy the
-//               stage's packed scale factors.
+//               stage's packed scale factors (with COPIER, first and onto a
+//               barrier of their own, sffull[s], so the copier can start early).
 //   warp 1      allocates 512 TMEM columns (two BN-column fp32 accumulators,
 //               plus scale-factor slots when block-scaled) and, in lane 0 of
 //               the pair's leader CTA, issues tcgen05.mma from shared-memory
@@ -22,10 +23,11 @@
 //               block scaling it first moves the stage's scales SMEM -> TMEM
 //               with tcgen05.cp (same page: SFA, SFB: GMEM --TMA--> SMEM
 //               --tcgen05.cp--> TMEM --tcgen05.mma-->).
-//   warp 2+EPI  (block-scaled instances with COPIER) issues the stage's scale copies
-//               SMEM -> TMEM ahead of the MMA issuer and signals them on sfull[s], so
-//               that copies and MMAs come from two threads.
-//   warps 2..5  epilogue warpgroup: warp w reads TMEM lanes 32*(w%4)..+31
+//   warp 2+EPI  (block-scaled instances with COPIER) waits for the stage's scales
+//               (sffull[s]), copies them SMEM -> TMEM ahead of the MMA issuer and
+//               signals the copies' completion on sfull[s], so that copies and MMAs
+//               come from two threads and overlap.
+//   warps 2..5  epilogue warps (2..9 with EPI_WARPS = 8): warp w reads TMEM lanes 32*(w%4)..+31
 //               ("Tensor Memory（TMEM）": each warp of a warpgroup reaches its
 //               own 32-lane window) with tcgen05.ld + tcgen05.wait::ld, adds C
 //               (TMA-loaded, 128-byte swizzled), converts, stages D in shared

@@ -14,7 +14,7 @@ namespace {
 
 // single CTAs: 128 x 128 tiles, two accumulators, five stages, 4 epilogue warps.
 // CTA pairs: 256 x 256 tiles, one 256-column accumulator drained to registers by
-// 8 epilogue warps, four stages (the shared memory the scales leave), and a copier
+// 8 epilogue warps, five stages (one epilogue staging buffer per warp), and a copier
 // warp that issues the scale copies so that they overlap the MMAs (measured on
 // 8192^3: +6 % with two scales per step, +19 % with four).
 template <bool OUT_BF16>

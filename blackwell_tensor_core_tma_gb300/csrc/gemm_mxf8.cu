@@ -14,9 +14,11 @@ namespace {
 
 // single CTAs: 128 x 224 tiles, two accumulators (448 TMEM columns) and four
 // stages of 12-column scale slots, 4 epilogue warps.
-// CTA pairs: 256 x 256 tiles (an MMA of N = 256 keeps the tensor pipe busiest),
-// one 256-column accumulator that 8 epilogue warps copy to registers and free
-// at once, the other 256 TMEM columns for the stages' scale slots.
+// CTA pairs: 256 x 256 tiles (the fewest operand bytes per FLOP that TMEM allows
+// alongside the scale slots), one 256-column accumulator that 8 epilogue warps
+// copy to registers and free at once, the other 256 TMEM columns for the stages'
+// scale slots, and a copier warp that issues the scale copies (measured on 8192^3:
+// +8.5 % over copies issued by the MMA thread).
 template <bool OUT_BF16>
 using Mx1 = TileCfg<1, OUT_BF16, KIND_MXF8, 224, 4, 2, 4>;
 // pair ring depth and epilogue staging buffers per warp (tuning knobs): one buffer per

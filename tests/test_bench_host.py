@@ -64,3 +64,17 @@ def test_reference_arm_line(capsys, monkeypatch):
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_kernel_hash_ignores_comments_only():
+    """Recorded DRAM traffic stays attached to a kernel across comment edits, not code edits."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = 'int a = 1; // note\n/* block\n comment */ asm("tcgen05.mma // not a comment");\n'
+    assert bench.strip_comments(src) == bench.strip_comments(src.replace("note", "other note"))
+    assert bench.strip_comments(src) == bench.strip_comments(src.replace("block", "a longer block"))
+    assert "not a comment" in bench.strip_comments(src)
+    assert bench.strip_comments(src) != bench.strip_comments(src.replace("a = 1", "a = 2"))
+    for fam in bench.KERNEL_SOURCES:
+        h = bench.kernel_source_hash(fam)
+        assert len(h) == 16 and h == bench.kernel_source_hash(fam)
