@@ -59,6 +59,7 @@ struct gemm_plan {
     int capacity;             // work units the persistent grid runs at once (CTAs or CTA pairs)
     int split_request;        // 0 = choose automatically, n >= 1 = asked for
     int sk_request;           // stream-K: 1 = where it balances the waves (default), 0 = never
+    int wide_epi;             // fp16/bf16 pairs, fp32 D, short K: the 8-epilogue-warp kernel
     int sk;                   // stream-K chosen
     int sk_dp_tiles;          // stream-K: tiles the units take whole before their spans
     int *sk_flags;            // stream-K: one flag per (slot, CTA of the group)
@@ -195,8 +196,8 @@ gemm_status configure_f16(gemm_plan *p) {
     F16Config cfg{cg, p->d == GEMM_BF16};
     if (f16_prepare(cfg) != cudaSuccess) return GEMM_ERR_CUDA;
     p->cta_group = cg;
-    p->stages = f16_stages(cg);
-    p->smem = f16_smem_bytes(cg);
+    p->stages = f16_stages(cfg);
+    p->smem = f16_smem_bytes(cfg);
     p->tile_n = TILE_N;
     p->tile_k = TILE_K16;
     p->num_kb = (int)((p->K + TILE_K16 - 1) / TILE_K16);
@@ -307,6 +308,17 @@ gemm_status choose_splits(gemm_plan *p) {
                 return GEMM_ERR_CUDA;
             }
         }
+    }
+    // whole-tile fp16/bf16 pairs with fp32 D and short K: the tile's C-in/D-out epilogue
+    // outlasts the next tile's main loop, so twice the epilogue warps (one stage fewer)
+    // pay; with bf16 D or longer K they lose (measured on GB300)
+    if (p->family == KIND_F16) {
+        F16Config cfg{p->cta_group, p->d == GEMM_BF16, 0};
+        cfg.wide_epi = p->cta_group == 2 && p->d == GEMM_F32 && s == 1 && !p->sk && p->num_kb <= 40;
+        if (cfg.wide_epi && f16_prepare(cfg) != cudaSuccess) return GEMM_ERR_CUDA;
+        p->wide_epi = cfg.wide_epi;
+        p->stages = f16_stages(cfg);
+        p->smem = f16_smem_bytes(cfg);
     }
     return GEMM_OK;
 }
@@ -462,7 +474,7 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
     } else {
         kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * p->cta_group), (uint32_t)TILE_N) |
                    ((uint32_t)p->a_mn << 15) | ((uint32_t)p->b_mn << 16);
-        F16Config cfg{p->cta_group, p->d == GEMM_BF16};
+        F16Config cfg{p->cta_group, p->d == GEMM_BF16, p->wide_epi};
         if (f16_launch(cfg, shape, p->maps, kp, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     }
     if (p->flags & GEMM_FLAG_SYNC) {
@@ -527,7 +539,7 @@ gemm_status launch_rows(gemm_plan *p, const void *A, const void *B, const void *
                ((uint32_t)p->b_mn << 16);
     const int units = kp.num_tiles < p->capacity ? kp.num_tiles : p->capacity;
     LaunchShape shape{cg * units, cg, p->smem};
-    F16Config cfg{cg, p->d == GEMM_BF16};
+    F16Config cfg{cg, p->d == GEMM_BF16, p->wide_epi};
     return f16_launch(cfg, shape, maps, kp, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 

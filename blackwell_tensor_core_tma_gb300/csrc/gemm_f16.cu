@@ -1,7 +1,11 @@
 // fp16 / bf16 instances of the tensor-core GEMM (gemm_kernel.cuh):
 //   cta_group::1  128 x 256 tiles, 4-stage ring
 //   cta_group::2  256 x 256 tiles per CTA pair, 6-stage ring
-// each with fp32 or bf16 D.
+// each with fp32 or bf16 D, and for pairs with fp32 D a wide-epilogue form: 8 epilogue
+// warps (two per TMEM lane window, each half of the tile's columns) and 5 stages, for
+// short K, where storing a tile (C in, D out, 512 KiB per pair) takes longer than the
+// next tile's main loop (measured: +14 % at 4096x4096x1024, +3.5 % at 4000x3000x2056,
+// -2 % at 4096^3, so the plan chooses it for at most 40 k-blocks).
 #include "gemm_kernel.cuh"
 
 // ring depths (tuning knobs; the defaults fill shared memory)
@@ -17,6 +21,8 @@ namespace {
 
 template <int CG, bool OUT_BF16>
 using F16Cfg = TileCfg<CG, OUT_BF16, KIND_F16, TILE_N, CG == 1 ? GB300_F16_CG1_STAGES : GB300_F16_CG2_STAGES>;
+using F16Wide = TileCfg<2, false, KIND_F16, TILE_N, 5, 2, 8>;
+bool wide(const F16Config &cfg) { return cfg.wide_epi && cfg.cta_group == 2 && !cfg.out_bf16; }
 
 // D = C (or 0): the starting value split-K slices add their partial products to
 __global__ void init_d_kernel(float4 *__restrict__ D, const float4 *__restrict__ C, size_t n4) {
@@ -36,18 +42,24 @@ cudaError_t init_d_launch(float *D, const float *C, size_t n, int sm_count, cuda
     return cudaGetLastError();
 }
 
-int f16_stages(int cta_group) { return cta_group == 1 ? F16Cfg<1, false>::STAGES : F16Cfg<2, false>::STAGES; }
+int f16_stages(const F16Config &cfg) {
+    if (wide(cfg)) return F16Wide::STAGES;
+    return cfg.cta_group == 1 ? F16Cfg<1, false>::STAGES : F16Cfg<2, false>::STAGES;
+}
 
-int f16_smem_bytes(int cta_group) {
-    return cta_group == 1 ? F16Cfg<1, false>::SMEM_BYTES : F16Cfg<2, false>::SMEM_BYTES;
+int f16_smem_bytes(const F16Config &cfg) {
+    if (wide(cfg)) return F16Wide::SMEM_BYTES;
+    return cfg.cta_group == 1 ? F16Cfg<1, false>::SMEM_BYTES : F16Cfg<2, false>::SMEM_BYTES;
 }
 
 cudaError_t f16_prepare(const F16Config &cfg) {
+    if (wide(cfg)) return prepare_tc<F16Wide>();
     if (cfg.cta_group == 1) return cfg.out_bf16 ? prepare_tc<F16Cfg<1, true>>() : prepare_tc<F16Cfg<1, false>>();
     return cfg.out_bf16 ? prepare_tc<F16Cfg<2, true>>() : prepare_tc<F16Cfg<2, false>>();
 }
 
 cudaError_t f16_max_active_clusters(const F16Config &cfg, int *clusters) {
+    if (wide(cfg)) return max_active_clusters_tc<F16Wide>(clusters);
     if (cfg.cta_group == 1)
         return cfg.out_bf16 ? max_active_clusters_tc<F16Cfg<1, true>>(clusters)
                             : max_active_clusters_tc<F16Cfg<1, false>>(clusters);
@@ -57,6 +69,7 @@ cudaError_t f16_max_active_clusters(const F16Config &cfg, int *clusters) {
 
 cudaError_t f16_launch(const F16Config &cfg, const LaunchShape &shape, const CUtensorMap *maps, const KParams &p,
                        cudaStream_t stream) {
+    if (wide(cfg)) return launch_tc<F16Wide>(shape, maps, p, stream);
     if (cfg.cta_group == 1)
         return cfg.out_bf16 ? launch_tc<F16Cfg<1, true>>(shape, maps, p, stream)
                             : launch_tc<F16Cfg<1, false>>(shape, maps, p, stream);

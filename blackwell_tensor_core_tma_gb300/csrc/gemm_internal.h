@@ -51,9 +51,10 @@ struct LaunchShape {
 struct F16Config {
     int cta_group;   // 1 or 2
     int out_bf16;    // D is bf16 (else fp32)
+    int wide_epi = 0;   // pairs with fp32 D: 8 epilogue warps and one stage fewer (short K)
 };
-int f16_stages(int cta_group);
-int f16_smem_bytes(int cta_group);
+int f16_stages(const F16Config &cfg);
+int f16_smem_bytes(const F16Config &cfg);
 cudaError_t f16_prepare(const F16Config &cfg);   // set the kernel's shared-memory limit
 cudaError_t f16_max_active_clusters(const F16Config &cfg, int *clusters);
 cudaError_t f16_launch(const F16Config &cfg, const LaunchShape &shape, const CUtensorMap *maps,

@@ -135,7 +135,7 @@ extern "C" gemm_status gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dt
     kp.timeout_ns = 1000000000ull;
     kp.fault = 0;
     const int units = cg == 2 ? s->pair_clusters : s->sm_count;
-    LaunchShape shape{cg * (kp.num_tiles < units ? kp.num_tiles : units), cg, f16_smem_bytes(cg)};
+    LaunchShape shape{cg * (kp.num_tiles < units ? kp.num_tiles : units), cg, f16_smem_bytes(cfg)};
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
     // the array keeps the previous call's status: it must start at zero
