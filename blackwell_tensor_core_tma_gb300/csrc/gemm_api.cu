@@ -195,20 +195,46 @@ gemm_status configure_f16(gemm_plan *p) {
     (void)pair_fits;
     F16Config cfg{cg, p->d == GEMM_BF16};
     if (f16_prepare(cfg) != cudaSuccess) return GEMM_ERR_CUDA;
-    p->cta_group = cg;
-    p->stages = f16_stages(cfg);
-    p->smem = f16_smem_bytes(cfg);
-    p->tile_n = TILE_N;
-    p->tile_k = TILE_K16;
-    p->num_kb = (int)((p->K + TILE_K16 - 1) / TILE_K16);
-    p->tiles_m = (int)((p->M + TILE_M * cg - 1) / (TILE_M * cg));
-    p->tiles_n = (int)((p->N + TILE_N - 1) / TILE_N);
-    p->tiles = p->tiles_m * p->tiles_n;
     int units = p->sm_count / cg;
     if (cg == 2) {
         int clusters = 0;
         if (f16_max_active_clusters(cfg, &clusters) == cudaSuccess && clusters > 0) units = clusters;
     }
+    p->tiles_m = (int)((p->M + TILE_M * cg - 1) / (TILE_M * cg));
+    // pairs: 256 x 224 tiles when they fill the persistent rounds clearly better than 256 x 256
+    // ones.  Estimated efficiency (each factor measured on GB300) = used share of the tile
+    // columns x busy share of the rounds (0.89 where stream-K would balance them) x, for 224,
+    // the 3.5 % its extra operand bytes per FLOP cost at 8192^3, or, for 256 with fp32 D and
+    // short K, the gain of the wide epilogue (+14 % at 16 k-blocks, +3.5 % at 33).  An
+    // N-contiguous B needs whole 64-element atoms per CTA (112 rows are not): it keeps 256.
+    if (cg == 2 && !p->b_mn) {
+        const int64_t kb = (p->K + TILE_K16 - 1) / TILE_K16;
+        const bool f32 = p->d == GEMM_F32;
+        auto eff = [&](int bn) {
+            const int64_t tn = (p->N + bn - 1) / bn, tiles = (int64_t)p->tiles_m * tn;
+            const int64_t rounds = (tiles + units - 1) / units;
+            const bool sk = f32 && kb >= 64 && tiles >= units && tiles % units != 0 && tiles < 4 * units;
+            double e = (double)p->N / (double)(tn * bn);
+            e *= sk ? 0.89 : (double)tiles / (double)(rounds * units);
+            if (bn == F16_NARROW_N) e *= 0.965;
+            else if (f32 && kb <= 40 && 2 * tiles > units) e *= 1.0 + 0.1 * (double)(40 - kb) / 24.0;
+            return e;
+        };
+        if (eff(F16_NARROW_N) > 1.02 * eff(TILE_N)) {
+            cfg.tile_n = F16_NARROW_N;
+            if (f16_prepare(cfg) != cudaSuccess) return GEMM_ERR_CUDA;
+            int clusters = 0;
+            if (f16_max_active_clusters(cfg, &clusters) == cudaSuccess && clusters > 0) units = clusters;
+        }
+    }
+    p->cta_group = cg;
+    p->stages = f16_stages(cfg);
+    p->smem = f16_smem_bytes(cfg);
+    p->tile_n = cfg.tile_n;
+    p->tile_k = TILE_K16;
+    p->num_kb = (int)((p->K + TILE_K16 - 1) / TILE_K16);
+    p->tiles_n = (int)((p->N + p->tile_n - 1) / p->tile_n);
+    p->tiles = p->tiles_m * p->tiles_n;
     p->capacity = units;
     p->grid = cg * (p->tiles < units ? p->tiles : units);
     p->group_m = cg == 2 ? GB300_GROUP_M_PAIRS : GB300_GROUP_M_SINGLE;
@@ -313,8 +339,9 @@ gemm_status choose_splits(gemm_plan *p) {
     // outlasts the next tile's main loop, so twice the epilogue warps (one stage fewer)
     // pay; with bf16 D or longer K they lose (measured on GB300)
     if (p->family == KIND_F16) {
-        F16Config cfg{p->cta_group, p->d == GEMM_BF16, 0};
-        cfg.wide_epi = p->cta_group == 2 && p->d == GEMM_F32 && s == 1 && !p->sk && p->num_kb <= 40;
+        F16Config cfg{p->cta_group, p->d == GEMM_BF16, 0, p->tile_n};
+        cfg.wide_epi = p->cta_group == 2 && p->tile_n == TILE_N && p->d == GEMM_F32 && s == 1 && !p->sk &&
+                       p->num_kb <= 40;
         if (cfg.wide_epi && f16_prepare(cfg) != cudaSuccess) return GEMM_ERR_CUDA;
         p->wide_epi = cfg.wide_epi;
         p->stages = f16_stages(cfg);
@@ -472,9 +499,9 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
             cudaSuccess)
             return GEMM_ERR_CUDA;
     } else {
-        kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * p->cta_group), (uint32_t)TILE_N) |
+        kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * p->cta_group), (uint32_t)p->tile_n) |
                    ((uint32_t)p->a_mn << 15) | ((uint32_t)p->b_mn << 16);
-        F16Config cfg{p->cta_group, p->d == GEMM_BF16, p->wide_epi};
+        F16Config cfg{p->cta_group, p->d == GEMM_BF16, p->wide_epi, p->tile_n};
         if (f16_launch(cfg, shape, p->maps, kp, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     }
     if (p->flags & GEMM_FLAG_SYNC) {
@@ -535,11 +562,11 @@ gemm_status launch_rows(gemm_plan *p, const void *A, const void *B, const void *
     kp.status = p->status;
     kp.timeout_ns = p->timeout_ns;
     kp.fault = p->fault;
-    kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * cg), (uint32_t)TILE_N) |
+    kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * cg), (uint32_t)p->tile_n) |
                ((uint32_t)p->b_mn << 16);
     const int units = kp.num_tiles < p->capacity ? kp.num_tiles : p->capacity;
     LaunchShape shape{cg * units, cg, p->smem};
-    F16Config cfg{cg, p->d == GEMM_BF16, p->wide_epi};
+    F16Config cfg{cg, p->d == GEMM_BF16, p->wide_epi, p->tile_n};
     return f16_launch(cfg, shape, maps, kp, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 

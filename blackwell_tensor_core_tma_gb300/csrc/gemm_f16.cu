@@ -5,7 +5,11 @@
 // warps (two per TMEM lane window, each half of the tile's columns) and 5 stages, for
 // short K, where storing a tile (C in, D out, 512 KiB per pair) takes longer than the
 // next tile's main loop (measured: +14 % at 4096x4096x1024, +3.5 % at 4000x3000x2056,
-// -2 % at 4096^3, so the plan chooses it for at most 40 k-blocks).
+// -2 % at 4096^3, so the plan chooses it for at most 40 k-blocks); and for pairs a
+// 256 x 224 tile (6 stages, 4 epilogue warps) that a plan takes when its tiles fill the
+// persistent waves clearly better than 256 x 256 ones (4096^3: 304 tiles = 4 waves of 76
+// pairs instead of 256 = 3.4; measured +6 %; at 8192^3 the extra operand bytes per FLOP
+// cost 3.5 %).
 #include "gemm_kernel.cuh"
 
 // ring depths (tuning knobs; the defaults fill shared memory)
@@ -22,7 +26,10 @@ namespace {
 template <int CG, bool OUT_BF16>
 using F16Cfg = TileCfg<CG, OUT_BF16, KIND_F16, TILE_N, CG == 1 ? GB300_F16_CG1_STAGES : GB300_F16_CG2_STAGES>;
 using F16Wide = TileCfg<2, false, KIND_F16, TILE_N, 5, 2, 8>;
-bool wide(const F16Config &cfg) { return cfg.wide_epi && cfg.cta_group == 2 && !cfg.out_bf16; }
+template <bool OUT_BF16>
+using F16Narrow = TileCfg<2, OUT_BF16, KIND_F16, F16_NARROW_N, GB300_F16_CG2_STAGES>;
+bool narrow(const F16Config &cfg) { return cfg.cta_group == 2 && cfg.tile_n == F16_NARROW_N; }
+bool wide(const F16Config &cfg) { return !narrow(cfg) && cfg.wide_epi && cfg.cta_group == 2 && !cfg.out_bf16; }
 
 // D = C (or 0): the starting value split-K slices add their partial products to
 __global__ void init_d_kernel(float4 *__restrict__ D, const float4 *__restrict__ C, size_t n4) {
@@ -43,22 +50,28 @@ cudaError_t init_d_launch(float *D, const float *C, size_t n, int sm_count, cuda
 }
 
 int f16_stages(const F16Config &cfg) {
+    if (narrow(cfg)) return F16Narrow<false>::STAGES;
     if (wide(cfg)) return F16Wide::STAGES;
     return cfg.cta_group == 1 ? F16Cfg<1, false>::STAGES : F16Cfg<2, false>::STAGES;
 }
 
 int f16_smem_bytes(const F16Config &cfg) {
+    if (narrow(cfg)) return F16Narrow<false>::SMEM_BYTES;
     if (wide(cfg)) return F16Wide::SMEM_BYTES;
     return cfg.cta_group == 1 ? F16Cfg<1, false>::SMEM_BYTES : F16Cfg<2, false>::SMEM_BYTES;
 }
 
 cudaError_t f16_prepare(const F16Config &cfg) {
+    if (narrow(cfg)) return cfg.out_bf16 ? prepare_tc<F16Narrow<true>>() : prepare_tc<F16Narrow<false>>();
     if (wide(cfg)) return prepare_tc<F16Wide>();
     if (cfg.cta_group == 1) return cfg.out_bf16 ? prepare_tc<F16Cfg<1, true>>() : prepare_tc<F16Cfg<1, false>>();
     return cfg.out_bf16 ? prepare_tc<F16Cfg<2, true>>() : prepare_tc<F16Cfg<2, false>>();
 }
 
 cudaError_t f16_max_active_clusters(const F16Config &cfg, int *clusters) {
+    if (narrow(cfg))
+        return cfg.out_bf16 ? max_active_clusters_tc<F16Narrow<true>>(clusters)
+                            : max_active_clusters_tc<F16Narrow<false>>(clusters);
     if (wide(cfg)) return max_active_clusters_tc<F16Wide>(clusters);
     if (cfg.cta_group == 1)
         return cfg.out_bf16 ? max_active_clusters_tc<F16Cfg<1, true>>(clusters)
@@ -69,6 +82,9 @@ cudaError_t f16_max_active_clusters(const F16Config &cfg, int *clusters) {
 
 cudaError_t f16_launch(const F16Config &cfg, const LaunchShape &shape, const CUtensorMap *maps, const KParams &p,
                        cudaStream_t stream) {
+    if (narrow(cfg))
+        return cfg.out_bf16 ? launch_tc<F16Narrow<true>>(shape, maps, p, stream)
+                            : launch_tc<F16Narrow<false>>(shape, maps, p, stream);
     if (wide(cfg)) return launch_tc<F16Wide>(shape, maps, p, stream);
     if (cfg.cta_group == 1)
         return cfg.out_bf16 ? launch_tc<F16Cfg<1, true>>(shape, maps, p, stream)

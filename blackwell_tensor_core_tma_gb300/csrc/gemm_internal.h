@@ -9,6 +9,10 @@
 
 namespace gb300 {
 
+constexpr int TILE_M = 128;   // rows of D per CTA
+constexpr int TILE_N = 256;   // columns of D per CTA (and per CTA pair)
+constexpr int TILE_K16 = 64;  // 16-bit K elements per stage (one 128-byte swizzle row)
+
 // Kernel parameters common to every GEMM kernel (passed by value).
 struct KParams {
     int M, N, K;
@@ -52,7 +56,10 @@ struct F16Config {
     int cta_group;   // 1 or 2
     int out_bf16;    // D is bf16 (else fp32)
     int wide_epi = 0;   // pairs with fp32 D: 8 epilogue warps and one stage fewer (short K)
+    int tile_n = TILE_N;   // pairs: TILE_N or F16_NARROW_N columns per tile
 };
+// the narrower pair tile the fp16/bf16 plans may choose when it fills the waves better
+constexpr int F16_NARROW_N = 224;
 int f16_stages(const F16Config &cfg);
 int f16_smem_bytes(const F16Config &cfg);
 cudaError_t f16_prepare(const F16Config &cfg);   // set the kernel's shared-memory limit
@@ -122,9 +129,6 @@ cudaError_t chain_prepare(int out_bf16);
 cudaError_t chain_launch(int out_bf16, int grid, const CUtensorMap *maps, const ChainParams &p, cudaStream_t stream);
 cudaError_t chain_max_active_clusters(int out_bf16, int *clusters);   // clusters of two CTAs
 
-constexpr int TILE_M = 128;   // rows of D per CTA
-constexpr int TILE_N = 256;   // columns of D per CTA (and per CTA pair)
-constexpr int TILE_K16 = 64;  // 16-bit K elements per stage (one 128-byte swizzle row)
 constexpr int EPI_COLS = 32;  // epilogue chunk width (columns)
 
 }  // namespace gb300

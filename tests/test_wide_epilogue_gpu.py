@@ -1,6 +1,6 @@
 """The wide-epilogue form of the fp16/bf16 CTA-pair kernel (8 epilogue warps, 5 stages),
-which a plan chooses for fp32 D, whole tiles (no split-K or stream-K: the shapes below fill the
-pairs or have fewer than 8 k-blocks) and at most 40 k-blocks: the choice itself (seen as
+which a plan chooses for fp32 D, 256-column tiles, whole tiles (no split-K or stream-K: the shapes
+below fill the pairs or have fewer than 8 k-blocks) and at most 40 k-blocks: the choice itself (seen as
 the plan's ring depth) and parity with the oracle over ragged shapes, C present and absent,
 both storage orders of A and B, and several tiles per CTA pair."""
 import dataclasses
@@ -18,9 +18,9 @@ PAIRS = gemm.GEMM_FLAG_FORCE_2CTA
 
 
 @pytest.mark.parametrize("base,M,N,K,a_row,b_row,c_none", [
-    (F16_NORM, 1000, 1040, 392, True, False, False),      # ragged M, N, K (K % 64 == 8), one wave
+    (F16_NORM, 2000, 2300, 392, True, False, False),      # ragged M, N, K (K % 64 == 8), one wave
     (BF16_UNI, 2048, 2304, 2560, True, False, False),     # 40 k-blocks: the longest K that takes it
-    (F16_NORM, 2560, 776, 1032, True, False, True),       # C absent
+    (F16_NORM, 4000, 1000, 1032, True, False, True),      # C absent
     (BF16_UNI, 1536, 1024, 264, False, True, False),      # column-major A, row-major B
     (F16_NORM, 4096, 4608, 192, True, False, False),      # 288 tiles: several per pair, 3 k-blocks
 ])
@@ -28,7 +28,8 @@ def test_wide_epilogue_parity(base, M, N, K, a_row, b_row, c_none):
     w = dataclasses.replace(synth.scaled(base, M, N, K), a_row_major=a_row, b_row_major=b_row)
     x, D, info, st, intact = gpucase.run(w, flags=PAIRS, c_none=c_none, guard=1024)
     assert st == gemm.GEMM_OK and intact
-    assert info["cta_group"] == 2 and info["stages"] == 5 and info["splits"] == 1 and info["stream_k"] == 0
+    assert info["cta_group"] == 2 and info["tile_n"] == 256
+    assert info["stages"] == 5 and info["splits"] == 1 and info["stream_k"] == 0
     gpucase.check_full(w, x, D, c_none=c_none)
 
 
