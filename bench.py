@@ -39,15 +39,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture
 # summarised in profiles/; valid only for the kernel sources the capture ran on
 MEASURED_TRAFFIC = {
-    "bf16_8192x8192x8192_bf16out": {"bytes": 1138562560 + 123100928, "src": "a476c8ed04fa1cf9",
+    "bf16_8192x8192x8192_bf16out": {"bytes": 1137170944 + 123108096, "src": "8f6015435e6b220b",
                                     "ncu": "profiles/gemm_tc_kernel_bf16_8192x8192x8192_bf16out_launches.md"},
-    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 676302080 + 235404032, "src": "078fa9d8bf7a0756",
+    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 676801792 + 235089664, "src": "083c41a4786c20e0",
                                           "ncu": "profiles/gemm_tc_kernel_mxf8_8192x8192x8192_launches.md"},
-    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 482768384 + 216126976, "src": "d1108a59d87a4cc5",
+    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 483997440 + 216198400, "src": "0ed5066fc605b36e",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 494488320 + 218182912, "src": "a0e3647d91deb099",
+    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 495284224 + 218123264, "src": "4e7bcfd32a187340",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312859136 + 12512000, "src": "625b27984023cb94",
+    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312690176 + 12679936, "src": "943e4156866938b5",
                                               "ncu": "profiles/chain_kernel_bf16_32768x4096_256x256_launches.md"},
 }
 
@@ -244,6 +244,31 @@ def workload(args):
 
 # --------------------------------------------------------------- our arm
 
+def timed_e2e(step, flops, world, dev, stream, steps, blocks=3):
+    """End-to-end rate through the host-buffer entry point: `blocks` separately timed blocks of
+    `steps` calls (each copying its inputs up and its result down), after two untimed calls.
+    The host link of this machine is shared with its other GPUs' jobs, and a block that meets
+    their traffic runs at half speed; the value is the median block, and every block is
+    reported beside it."""
+    import torch
+    for _ in range(2):
+        step()
+    vals = []
+    for _ in range(blocks):
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        _, rate = aggregate(e0.elapsed_time(e1) / steps, flops, world)
+        vals.append(round(rate / 1e12, 3))
+    return statistics.median(vals), vals
+
+
 def tensor_rate(w, info, achieved, clock_summary):
     """Per-clock view of the roofline: the tensor-pipe rate probe (after the timed region)
     gives the FLOP per SM clock of the plan's MMA shape; the kernel's TFLOP/s is then set
@@ -332,22 +357,12 @@ def run_ours(args, rank, world, local_rank):
         hSFB = torch.from_numpy(x["SFB"]).pin_memory() if w.block_scaled else None
         hD = torch.empty((w.M, w.N), dtype=d_t).pin_memory()
         e_steps = max(3, min(args.steps, args.e2e_steps))
-        for _ in range(2):
-            plan.run_host(hA, hB, hC, hD, hSFA, hSFB, stream)
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e_steps):
-            plan.run_host(hA, hB, hC, hD, hSFA, hSFB, stream)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        _, e2e_flops = aggregate(e0.elapsed_time(e1) / e_steps, w.flops, world)
+        e2e_value, blocks = timed_e2e(lambda: plan.run_host(hA, hB, hC, hD, hSFA, hSFB, stream), w.flops, world, dev,
+                                  stream, e_steps)
         h2d = x["A"].nbytes + x["B"].nbytes + x["C"].nbytes + \
             (x["SFA"].nbytes + x["SFB"].nbytes if w.block_scaled else 0)
-        e2e = {"value": round(e2e_flops / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(hD.numel() * hD.element_size()), "steps": e_steps}
+        e2e = {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(hD.numel() * hD.element_size()), "steps": e_steps, "blocks": blocks}
 
     peaks, source = load_peaks()
     traffic, traffic_src = (args.traffic, "--traffic") if args.traffic is not None else measured_traffic(w.name)
@@ -449,21 +464,11 @@ def run_ours_chain(args, rank, world, local_rank):
              for k in ("A", "B", "E", "C")}
         hD = torch.empty((w.M, w.N2), dtype=d_t).pin_memory()
         e_steps = max(3, min(args.steps, args.e2e_steps))
-        for _ in range(2):
-            plan.run_host(h["A"], h["B"], h["E"], h["C"], hD, stream)
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e_steps):
-            plan.run_host(h["A"], h["B"], h["E"], h["C"], hD, stream)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        _, e2e_flops = aggregate(e0.elapsed_time(e1) / e_steps, w.flops, world)
+        e2e_value, blocks = timed_e2e(lambda: plan.run_host(h["A"], h["B"], h["E"], h["C"], hD, stream), w.flops, world,
+                                  dev, stream, e_steps)
         h2d = sum(x[k].nbytes for k in ("A", "B", "E", "C"))
-        e2e = {"value": round(e2e_flops / 1e12, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(hD.numel() * hD.element_size()), "steps": e_steps}
+        e2e = {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(hD.numel() * hD.element_size()), "steps": e_steps, "blocks": blocks}
 
     # roofline: the bound is whichever of HBM bytes and tensor FLOPs takes longer at the measured peaks
     peaks, source = load_peaks()
