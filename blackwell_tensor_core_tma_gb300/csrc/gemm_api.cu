@@ -187,12 +187,31 @@ gemm_status encode_maps(gemm_plan *p, const void *A, const void *B, const void *
     return GEMM_OK;
 }
 
+// The column width of an fp16/bf16 CTA-pair tile: 256 x 224 tiles when they fill the
+// persistent rounds of `units` pairs clearly better than 256 x 256 ones.  Estimated
+// efficiency (each factor measured on GB300) = used share of the tile columns x busy share of
+// the rounds (0.89 where stream-K would balance them) x, for 224, the 3.5 % its extra operand
+// bytes per FLOP cost at 8192^3, or, for 256 with fp32 D and short K, the gain of the wide
+// epilogue (+14 % at 16 k-blocks, +3.5 % at 33); 224 must win by 2 %.
+int pair_tile_n(int64_t M, int64_t N, int64_t K, bool f32, int units) {
+    const int64_t tiles_m = (M + 2 * TILE_M - 1) / (2 * TILE_M), kb = (K + TILE_K16 - 1) / TILE_K16;
+    auto eff = [&](int bn) {
+        const int64_t tn = (N + bn - 1) / bn, tiles = tiles_m * tn;
+        const int64_t rounds = (tiles + units - 1) / units;
+        const bool sk = f32 && kb >= 64 && tiles >= units && tiles % units != 0 && tiles < 4 * units;
+        double e = (double)N / (double)(tn * bn);
+        e *= sk ? 0.89 : (double)tiles / (double)(rounds * units);
+        if (bn == F16_NARROW_N) e *= 0.965;
+        else if (f32 && kb <= 40 && 2 * tiles > units) e *= 1.0 + 0.1 * (double)(40 - kb) / 24.0;
+        return e;
+    };
+    return eff(F16_NARROW_N) > 1.02 * eff(TILE_N) ? F16_NARROW_N : TILE_N;
+}
+
 gemm_status configure_f16(gemm_plan *p) {
-    const bool pair_fits = p->M >= 2 * TILE_M;
     int cg = (p->M >= 1024 && p->N >= 1024) ? 2 : 1;
     if (p->flags & GEMM_FLAG_FORCE_1CTA) cg = 1;
     if (p->flags & GEMM_FLAG_FORCE_2CTA) cg = 2;
-    (void)pair_fits;
     F16Config cfg{cg, p->d == GEMM_BF16};
     if (f16_prepare(cfg) != cudaSuccess) return GEMM_ERR_CUDA;
     int units = p->sm_count / cg;
@@ -201,26 +220,10 @@ gemm_status configure_f16(gemm_plan *p) {
         if (f16_max_active_clusters(cfg, &clusters) == cudaSuccess && clusters > 0) units = clusters;
     }
     p->tiles_m = (int)((p->M + TILE_M * cg - 1) / (TILE_M * cg));
-    // pairs: 256 x 224 tiles when they fill the persistent rounds clearly better than 256 x 256
-    // ones.  Estimated efficiency (each factor measured on GB300) = used share of the tile
-    // columns x busy share of the rounds (0.89 where stream-K would balance them) x, for 224,
-    // the 3.5 % its extra operand bytes per FLOP cost at 8192^3, or, for 256 with fp32 D and
-    // short K, the gain of the wide epilogue (+14 % at 16 k-blocks, +3.5 % at 33).  An
-    // N-contiguous B needs whole 64-element atoms per CTA (112 rows are not): it keeps 256.
+    // pairs: 256 x 224 tiles where they fill the persistent rounds clearly better (pair_tile_n);
+    // an N-contiguous B needs whole 64-element atoms per CTA (112 rows are not): it keeps 256
     if (cg == 2 && !p->b_mn) {
-        const int64_t kb = (p->K + TILE_K16 - 1) / TILE_K16;
-        const bool f32 = p->d == GEMM_F32;
-        auto eff = [&](int bn) {
-            const int64_t tn = (p->N + bn - 1) / bn, tiles = (int64_t)p->tiles_m * tn;
-            const int64_t rounds = (tiles + units - 1) / units;
-            const bool sk = f32 && kb >= 64 && tiles >= units && tiles % units != 0 && tiles < 4 * units;
-            double e = (double)p->N / (double)(tn * bn);
-            e *= sk ? 0.89 : (double)tiles / (double)(rounds * units);
-            if (bn == F16_NARROW_N) e *= 0.965;
-            else if (f32 && kb <= 40 && 2 * tiles > units) e *= 1.0 + 0.1 * (double)(40 - kb) / 24.0;
-            return e;
-        };
-        if (eff(F16_NARROW_N) > 1.02 * eff(TILE_N)) {
+        if (pair_tile_n(p->M, p->N, p->K, p->d == GEMM_F32, units) == F16_NARROW_N) {
             cfg.tile_n = F16_NARROW_N;
             if (f16_prepare(cfg) != cudaSuccess) return GEMM_ERR_CUDA;
             int clusters = 0;
@@ -895,6 +898,13 @@ gemm_status gemm_chain_run_host(gemm_plan_t p, const void *A, const void *B, con
 
 // Test hook (declared in include/gb300gemm_testing.h): make the next runs'
 // producer withhold one arrival so that a bounded wait runs out.
+gemm_status gemm_testing_pair_tile_n(int64_t M, int64_t N, int64_t K, gemm_dtype d, int units, int *tile_n) {
+    if (!tile_n || M <= 0 || N <= 0 || K <= 0 || units <= 0 || (d != GEMM_F32 && d != GEMM_BF16))
+        return GEMM_ERR_INVALID_ARG;
+    *tile_n = pair_tile_n(M, N, K, d == GEMM_F32, units);
+    return GEMM_OK;
+}
+
 gemm_status gemm_testing_set_fault(gemm_plan_t p, int fault) {
     if (!p || fault < 0 || fault > 1) return GEMM_ERR_INVALID_ARG;
     p->fault = fault;

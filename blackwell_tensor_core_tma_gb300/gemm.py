@@ -24,7 +24,8 @@ DTYPE = {"f16": GEMM_F16, "bf16": GEMM_BF16, "e4m3": GEMM_E4M3, "f32": GEMM_F32,
 EXPORTS = ["gemm_plan_create", "gemm_run", "gemm_run_host", "gemm_plan_last_status", "gemm_plan_get_info",
            "gemm_plan_set_timeout", "gemm_plan_destroy", "gemm_status_string", "gemm_testing_set_fault",
            "gemm_run_noalloc", "gemm_plan_set_split_k", "gemm_chain_plan_create", "gemm_chain_run",
-           "gemm_chain_run_host", "gemm_plan_set_stream_k", "gemm_measure_tensor_rate"]
+           "gemm_chain_run_host", "gemm_plan_set_stream_k", "gemm_measure_tensor_rate",
+           "gemm_testing_pair_tile_n"]
 
 
 class GemmError(RuntimeError):
@@ -84,6 +85,8 @@ def lib():
         L.gemm_plan_set_stream_k.restype = st
         L.gemm_run_noalloc.argtypes = [i64, i64, i64, st, st, vp, vp, vp, vp, vp, st]
         L.gemm_run_noalloc.restype = st
+        L.gemm_testing_pair_tile_n.argtypes = [i64, i64, i64, st, st, ctypes.POINTER(ctypes.c_int)]
+        L.gemm_testing_pair_tile_n.restype = st
         L.gemm_measure_tensor_rate.argtypes = [st, st, st, i64, ctypes.POINTER(TensorRate)]
         L.gemm_measure_tensor_rate.restype = st
         L.gemm_chain_plan_create.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i64, st, st, ctypes.c_uint]

@@ -136,3 +136,45 @@ def test_tensor_rate_probe_rejects_before_device(lib, args, status):
     import ctypes
     assert lib.gemm_measure_tensor_rate(*args, ctypes.byref(out)) == status
     assert lib.gemm_measure_tensor_rate(gemm.GEMM_BF16, 0, 2, 64, None) == gemm.GEMM_ERR_INVALID_ARG
+
+
+def _tile_rule(M, N, K, f32, units=76):
+    """The pair tile-width rule restated from its definition (column share x round share, 0.89
+    under stream-K, x 0.965 for 224 or the wide-epilogue gain for 256; 224 must win by 2 %)."""
+    tiles_m, kb = -(-M // 256), -(-K // 64)
+
+    def eff(bn):
+        tn = -(-N // bn)
+        tiles = tiles_m * tn
+        rounds = -(-tiles // units)
+        sk = f32 and kb >= 64 and tiles >= units and tiles % units != 0 and tiles < 4 * units
+        e = N / (tn * bn) * (0.89 if sk else tiles / (rounds * units))
+        if bn == 224:
+            e *= 0.965
+        elif f32 and kb <= 40 and 2 * tiles > units:
+            e *= 1.0 + 0.1 * (40 - kb) / 24.0
+        return e
+    return 224 if eff(224) > 1.02 * eff(256) else 256
+
+
+def test_pair_tile_rule_without_device(lib):
+    import ctypes
+    import numpy as np
+    out = ctypes.c_int()
+    # the measured cases: 4096^3 and 4000x3000x2056 take 224; 8192^3, 2048x2560x4096 (both
+    # tilings need stream-K) and 4096x4096x1024 (the wide epilogue) keep 256
+    for (M, N, K, d), want in [((4096, 4096, 4096, gemm.GEMM_F32), 224), ((4000, 3000, 2056, gemm.GEMM_F32), 224),
+                               ((8192, 8192, 8192, gemm.GEMM_BF16), 256), ((2048, 2560, 4096, gemm.GEMM_F32), 256),
+                               ((4096, 4096, 1024, gemm.GEMM_F32), 256), ((4096, 4096, 4096, gemm.GEMM_BF16), 224)]:
+        assert lib.gemm_testing_pair_tile_n(M, N, K, d, 76, ctypes.byref(out)) == gemm.GEMM_OK
+        assert out.value == want, (M, N, K, d)
+    rng = np.random.default_rng(7)
+    for _ in range(2000):
+        M, N, K = (int(v) for v in rng.integers(1, 20000, 3))
+        d = gemm.GEMM_F32 if rng.integers(2) else gemm.GEMM_BF16
+        units = int(rng.integers(1, 160))
+        assert lib.gemm_testing_pair_tile_n(M, N, K, d, units, ctypes.byref(out)) == gemm.GEMM_OK
+        assert out.value == _tile_rule(M, N, K, d == gemm.GEMM_F32, units), (M, N, K, d, units)
+    assert lib.gemm_testing_pair_tile_n(0, 1, 1, gemm.GEMM_F32, 76, ctypes.byref(out)) == gemm.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_testing_pair_tile_n(1, 1, 1, gemm.GEMM_F16, 76, ctypes.byref(out)) == gemm.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_testing_pair_tile_n(1, 1, 1, gemm.GEMM_F32, 76, None) == gemm.GEMM_ERR_INVALID_ARG
