@@ -51,6 +51,7 @@ namespace gb300 {
 //   KIND    operand kind (GemmKind): fp16/bf16, or block-scaled e4m3 (1X),
 //           e2m1 with UE8M0 per 32 (2X) or e2m1 with UE4M3 per 16 (4X)
 //   BN      tile columns (MMA N)
+//   STAGES  depth of the shared-memory operand ring (k-blocks the producer runs ahead)
 //   ACC_BUFS  TMEM accumulators: 2 = the epilogue drains one while the MMA fills
 //             the other; 1 = the epilogue copies the accumulator to registers
 //             and frees it before converting and storing (leaves TMEM columns
