@@ -44,10 +44,14 @@ def _host_run(w, c_none=False, flags=0, reps=1):
     (4096, 1024, 512, "f32"),     # four chunks of 1024 rows
     (3500, 776, 264, "bf16"),     # three whole chunks and a ragged one; ragged N and K
     (2048, 512, 1024, "f32"),     # exactly two chunks
+    (4096, 2904, 1032, "bf16"),   # CTA pairs with 256 x 224 tiles in every chunk
+    (4096, 1024, 512, "bf16"),    # CTA pairs with 256 x 256 tiles, bf16 D
 ])
 def test_pipelined_host_run_matches_oracle(M, N, K, d):
     w = synth.scaled(W["bf16_4096x4096x4096_f32out"], M, N, K, d=d)
     x, (D,), info = _host_run(w)
+    if (M, N) == (4096, 2904) and info["grid"] == 152:
+        assert info["cta_group"] == 2 and info["tile_n"] == 224
     rows, cols = gpucase.sample_entries(w.M, w.N, info["tile_m"], info["tile_n"], n_random=8192)
     gpucase.check_entries(w, x, D, rows, cols)
 
