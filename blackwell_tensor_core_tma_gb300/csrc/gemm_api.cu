@@ -542,12 +542,15 @@ void pipe_destroy(gemm_plan *p) {
     }
 }
 
-// The fp16/bf16 kernel on rows [0, rows) of device operands A, C, D (whole tiles, no split-K)
-gemm_status launch_rows(gemm_plan *p, const void *A, const void *B, const void *C, void *D, int64_t rows,
-                        cudaStream_t stream) {
+// The plan's kernel on rows [0, rows) of device operands A, C, D (and, block-scaled, the
+// same rows of SFA with all of SFB): whole tiles, no split-K or stream-K
+gemm_status launch_rows(gemm_plan *p, const void *A, const void *B, const void *C, void *D, const uint8_t *SFA,
+                        const uint8_t *SFB, int64_t rows, cudaStream_t stream) {
     CUtensorMap maps[NUM_MAPS];
     std::memset(maps, 0, sizeof maps);
     if (!encode_operand_maps(p, maps, A, B, C, D, rows)) return GEMM_ERR_CUDA;
+    maps[4] = p->maps[4];                 // packed-scale workspaces (block-scaled plans)
+    maps[5] = p->maps[5];
     const int cg = p->cta_group;
     KParams kp{};
     kp.M = (int)rows;
@@ -565,20 +568,36 @@ gemm_status launch_rows(gemm_plan *p, const void *A, const void *B, const void *
     kp.status = p->status;
     kp.timeout_ns = p->timeout_ns;
     kp.fault = p->fault;
-    kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * cg), (uint32_t)p->tile_n) |
-               ((uint32_t)p->b_mn << 16);
     const int units = kp.num_tiles < p->capacity ? kp.num_tiles : p->capacity;
     LaunchShape shape{cg * units, cg, p->smem};
+    if (p->family != KIND_F16) {
+        const uint32_t tm = (uint32_t)(TILE_M * cg), tn = (uint32_t)p->tile_n;
+        kp.idesc = p->family == KIND_MXF8 ? idesc_mxf8(tm, tn, 0, 0) | ((uint32_t)p->b_mn << 16)
+                                          : idesc_mxf4(tm, tn, p->family == KIND_NVF4);
+        kp.sfa = p->ws_a;
+        kp.sfb = p->ws_b;
+        const int sfk = (int)((p->K + scale_block(p->family) - 1) / scale_block(p->family));
+        const int n_wg = p->num_kb * (p->sfa_stage_bytes / 512);
+        if (sf_pack(SFA, SFB, p->ws_a, p->ws_b, kp.M, kp.N, sfk, kp.tiles_m * cg, p->tiles_n, p->tile_n, n_wg,
+                    unit_scale(p->family), stream) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        return scaled_family(p->family).launch(cg, p->d == GEMM_BF16, shape, maps, kp, stream) == cudaSuccess
+                   ? GEMM_OK
+                   : GEMM_ERR_CUDA;
+    }
+    kp.idesc = idesc_f16(p->ab == GEMM_BF16 ? 1u : 0u, (uint32_t)(TILE_M * cg), (uint32_t)p->tile_n) |
+               ((uint32_t)p->b_mn << 16);
     F16Config cfg{cg, p->d == GEMM_BF16, p->wide_epi, p->tile_n};
     return f16_launch(cfg, shape, maps, kp, stream) == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-// Host-buffer run as a pipeline over row chunks (fp16/bf16, row-major A, no split-K):
-// B first, then each chunk's rows of A and C go up on one stream, its product runs on a
-// second as soon as they have landed, and its rows of D come back on a third, so that
-// transfers in both directions and the kernels overlap.
-gemm_status run_host_pipelined(gemm_plan *p, const void *A, const void *B, const void *C, void *D, int64_t chunk,
-                               cudaStream_t stream) {
+// Host-buffer run as a pipeline over row chunks (row-major A, no split-K): B (and SFB)
+// first, then each chunk's rows of A, C (and SFA) go up on one stream, its product runs on
+// a second as soon as they have landed (block-scaled: after packing the chunk's scales), and
+// its rows of D come back on a third, so that transfers in both directions and the kernels
+// overlap.  The chunks' kernels share the scale workspaces in stream order.
+gemm_status run_host_pipelined(gemm_plan *p, const void *A, const void *B, const void *C, void *D,
+                               const uint8_t *SFA, const uint8_t *SFB, int64_t chunk, cudaStream_t stream) {
     if (pipe_setup(p) != GEMM_OK) return GEMM_ERR_CUDA;
     const size_t a_row = bytes_of(p->ab, p->K), c_row = (size_t)p->N * 4, d_row = bytes_of(p->d, p->N);
     const size_t b_bytes = bytes_of(p->ab, p->K * p->N);
@@ -592,6 +611,11 @@ gemm_status run_host_pipelined(gemm_plan *p, const void *A, const void *B, const
         cudaStreamWaitEvent(p->pipe_out, p->pipe_entry, 0) != cudaSuccess ||
         cudaMemcpyAsync(p->hB, B, b_bytes, cudaMemcpyHostToDevice, p->pipe_in) != cudaSuccess)
         return GEMM_ERR_CUDA;
+    const bool scaled = p->family != KIND_F16;
+    const size_t sfk = scaled ? (size_t)((p->K + scale_block(p->family) - 1) / scale_block(p->family)) : 0;
+    uint8_t *dSFA = static_cast<uint8_t *>(p->hSFA);
+    if (scaled && cudaMemcpyAsync(p->hSFB, SFB, (size_t)p->N * sfk, cudaMemcpyHostToDevice, p->pipe_in) != cudaSuccess)
+        return GEMM_ERR_CUDA;
     int i = 0;
     for (int64_t r0 = 0; r0 < p->M; r0 += chunk, ++i) {
         const int64_t rows = p->M - r0 < chunk ? p->M - r0 : chunk;
@@ -599,11 +623,14 @@ gemm_status run_host_pipelined(gemm_plan *p, const void *A, const void *B, const
                 cudaSuccess ||
             (C && cudaMemcpyAsync(dC + r0 * c_row, hC + r0 * c_row, rows * c_row, cudaMemcpyHostToDevice,
                                   p->pipe_in) != cudaSuccess) ||
+            (scaled && cudaMemcpyAsync(dSFA + r0 * sfk, SFA + r0 * sfk, rows * sfk, cudaMemcpyHostToDevice,
+                                       p->pipe_in) != cudaSuccess) ||
             cudaEventRecord(p->pipe_in_done[i], p->pipe_in) != cudaSuccess ||
             cudaStreamWaitEvent(p->pipe_comp, p->pipe_in_done[i], 0) != cudaSuccess)
             return GEMM_ERR_CUDA;
-        const gemm_status st = launch_rows(p, dA + r0 * a_row, p->hB, C ? dC + r0 * c_row : nullptr, dD + r0 * d_row,
-                                           rows, p->pipe_comp);
+        const gemm_status st =
+            launch_rows(p, dA + r0 * a_row, p->hB, C ? dC + r0 * c_row : nullptr, dD + r0 * d_row,
+                        scaled ? dSFA + r0 * sfk : nullptr, static_cast<const uint8_t *>(p->hSFB), rows, p->pipe_comp);
         if (st != GEMM_OK) return st;
         if (cudaEventRecord(p->pipe_k_done[i], p->pipe_comp) != cudaSuccess ||
             cudaStreamWaitEvent(p->pipe_out, p->pipe_k_done[i], 0) != cudaSuccess ||
@@ -631,25 +658,27 @@ gemm_status gemm_run_host(gemm_plan_t p, const void *A, const void *B, const voi
             return GEMM_ERR_CUDA;
     }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
-    // fp16/bf16 with row-major A (contiguous row chunks) and room for two or more chunks of
-    // at least 1024 rows: the pipelined form
-    if (p->family == KIND_F16 && !p->a_mn && p->splits == 1) {
+    const size_t sfk = p->family != KIND_F16 ? (size_t)((p->K + scale_block(p->family) - 1) / scale_block(p->family)) : 0;
+    if (p->family != KIND_F16) {
+        if (!SFA || !SFB) return GEMM_ERR_INVALID_ARG;
+        if (!p->hSFA && (cudaMalloc(&p->hSFA, (size_t)p->M * sfk) != cudaSuccess ||
+                         cudaMalloc(&p->hSFB, (size_t)p->N * sfk) != cudaSuccess))
+            return GEMM_ERR_CUDA;
+    }
+    // row-major A (contiguous row chunks), whole tiles, and room for two or more chunks of at
+    // least HOST_MIN_ROWS rows: the pipelined form
+    if (!p->a_mn && p->splits == 1) {
         const int64_t tile = (int64_t)TILE_M * p->cta_group;
         int64_t chunk = (p->M + HOST_CHUNKS - 1) / HOST_CHUNKS;
         chunk = (chunk + tile - 1) / tile * tile;
         if (chunk < HOST_MIN_ROWS) chunk = HOST_MIN_ROWS;
-        if (p->M >= 2 * chunk) return run_host_pipelined(p, A, B, C, D, chunk, stream);
+        if (p->M >= 2 * chunk) return run_host_pipelined(p, A, B, C, D, SFA, SFB, chunk, stream);
     }
     if (cudaMemcpyAsync(p->hA, A, a_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
         cudaMemcpyAsync(p->hB, B, b_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
     if (C && cudaMemcpyAsync(p->hC, C, c_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     if (p->family != KIND_F16) {
-        if (!SFA || !SFB) return GEMM_ERR_INVALID_ARG;
-        const size_t sfk = (size_t)((p->K + scale_block(p->family) - 1) / scale_block(p->family));
-        if (!p->hSFA && (cudaMalloc(&p->hSFA, (size_t)p->M * sfk) != cudaSuccess ||
-                         cudaMalloc(&p->hSFB, (size_t)p->N * sfk) != cudaSuccess))
-            return GEMM_ERR_CUDA;
         if (cudaMemcpyAsync(p->hSFA, SFA, (size_t)p->M * sfk, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
             cudaMemcpyAsync(p->hSFB, SFB, (size_t)p->N * sfk, cudaMemcpyHostToDevice, stream) != cudaSuccess)
             return GEMM_ERR_CUDA;

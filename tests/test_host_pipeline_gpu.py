@@ -69,8 +69,23 @@ def test_plain_host_run_where_the_pipeline_does_not_apply(case):
         w = synth.scaled(W["bf16_4096x4096x4096_f32out"], 1000, 512, 256)
     elif case == "col-major-A":
         w = synth.scaled(W["bf16_4096x4096x4096_f32out"], 4096, 512, 256, a_row_major=False)
-    else:
-        w = synth.scaled(W["mxf8e4m3_8192x8192x8192_c0_f32out"], 4096, 512, 256, c="normal")
+    else:                                   # below two chunks of rows
+        w = synth.scaled(W["mxf8e4m3_8192x8192x8192_c0_f32out"], 1000, 512, 256, c="normal")
+    x, (D,), info = _host_run(w)
+    rows, cols = gpucase.sample_entries(w.M, w.N, info["tile_m"], info["tile_n"], n_random=4096)
+    gpucase.check_entries(w, x, D, rows, cols)
+
+
+@pytest.mark.parametrize("name,M,N,K", [
+    ("mxf8e4m3_8192x8192x8192_c0_f32out", 4096, 512, 256),     # four chunks, single CTAs
+    ("mxf8e4m3_8192x8192x8192_c0_f32out", 3000, 1280, 512),    # CTA pairs, a ragged last chunk
+    ("mxf4e2m1_8192x8192x8192_c0_f32out", 2048, 1024, 1024),   # UE8M0 / 32, exactly two chunks
+    ("nvf4e2m1_8192x8192x8192_c0_f32out", 4096, 1536, 512),    # UE4M3 / 16
+])
+def test_pipelined_block_scaled_host_run(name, M, N, K):
+    """Block-scaled plans from host buffers run as the row-chunk pipeline: each chunk's SFA
+    rows go up with its A and C rows and are packed before its kernel; SFB goes up once."""
+    w = synth.scaled(W[name], M, N, K, c="normal")
     x, (D,), info = _host_run(w)
     rows, cols = gpucase.sample_entries(w.M, w.N, info["tile_m"], info["tile_n"], n_random=4096)
     gpucase.check_entries(w, x, D, rows, cols)
