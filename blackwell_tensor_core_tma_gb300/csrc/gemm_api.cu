@@ -925,8 +925,7 @@ gemm_status gemm_chain_run_host(gemm_plan_t p, const void *A, const void *B, con
     return gemm_plan_last_status(p);
 }
 
-// Test hook (declared in include/gb300gemm_testing.h): make the next runs'
-// producer withhold one arrival so that a bounded wait runs out.
+// Test hook (declared in include/gb300gemm_testing.h): the pair tile-width rule alone.
 gemm_status gemm_testing_pair_tile_n(int64_t M, int64_t N, int64_t K, gemm_dtype d, int units, int *tile_n) {
     if (!tile_n || M <= 0 || N <= 0 || K <= 0 || units <= 0 || (d != GEMM_F32 && d != GEMM_BF16))
         return GEMM_ERR_INVALID_ARG;
@@ -934,6 +933,8 @@ gemm_status gemm_testing_pair_tile_n(int64_t M, int64_t N, int64_t K, gemm_dtype
     return GEMM_OK;
 }
 
+// Test hook (declared in include/gb300gemm_testing.h): make the next runs'
+// producer withhold one arrival so that a bounded wait runs out.
 gemm_status gemm_testing_set_fault(gemm_plan_t p, int fault) {
     if (!p || fault < 0 || fault > 1) return GEMM_ERR_INVALID_ARG;
     p->fault = fault;

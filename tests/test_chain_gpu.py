@@ -82,3 +82,23 @@ def test_chain_timeout_and_recovery():
         torch.cuda.synchronize()
         assert plan.last_status() == gemm.GEMM_OK
     gpucase.check_chain(w, x, gpucase.decode_d(D, w.d))
+
+
+@pytest.mark.parametrize("M,K,N1,N2,d,c_none", [
+    (1000, 520, 200, 136, "bf16", False),     # ragged, bf16 D
+    (640, 1024, 256, 256, "f32", True),       # C absent
+])
+def test_chain_host_run(M, K, N1, N2, d, c_none):
+    """gemm_chain_run_host: the same result from pinned host buffers as from device buffers."""
+    import torch
+    w = synth.scaled_chain(CW, M, N1, N2, K, d=d)
+    x, D_dev, info, st, intact = gpucase.run_chain(w, c_none=c_none)
+    assert st == gemm.GEMM_OK
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).pin_memory()
+    hD = torch.full((M, N2), float("nan"), dtype=torch.bfloat16 if d == "bf16" else torch.float32).pin_memory()
+    with gemm.ChainPlan(M, N1, N2, K, w.ab, d) as plan:
+        assert plan.run_host(pin(x["A"]), pin(x["B"]), pin(x["E"]), None if c_none else pin(x["C"]), hD,
+                             torch.cuda.current_stream()) == gemm.GEMM_OK
+    D_host = gpucase.decode_d(hD, d)
+    assert np.array_equal(D_host, D_dev)
+    gpucase.check_chain(w, x, D_host, c_none=c_none)
