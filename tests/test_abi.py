@@ -178,3 +178,16 @@ def test_pair_tile_rule_without_device(lib):
     assert lib.gemm_testing_pair_tile_n(0, 1, 1, gemm.GEMM_F32, 76, ctypes.byref(out)) == gemm.GEMM_ERR_INVALID_ARG
     assert lib.gemm_testing_pair_tile_n(1, 1, 1, gemm.GEMM_F16, 76, ctypes.byref(out)) == gemm.GEMM_ERR_INVALID_ARG
     assert lib.gemm_testing_pair_tile_n(1, 1, 1, gemm.GEMM_F32, 76, None) == gemm.GEMM_ERR_INVALID_ARG
+
+
+def test_product_code_does_not_reach_the_oracle():
+    """The package (binding, builders, CUDA sources) neither imports nor links the CPU oracle;
+    only tests, smoke() and the bench's CPU legs may use it."""
+    pkg = os.path.join(ROOT, "blackwell_tensor_core_tma_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if not f.endswith((".py", ".cu", ".cuh", ".h", ".c")):
+                continue
+            text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+            assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+            assert "liboracle" not in text and "gemm_oracle" not in text, f
