@@ -806,13 +806,8 @@ gemm_status gemm_chain_plan_create(gemm_plan_t *out, int64_t M, int64_t N1, int6
     p->tiles_m = (int)((M + TILE_M - 1) / TILE_M);
     p->tiles_n = 1;
     p->tiles = p->tiles_m;
-    // clusters of two CTAs take neighbouring tiles and share B and E (multicast)
-    int clusters = p->sm_count / 2;
-    int fit = 0;
-    if (chain_max_active_clusters(d == GEMM_BF16, &fit) == cudaSuccess && fit > 0) clusters = fit;
-    const int64_t tile_pairs = (p->tiles + 1) / 2;
-    p->capacity = 2 * clusters;
-    p->grid = 2 * (int)(tile_pairs < clusters ? tile_pairs : clusters);
+    p->capacity = p->sm_count;
+    p->grid = p->tiles < p->sm_count ? p->tiles : p->sm_count;
     p->splits = 1;
     if (cudaMalloc(&p->status, sizeof(int)) != cudaSuccess) {
         delete p;
@@ -837,9 +832,8 @@ gemm_status encode_chain_maps(gemm_plan *p, const void *A, const void *B, const 
     const CUtensorMapDataType dt = tma_dtype(p->ab);
     const uint32_t n1p = (uint32_t)((p->N + 15) / 16 * 16), n2p = (uint32_t)p->tile_n;
     bool ok = encode_2d(&p->maps[0], dt, 2, A, p->K, p->M, TILE_K16, TILE_M, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              // B and E: boxes of half the rows, one half loaded (and multicast) by each CTA of a cluster
-              encode_2d(&p->maps[1], dt, 2, B, p->K, p->N, TILE_K16, n1p / 2, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_2d(&p->maps[4], dt, 2, E, p->N, p->N2, TILE_K16, n2p / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+              encode_2d(&p->maps[1], dt, 2, B, p->K, p->N, TILE_K16, n1p, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode_2d(&p->maps[4], dt, 2, E, p->N, p->N2, TILE_K16, n2p, CU_TENSOR_MAP_SWIZZLE_128B);
     if (ok && C)
         ok = encode_2d(&p->maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, p->N2, p->M, EPI_COLS, 32,
                        CU_TENSOR_MAP_SWIZZLE_128B);

@@ -7,14 +7,7 @@
 //     D = C + P·E    tcgen05.mma with A = P read from TMEM and E from shared memory,
 //                    fp32 accumulator in TMEM columns [256, 512)
 // so the intermediate never leaves the SM.  One CTA owns a 128-row tile at a
-// time and walks the tiles persistently, in clusters of two: the CTAs of a cluster
-// take neighbouring tiles, step through the same K blocks together, and share B
-// and E, which every tile reads whole — each CTA loads one half of a stage's B (or
-// E) rows and multicasts it into both CTAs' shared memory, so a tile draws A and
-// half of B from L2 instead of A and all of B.  A stage is consumed when both CTAs'
-// MMAs have read it (each MMA thread's commit arrives on both CTAs' empty barrier).
-// A cluster whose second tile lies past M computes zeros (A's box is read as zero
-// fill) and stores nothing.  Warp roles (192 threads):
+// time and walks the tiles persistently.  Warp roles (192 threads):
 //   warp 0     TMA producer: per tile the K blocks of A and B, then the K blocks
 //              of E, through one STAGES-deep ring (a stage holds A 128 x 64 and
 //              B N1 x 64, or E N2 x 64; 128-byte swizzled rows).
@@ -66,8 +59,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const int pair0 = blockIdx.x / 2, pair_step = gridDim.x / 2;   // tiles 2 * pair + rank
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);
     uint64_t *full = bars;
@@ -90,7 +81,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         if (p.has_c) prefetch_tensormap(&tmC);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 2);      // both CTAs' MMAs have read the stage
+            mbar_init(&empty[s], 1);
         }
         mbar_init(tfull, 1);
         mbar_init(pready, 4);
@@ -106,7 +97,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         tmem_relinquish<1>();
     }
     tc_fence_before_sync();
-    cluster_sync();                       // the peer's barriers exist before anything targets them
+    __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -116,34 +107,23 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            const int h1 = p.n1p / 2, h2 = p.n2p / 2;   // B / E rows this CTA loads for both
-            for (int pt = pair0; ok && 2 * pt < p.tiles; pt += pair_step) {
-                const int m0 = (2 * pt + (int)rank) * TILE_M;
+            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+                const int m0 = t * TILE_M;
                 for (int kb = 0; kb < p.num_kb1 + p.num_kb2; ++kb) {
-                    // both CTAs' MMAs have finished with the stage: this CTA's half of B or E
-                    // may land in either
                     if (!W.wait(&empty[s], ph ^ 1u)) { ok = false; break; }
-                    const bool withhold = p.fault == 1 && pt == pair0 && kb == 0;
+                    const bool withhold = p.fault == 1 && t == (int)blockIdx.x && kb == 0;
                     uint8_t *st = smem + s * Cfg::STAGE_BYTES;
                     const uint32_t fb = smem_addr(&full[s]);
                     if (kb < p.num_kb1) {         // A rows m0.., B rows 0..n1p of K block kb
                         if (!withhold) mbar_arrive_expect_tx(&full[s], Cfg::A_BYTES + p.n1p * 128);
                         tma_load_2d(smem_addr(st), &tmA, fb, kb * Cfg::BK, m0);
-                        tma_load_2d_multicast(smem_addr(st + Cfg::A_BYTES + (int)rank * h1 * 128), &tmB, fb,
-                                              kb * Cfg::BK, (int)rank * h1, 0x3);
+                        tma_load_2d(smem_addr(st + Cfg::A_BYTES), &tmB, fb, kb * Cfg::BK, 0);
                     } else {                      // E rows 0..n2p of K block kb - num_kb1
                         mbar_arrive_expect_tx(&full[s], p.n2p * 128);
-                        tma_load_2d_multicast(smem_addr(st + (int)rank * h2 * 128), &tmE, fb,
-                                              (kb - p.num_kb1) * Cfg::BK, (int)rank * h2, 0x3);
+                        tma_load_2d(smem_addr(st), &tmE, fb, (kb - p.num_kb1) * Cfg::BK, 0);
                     }
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
-            }
-            // tail: the last use of every stage has been released by both CTAs, so no
-            // commit from the peer is still on its way to this CTA's barriers at exit
-            for (int i = 0; ok && i < STAGES; ++i) {
-                if (!W.wait(&empty[s], ph ^ 1u)) break;
-                if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
         }
     } else if (warp == 1) {
@@ -154,7 +134,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int s = 0;
             uint32_t ph = 0, it = 0;
             bool ok = true;
-            for (int pt = pair0; ok && 2 * pt < p.tiles; pt += pair_step, ++it) {
+            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x, ++it) {
                 // T's columns are free once the previous tile's second product (which read
                 // P from them) has completed
                 if (it > 0 && !W.wait(dfull, (it - 1) & 1u)) break;
@@ -168,7 +148,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < Cfg::BK / 16; ++k)   // 32 bytes of K = 2 descriptor units
                         mma_f16<1>(t_tmem, ad + 2 * k, bd + 2 * k, p.idesc1, (kb != 0) | (k != 0));
-                    tc_commit_multicast(smem_addr(&empty[s]), 0x3);
+                    tc_commit<1>(smem_addr(&empty[s]));
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
@@ -185,7 +165,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         const int kk = j * Cfg::BK + 16 * k;   // K index of the second product
                         if (kk < p.n1p) mma_f16_ts(d_tmem, t_tmem + kk / 2, ed + 2 * k, p.idesc2, kk != 0);
                     }
-                    tc_commit_multicast(smem_addr(&empty[s]), 0x3);
+                    tc_commit<1>(smem_addr(&empty[s]));
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
@@ -209,8 +189,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // ec % 2, and its C load is that buffer's (ec / 2)-th
         uint32_t it = 0, ec = 0;
         bool ok = true;
-        for (int pt = pair0; ok && 2 * pt < p.tiles; pt += pair_step, ++it) {
-            const int m_warp = (2 * pt + (int)rank) * TILE_M + 32 * q;
+        for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x, ++it) {
+            const int m_warp = t * TILE_M + 32 * q;
             // P = round(T): chunk c of 32 fp32 columns becomes 16 columns of packed pairs at
             // column 16c, over columns whose T values this warp has already read
             if (!__all_sync(0xffffffffu, W.wait(tfull, it & 1u))) break;
@@ -317,7 +297,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int i = 0; i < 64; ++i) __nanosleep(1000);
     }
     tc_fence_before_sync();
-    cluster_sync();                       // the peer's last arrivals on this CTA's barriers have landed
+    __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<1>(tmem_base, 512);
@@ -325,28 +305,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 }
 
 template <bool OUT_BF16>
-cudaLaunchConfig_t chain_config(int grid, cudaStream_t stream, cudaLaunchAttribute *attr) {
-    cudaLaunchConfig_t lc = {};
-    lc.gridDim = dim3(grid, 1, 1);
-    lc.blockDim = dim3(ChainCfg<OUT_BF16>::THREADS, 1, 1);
-    lc.dynamicSmemBytes = ChainCfg<OUT_BF16>::SMEM_BYTES;
-    lc.stream = stream;
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    lc.attrs = attr;
-    lc.numAttrs = 1;
-    return lc;
-}
-
-template <bool OUT_BF16>
 cudaError_t launch_chain(int grid, const CUtensorMap *maps, const ChainParams &p, cudaStream_t stream) {
-    cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t lc = chain_config<OUT_BF16>(grid, stream, attr);
-    void *args[6] = {(void *)&maps[0], (void *)&maps[1], (void *)&maps[2], (void *)&maps[3], (void *)&maps[4],
-                     (void *)&p};
-    return cudaLaunchKernelExC(&lc, reinterpret_cast<const void *>(&chain_kernel<ChainCfg<OUT_BF16>>), args);
+    using Cfg = ChainCfg<OUT_BF16>;
+    chain_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -361,15 +323,6 @@ cudaError_t chain_prepare(int out_bf16) {
 
 cudaError_t chain_launch(int out_bf16, int grid, const CUtensorMap *maps, const ChainParams &p, cudaStream_t stream) {
     return out_bf16 ? launch_chain<true>(grid, maps, p, stream) : launch_chain<false>(grid, maps, p, stream);
-}
-
-cudaError_t chain_max_active_clusters(int out_bf16, int *clusters) {
-    cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t lc = out_bf16 ? chain_config<true>(2 * 1024, nullptr, attr)
-                                           : chain_config<false>(2 * 1024, nullptr, attr);
-    const void *fn = out_bf16 ? reinterpret_cast<const void *>(&chain_kernel<ChainCfg<true>>)
-                              : reinterpret_cast<const void *>(&chain_kernel<ChainCfg<false>>);
-    return cudaOccupancyMaxActiveClusters(clusters, fn, &lc);
 }
 
 }  // namespace gb300

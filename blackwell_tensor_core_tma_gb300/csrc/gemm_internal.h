@@ -127,7 +127,6 @@ constexpr int CHAIN_MAX_N = 256;   // N1 and N2 limits: both products' accumulat
 int chain_smem_bytes();
 cudaError_t chain_prepare(int out_bf16);
 cudaError_t chain_launch(int out_bf16, int grid, const CUtensorMap *maps, const ChainParams &p, cudaStream_t stream);
-cudaError_t chain_max_active_clusters(int out_bf16, int *clusters);   // clusters of two CTAs
 
 constexpr int EPI_COLS = 32;  // epilogue chunk width (columns)
 

@@ -113,18 +113,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// Same, multicast: the box lands at offset `dst` in the shared memory of every CTA
-// of `cta_mask` in the cluster, and each completes its transaction bytes on the
-// barrier at offset `mbar` of its own shared memory.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *m, uint32_t mbar, int32_t c0,
-                                                      int32_t c1, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(m), "r"(mbar), "r"(c0), "r"(c1), "h"(cta_mask)
-        : "memory");
-}
-
 // 1-D bulk copy GMEM -> own SMEM (16-byte aligned addresses, size % 16 == 0)
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t mbar) {
     asm volatile(
@@ -314,16 +302,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
     else
         asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                      : "memory");
-}
-
-// single-CTA MMAs, multicast completion: arrive once on the barrier at the same
-// offset in every CTA of `cta_mask` when this thread's prior tcgen05 ops complete
-__device__ __forceinline__ void tc_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"(cta_mask)
-        : "memory");
 }
 
 // pair form: arrive on the barrier at the same offset in every CTA of `cta_mask`
