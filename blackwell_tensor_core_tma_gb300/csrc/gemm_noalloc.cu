@@ -103,7 +103,9 @@ extern "C" gemm_status gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dt
     gemm_status st = setup(dev, &s);
     if (st != GEMM_OK) return st;
 
-    // same kernel choice as a plan without flags
+    // the CTA mode a plan without flags would choose, but always 128 x 256 (single CTA) or
+    // 256 x 256 (pair) tiles, the 4-warp epilogue, groups of 8 pair tiles (16 single-CTA
+    // tiles) and no split-K or stream-K: a plan may pick other forms of the kernel
     const int cg = (M >= 1024 && N >= 1024) ? 2 : 1;
     const F16Config cfg{cg, d == GEMM_BF16};
     CUtensorMap maps[NUM_MAPS];
@@ -138,6 +140,13 @@ extern "C" gemm_status gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dt
     LaunchShape shape{cg * (kp.num_tiles < units ? kp.num_tiles : units), cg, f16_smem_bytes(cfg)};
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
+    if (wait) {
+        // waiting would synchronise a stream that is being captured into a graph, which
+        // fails and invalidates the capture: refuse before enqueueing anything
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (cs != cudaStreamCaptureStatusNone) return GEMM_ERR_INVALID_ARG;
+    }
     // the array keeps the previous call's status: it must start at zero
     if (cudaMemsetAsync(s->status, 0, kStatusBytes, stream) != cudaSuccess) return GEMM_ERR_CUDA;
     if (f16_launch(cfg, shape, maps, kp, stream) != cudaSuccess) return GEMM_ERR_CUDA;

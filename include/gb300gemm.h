@@ -226,12 +226,23 @@ gemm_status gemm_plan_destroy(gemm_plan_t p);
  * than the array holds would be rejected with GEMM_ERR_INVALID_ARG.
  *
  * Arguments mean what they mean for gemm_plan_create + gemm_run with
- * a_row_major = 1, b_row_major = 0, c = GEMM_F32, no flags (the same kernel
- * is chosen): ab is GEMM_F16 or GEMM_BF16, d is GEMM_F32 or GEMM_BF16, C may
- * be NULL.  The caller owns and passes every input and output.  With
- * wait = 0 the call returns after enqueueing; with wait != 0 it synchronises
- * cuda_stream and returns the kernel's status (GEMM_ERR_TIMEOUT if a bounded
- * wait ran out).
+ * a_row_major = 1, b_row_major = 0, c = GEMM_F32 and no flags: ab is GEMM_F16
+ * or GEMM_BF16, d is GEMM_F32 or GEMM_BF16, C may be NULL.  The caller owns
+ * and passes every input and output.  The kernel takes the CTA mode such a
+ * plan would (CTA pairs when M >= 1024 and N >= 1024), but always with
+ * 128 x 256 (single CTA) or 256 x 256 (pair) tiles, the 4-warp epilogue and
+ * no split-K or stream-K; a plan may choose 256 x 224 pair tiles, the 8-warp
+ * epilogue, split-K or stream-K instead, so results can differ from
+ * gemm_run's in the order of the fp32 sums (both meet the same accuracy
+ * bound) and in speed.
+ *
+ * With wait = 0 the call returns after enqueueing and the kernel's status is
+ * not reported: a GEMM_ERR_TIMEOUT stays in the array until the next call
+ * clears it.  With wait != 0 it synchronises cuda_stream and returns the
+ * kernel's status (GEMM_ERR_TIMEOUT if a bounded wait ran out); that
+ * synchronisation is not allowed on a stream being captured into a graph,
+ * so wait != 0 on a capturing stream returns GEMM_ERR_INVALID_ARG before
+ * anything is enqueued.
  *
  * The first call on a device does a one-time set-up there (it looks up the
  * array's device address with cudaGetSymbolAddress and sets the kernel's

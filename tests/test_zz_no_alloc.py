@@ -63,6 +63,56 @@ def test_two_calls_in_a_row_match_gemm_run():
         assert np.all(np.abs(D_free - D_ref) <= tol)
 
 
+def test_enqueue_only_call_then_waiting_call_on_one_stream():
+    """A caller on a latency-critical path enqueues without waiting (wait = 0); the next call
+    on the same stream waits.  Its clearing of the shared status word is ordered after the
+    first kernel by the stream, so both products come out right and the second call reports
+    the status of its own kernel."""
+    import torch
+    cases = [
+        _setup(synth.scaled(synth.WORKLOADS["bf16_4096x4096x4096_f32out"], 1040, 1280, 776), False),
+        _setup(synth.scaled(synth.WORKLOADS["f16_4000x3000x2056_f32out"], 700, 264, 1112), True),
+    ]
+    stream = torch.cuda.current_stream()
+    for k, wait in zip(cases, (0, 1)):
+        w = k["w"]
+        st = gemm.gemm_run_noalloc(w.M, w.N, w.K, w.ab, w.d, k["A"], k["B"], k["C"], k["D_free"], stream,
+                                   wait=wait)
+        assert st == gemm.GEMM_OK
+    torch.cuda.synchronize()
+    for k in cases:
+        w, x, c_none = k["w"], k["x"], k["c_none"]
+        D_plan = gpucase.decode_d(k["D_plan"], w.d)
+        D_free = gpucase.decode_d(k["D_free"], w.d)
+        D_ref, S = oracle.gemm(x["A"], x["B"], None if c_none else x["C"], w.M, w.N, w.K, w.ab)
+        c = np.zeros_like(S) if c_none else x["C"].astype(np.float64)
+        tol = gpucase.tolerance(w, D_ref, S, c)
+        assert np.all(np.abs(D_free - D_plan) <= tol)
+        assert np.all(np.abs(D_free - D_ref) <= tol)
+
+
+def test_waiting_call_is_refused_on_a_capturing_stream():
+    """Synchronising inside a graph capture would break the capture: a waiting call on a
+    capturing stream is refused before anything is enqueued, and the capture stays valid."""
+    import torch
+    w = synth.scaled(synth.WORKLOADS["bf16_4096x4096x4096_f32out"], 256, 256, 256)
+    x = synth.make_inputs(w)
+    A, B = gpucase.to_device(x["A"]), gpucase.to_device(x["B"])
+    D = torch.empty((w.M, w.N), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    # the device's one-time set-up happens outside the capture
+    assert gemm.gemm_run_noalloc(w.M, w.N, w.K, w.ab, w.d, A, B, None, D, s, wait=1) == gemm.GEMM_OK
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        try:
+            with pytest.raises(gemm.GemmError) as e:
+                gemm.gemm_run_noalloc(w.M, w.N, w.K, w.ab, w.d, A, B, None, D, s, wait=1)
+        finally:
+            g.capture_end()
+    assert e.value.status == gemm.GEMM_ERR_INVALID_ARG
+
+
 def test_rejects_bad_arguments_without_launching():
     with pytest.raises(gemm.GemmError) as e:
         gemm.gemm_run_noalloc(0, 256, 256, "bf16", "f32", 16, 16, None, 16)
