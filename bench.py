@@ -269,24 +269,59 @@ def timed_e2e(step, flops, world, dev, stream, steps, blocks=3):
     return statistics.median(vals), vals
 
 
-def tensor_rate(w, info, achieved, clock_summary):
+def tensor_rate(w, info, achieved, clock_summary, kernel_mhz=None):
     """Per-clock view of the roofline: the tensor-pipe rate probe (after the timed region)
     gives the FLOP per SM clock of the plan's MMA shape; the kernel's TFLOP/s is then set
-    against that rate at the maximum SM clock and at the clock sampled while it ran.  The
-    probe's operands are zero, so its own clock (and TFLOP/s) sits above what real data
-    draws under the power limit; the per-clock rate does not depend on the clock."""
+    against that rate at the maximum SM clock and at the SM clock the kernel itself ran at
+    (the plan's clock meter: every CTA's clock64 cycles over its globaltimer nanoseconds,
+    summed over the timed launches; nvidia-smi's median is the fallback).  The probe's
+    operands are hashed values of ordinary magnitude; the per-clock rate does not depend
+    on the clock."""
     from blackwell_tensor_core_tma_gb300 import gemm
     r = gemm.gemm_measure_tensor_rate(w.ab, w.block_scaled, info["cta_group"], 8192)
     per_clk, sms = r["flop_per_clk_per_sm"], info["sm_count"]
     max_mhz = clock_summary.get("sm_max_mhz") or 2070.0
     at_max = sms * per_clk * max_mhz * 1e6 / 1e12
-    run_mhz = clock_summary.get("sm_mhz")
+    run_mhz = kernel_mhz or clock_summary.get("sm_mhz")
     at_run = sms * per_clk * run_mhz * 1e6 / 1e12 if run_mhz else None
     return {"flop_per_clk_per_sm": round(per_clk, 1), "probe_sm_mhz": round(r["sm_mhz"], 1),
             "probe_tflops": round(r["tflops"], 1), "peak_at_max_clock": round(at_max, 1),
             "max_mhz": max_mhz, "frac_at_max_clock": round(achieved / at_max, 4),
+            "run_mhz": round(run_mhz, 1) if run_mhz else None,
             "frac_at_run_clock": round(achieved / at_run, 4) if at_run else None,
-            "run_clock_source": "nvidia-smi median over the timed region"}
+            "run_clock_source": ("the kernel's own SM clock over the timed launches (clock meter: clock64 / "
+                                 "globaltimer per CTA)") if kernel_mhz else "nvidia-smi median over the timed region"}
+
+
+def trace_summary(tr, info, steps, w):
+    """Per-role clock accounting of a trace build, per launch: where the MMA issuer's
+    cycles go per k-block, and the epilogue's per piece."""
+    import numpy as np
+
+    from blackwell_tensor_core_tma_gb300 import gemm
+    F = {n: i for i, n in enumerate(gemm.TRACE_FIELDS)}
+    t = tr.reshape(info["grid"], -1).astype(np.float64) / steps
+    lead = t[:, F["mma_kblocks"]] > 0
+    kb = t[lead, F["mma_kblocks"]].sum()
+    col = lambda n: t[:, F[n]]
+    per_kb = lambda n: round(float(col(n)[lead].sum() / kb), 1)
+    epi = col("epi_pieces").sum()
+    out = {
+        "launches": steps, "leader_ctas": int(lead.sum()), "kblocks_per_leader": round(float(kb / lead.sum()), 2),
+        "kernel_mhz": round(float(col("kernel_clk").sum() / col("kernel_ns").sum() * 1e3), 1),
+        "clk_per_kblock": round(float((col("kernel_clk")[lead] / col("mma_kblocks")[lead]).mean()), 1),
+        "mma_per_kblock": {n: per_kb("mma_" + n) for n in ("wait_ab", "wait_sf", "wait_acc", "issue")},
+        "mma_first_clk": round(float(col("mma_first")[lead].mean()), 0),
+        "mma_tail_clk": round(float((col("kernel_clk") - col("mma_end"))[lead].mean()), 0),
+        "prod_per_stage": {n: round(float(col("prod_" + n).sum() / col("prod_stages").sum()), 1)
+                           for n in ("wait", "issue")},
+        "epi_per_piece_per_warp": {n: round(float(col("epi_" + n).sum() / max(epi, 1)), 1)
+                                   for n in ("wait_acc", "tmem_ld", "wait_c", "store")},
+        "epi_end_clk": round(float(col("epi_end").max()), 0),
+    }
+    if w.block_scaled:
+        out["copier_per_kblock"] = {n: per_kb("cp_" + n) for n in ("wait", "issue")}
+    return out
 
 
 def run_ours(args, rank, world, local_rank):
@@ -329,6 +364,12 @@ def run_ours(args, rank, world, local_rank):
     # per-launch events on the launching stream give the kernel's duration
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    trace_buf = None
+    if args.trace:
+        slots = gemm.gemm_testing_trace_slots()
+        trace_buf = torch.zeros(info["grid"] * slots, dtype=torch.int64, device=dev)
+        gemm.gemm_testing_set_trace(plan.handle, trace_buf, trace_buf.numel() * 8)
+    plan.set_clock_meter(True)               # the kernel's own SM clock over the timed launches
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(smi_index(local_rank)) as clocks:
@@ -342,6 +383,12 @@ def run_ours(args, rank, world, local_rank):
     barrier(world)
     if plan.last_status() != gemm.GEMM_OK:
         raise RuntimeError("kernel reported a timeout in the timed region")
+    meter = plan.read_clock_meter()
+    plan.set_clock_meter(False)
+    trace = None
+    if trace_buf is not None:
+        gemm.gemm_testing_set_trace(plan.handle, None, 0)
+        trace = trace_summary(trace_buf.cpu().numpy(), info, args.steps, w)
     local_ms = t0.elapsed_time(t1) / args.steps
     kernel_ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
     max_ms, flops_per_s = aggregate(local_ms, w.flops, world)
@@ -380,8 +427,9 @@ def run_ours(args, rank, world, local_rank):
                 "kernel": "gemm_tc_kernel",
                 "kernel_ms": round(kernel_ms, 5)}
     clock_summary = clocks.summary()
+    clock_summary["kernel_sm_mhz"] = round(meter["sm_mhz"], 1) if meter["sm_mhz"] else None
     if not args.no_probe:
-        roofline["tensor_rate"] = tensor_rate(w, info, achieved, clock_summary)
+        roofline["tensor_rate"] = tensor_rate(w, info, achieved, clock_summary, meter["sm_mhz"] or None)
 
     out = {
         "metric": "GEMM TFLOP/s and % of GB300 dense tensor peak (bf16 8192^3), vs CPU oracle",
@@ -400,6 +448,9 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": args.steps * info["launches_per_run"],
         "clocks": clock_summary,
     }
+    if trace is not None:
+        out["trace"] = trace
+        out["library"] = "trace build (GB300_TRACE=1): timings include the counters' cost"
     plan.close()
     if rank == 0 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(w, x, args.cpu_seconds)
@@ -665,9 +716,18 @@ def main(argv=None):
     ap.add_argument("--reference-seconds", type=float, default=120.0)
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
+    ap.add_argument("--trace", action="store_true",
+                    help="load the trace build of the library (GB300_TRACE=1, built if needed) and add the "
+                         "kernels' per-role clock accounting to the line (GEMM workloads; a diagnostic run)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.trace:
+        if args.workload in synth.CHAIN_WORKLOADS:
+            ap.error("--trace covers the GEMM kernels, not the chain")
+        from blackwell_tensor_core_tma_gb300 import build as _libbuild
+        _libbuild.build(variant="trace")
+        os.environ["GB300GEMM_VARIANT"] = "trace"
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         if rank != 0:

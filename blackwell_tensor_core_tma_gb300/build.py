@@ -3,6 +3,11 @@
 Each translation unit under csrc/ compiles in parallel to an object file,
 then nvcc links them (with the static CUDA runtime) into a shared library
 next to this file.  Nothing is installed anywhere else.
+
+Variant "trace" (libgb300gemm_trace.so, compiled with GB300_TRACE=1) keeps the
+kernels' per-role clock counters (gemm_testing_set_trace); the default library
+compiles them out.  The binding loads the variant named by the environment
+variable GB300GEMM_VARIANT (unset: the default library).
 """
 
 from __future__ import annotations
@@ -18,6 +23,13 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libgb300gemm.so")
+VARIANTS = {"": [], "trace": ["-DGB300_TRACE=1"]}
+
+
+def lib_path(variant: str = "") -> str:
+    if variant not in VARIANTS:
+        raise ValueError(f"unknown library variant {variant!r} (known: {sorted(VARIANTS)})")
+    return LIB if not variant else os.path.join(HERE, f"libgb300gemm_{variant}.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -40,18 +52,20 @@ def _inputs() -> list[str]:
         glob.glob(os.path.join(ROOT, "include", "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(variant: str = "") -> bool:
+    out = lib_path(variant)
+    if not os.path.exists(out):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(out)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    if not force and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None, variant: str = "") -> str:
+    target = lib_path(variant)
+    if not force and up_to_date(variant):
+        return target
     cc = nvcc()
-    extra = list(extra or [])
+    extra = VARIANTS[variant] + list(extra or [])
     with tempfile.TemporaryDirectory(prefix="gb300gemm_") as tmp:
         def compile_one(src):
             obj = os.path.join(tmp, os.path.basename(src) + ".o")
@@ -70,13 +84,14 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc link failed:\n{r.stderr}")
-        staged = LIB + ".tmp"
+        staged = target + ".tmp"
         shutil.copyfile(out, staged)
-        os.replace(staged, LIB)
-    return LIB
+        os.replace(staged, target)
+    return target
 
 
 if __name__ == "__main__":
     import sys
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                extra=["-Xptxas", "-v"] if "--ptxas" in sys.argv else None))
+                extra=["-Xptxas", "-v"] if "--ptxas" in sys.argv else None,
+                variant="trace" if "--trace" in sys.argv else ""))

@@ -83,6 +83,9 @@ struct gemm_plan {
     const void *lastA, *lastB, *lastC, *lastD;
     CUtensorMap maps[NUM_MAPS];   // A, B, C, D, packed SFA, packed SFB (chain plans: A, B, C, D, E)
     bool maps_valid;
+    unsigned long long *clk_meter;   // clock meter: SM cycles, globaltimer ns (device, allocated on first use)
+    bool clk_meter_on;
+    unsigned long long *trace;       // per-role trace buffer (caller-owned, trace builds only)
 };
 
 namespace {
@@ -477,6 +480,8 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
     kp.status = p->status;
     kp.timeout_ns = p->timeout_ns;
     kp.fault = p->fault;
+    kp.clk_meter = p->clk_meter_on ? p->clk_meter : nullptr;
+    kp.trace = p->trace;
     if (p->sk) {
         kp.sk = 1;
         kp.sk_dp_tiles = p->sk_dp_tiles;
@@ -568,6 +573,7 @@ gemm_status launch_rows(gemm_plan *p, const void *A, const void *B, const void *
     kp.status = p->status;
     kp.timeout_ns = p->timeout_ns;
     kp.fault = p->fault;
+    kp.clk_meter = p->clk_meter_on ? p->clk_meter : nullptr;
     const int units = kp.num_tiles < p->capacity ? kp.num_tiles : p->capacity;
     LaunchShape shape{cg * units, cg, p->smem};
     if (p->family != KIND_F16) {
@@ -756,6 +762,7 @@ gemm_status gemm_plan_destroy(gemm_plan_t p) {
     cudaFree(p->ws_a);
     cudaFree(p->ws_b);
     cudaFree(p->sk_flags);
+    cudaFree(p->clk_meter);
     delete p;
     return GEMM_OK;
 }
@@ -924,6 +931,53 @@ gemm_status gemm_testing_pair_tile_n(int64_t M, int64_t N, int64_t K, gemm_dtype
     if (!tile_n || M <= 0 || N <= 0 || K <= 0 || units <= 0 || (d != GEMM_F32 && d != GEMM_BF16))
         return GEMM_ERR_INVALID_ARG;
     *tile_n = pair_tile_n(M, N, K, d == GEMM_F32, units);
+    return GEMM_OK;
+}
+
+gemm_status gemm_plan_set_clock_meter(gemm_plan_t p, int enable) {
+    if (!p || enable < 0 || enable > 1) return GEMM_ERR_INVALID_ARG;
+    if (p->family == FAMILY_CHAIN) return GEMM_ERR_UNSUPPORTED;
+    if (enable) {
+        if (!p->clk_meter && cudaMalloc(&p->clk_meter, 2 * sizeof(unsigned long long)) != cudaSuccess) {
+            p->clk_meter = nullptr;
+            return GEMM_ERR_CUDA;
+        }
+        if (cudaMemset(p->clk_meter, 0, 2 * sizeof(unsigned long long)) != cudaSuccess) return GEMM_ERR_CUDA;
+    }
+    p->clk_meter_on = enable != 0;
+    return GEMM_OK;
+}
+
+gemm_status gemm_plan_read_clock_meter(gemm_plan_t p, double *sm_mhz, double *cta_seconds) {
+    if (!p || !sm_mhz || !cta_seconds) return GEMM_ERR_INVALID_ARG;
+    *sm_mhz = 0.0;
+    *cta_seconds = 0.0;
+    if (!p->clk_meter) return GEMM_OK;
+    unsigned long long v[2] = {0, 0};
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(v, p->clk_meter, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(p->clk_meter, 0, sizeof v) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (v[1] > 0) {
+        *sm_mhz = (double)v[0] / (double)v[1] * 1e3;
+        *cta_seconds = (double)v[1] * 1e-9;
+    }
+    return GEMM_OK;
+}
+
+// Test hook (declared in include/gb300gemm_testing.h): the per-role trace of a
+// GB300_TRACE=1 build.
+#ifndef GB300_TRACE
+#define GB300_TRACE 0
+#endif
+int gemm_testing_trace_slots(void) { return GB300_TRACE ? (int)TRACE_SLOTS : 0; }
+
+gemm_status gemm_testing_set_trace(gemm_plan_t p, void *dev_buffer, int64_t bytes) {
+    if (!p) return GEMM_ERR_INVALID_ARG;
+    if (!GB300_TRACE || p->family == FAMILY_CHAIN) return GEMM_ERR_UNSUPPORTED;
+    if (dev_buffer && bytes < (int64_t)p->grid * TRACE_SLOTS * (int64_t)sizeof(unsigned long long))
+        return GEMM_ERR_INVALID_ARG;
+    p->trace = static_cast<unsigned long long *>(dev_buffer);
     return GEMM_OK;
 }
 

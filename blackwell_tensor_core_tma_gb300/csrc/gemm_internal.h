@@ -39,6 +39,39 @@ struct KParams {
     int sk_units;
     int epoch;
     int *sk_flags;
+    // clock meter (non-null: thread 0 of every CTA adds its SM cycles and globaltimer
+    // nanoseconds, from entry to exit, into clk_meter[0] and clk_meter[1])
+    unsigned long long *clk_meter;
+    // per-role clock accounting, TRACE_SLOTS counters per CTA (a GB300_TRACE=1 build only)
+    unsigned long long *trace;
+};
+
+// Counters of the per-role trace (GB300_TRACE=1 builds), per CTA, in SM clock cycles
+// unless noted.  Waits are the cycles a role spent in a barrier wait; issue/ld/store the
+// cycles between its waits.  Epilogue counters are summed over the epilogue warps.
+enum TraceSlot : int {
+    TR_KERNEL_CLK = 0,   // entry to exit of thread 0
+    TR_KERNEL_NS,        // the same span in globaltimer nanoseconds
+    TR_PROD_WAIT,        // producer: waits for a free stage (empty[s])
+    TR_PROD_ISSUE,       // producer: arming barriers and issuing the stage's TMA loads
+    TR_PROD_STAGES,      // producer: stages filled (count)
+    TR_MMA_WAIT_ACC,     // MMA issuer: waits for a free accumulator (tempty)
+    TR_MMA_WAIT_AB,      // MMA issuer: waits for a stage's operands (full[s])
+    TR_MMA_WAIT_SF,      // MMA issuer: waits for a stage's scales in TMEM (sfull[s], copier kernels)
+    TR_MMA_ISSUE,        // MMA issuer: scale copies (no copier), MMAs and commits
+    TR_MMA_KBLOCKS,      // MMA issuer: k-blocks consumed (count)
+    TR_MMA_PIECES,       // MMA issuer: work pieces (count)
+    TR_MMA_FIRST,        // MMA issuer: entry to its first k-block's operands landing
+    TR_MMA_END,          // MMA issuer: entry to the completion of its last MMA
+    TR_CP_WAIT,          // copier: waits for a stage's scales in shared memory (sffull[s])
+    TR_CP_ISSUE,         // copier: scale copies and commits
+    TR_EPI_WAIT_ACC,     // epilogue: waits for a finished accumulator (tfull)
+    TR_EPI_TMEM_LD,      // epilogue: tcgen05.ld and wait::ld
+    TR_EPI_WAIT_C,       // epilogue: waits for a C box (and the partial sum of a stream-K tile)
+    TR_EPI_STORE,        // epilogue: add C, convert, stage, issue the TMA store
+    TR_EPI_PIECES,       // epilogue: pieces handled (count, summed over warps)
+    TR_EPI_END,          // epilogue: entry to the last store issued (max over warps)
+    TRACE_SLOTS = 24
 };
 
 // Tensor maps a kernel takes: A, B, C, D, and the packed scale factors (block-scaled only).

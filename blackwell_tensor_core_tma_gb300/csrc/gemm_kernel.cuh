@@ -276,6 +276,49 @@ struct Waiter {
     }
 };
 
+// Per-role clock accounting of a GB300_TRACE=1 build (off by default): a role keeps its
+// counters in registers (RoleClock laps between its waits) and adds them to its CTA's
+// TRACE_SLOTS counters in KParams::trace when it ends.  In other builds every mark and
+// lap compiles to nothing and the counters are dead code.
+#ifndef GB300_TRACE
+#define GB300_TRACE 0
+#endif
+struct RoleClock {
+#if GB300_TRACE
+    long long t = 0;
+    __device__ __forceinline__ void mark() { t = clock64(); }
+    __device__ __forceinline__ void lap(unsigned long long &acc) {
+        const long long n = clock64();
+        acc += (unsigned long long)(n - t);
+        t = n;
+    }
+#else
+    __device__ __forceinline__ void mark() {}
+    __device__ __forceinline__ void lap(unsigned long long &) {}
+#endif
+};
+
+__device__ __forceinline__ void trace_add(const KParams &p, int slot, unsigned long long v) {
+#if GB300_TRACE
+    if (p.trace) atomicAdd(p.trace + (size_t)blockIdx.x * TRACE_SLOTS + slot, v);
+#endif
+}
+
+__device__ __forceinline__ void trace_max(const KParams &p, int slot, unsigned long long v) {
+#if GB300_TRACE
+    if (p.trace) atomicMax(p.trace + (size_t)blockIdx.x * TRACE_SLOTS + slot, v);
+#endif
+}
+
+// clock64() at some point of this thread minus its value at kernel entry (trace builds)
+__device__ __forceinline__ unsigned long long since(long long t_entry) {
+#if GB300_TRACE
+    return (unsigned long long)(clock64() - t_entry);
+#else
+    return 0ull;
+#endif
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -305,6 +348,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     constexpr int CG = Cfg::CG;
     constexpr int STAGES = Cfg::STAGES;
     constexpr int BN = Cfg::BN;
+    const long long t_entry = clock64();             // this thread's entry (clock meter, trace)
+    const uint64_t ns_entry = threadIdx.x == 0 ? globaltimer_ns() : 0ull;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -377,6 +422,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             uint32_t ph = 0;
             bool ok = true;
             uint32_t round = 0;
+            RoleClock rc;
+            unsigned long long tr_wait = 0, tr_issue = 0, tr_stages = 0;
             WorkIter it(p, tile0, tile_step);
             Work wk;
             for (; ok && it.next(p, wk); ++round) {
@@ -385,7 +432,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const int n0 = tn * BN + (int)rank * Cfg::B_ROWS;
                 for (int j = 0; j < kb1 - kb0; ++j) {
                     const int kb = kb_at(j, kb0, kb1, round);
+                    rc.mark();
                     if (!W.wait(&empty[s], ph ^ 1u)) { ok = false; break; }
+                    rc.lap(tr_wait);
                     const bool withhold = p.fault == 1 && round == 0 && j == 0;
                     if (rank == 0 && Cfg::COPIER) mbar_arrive_expect_tx(&sffull[s], Cfg::TX_SF);
                     if (rank == 0 && !withhold) mbar_arrive_expect_tx(&full[s], Cfg::COPIER ? Cfg::TX_AB : Cfg::TX_BYTES);
@@ -426,9 +475,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     load_operand(a_dst, &tmA, m0, TILE_M, p.a_mn != 0);
                     load_operand(b_dst, &tmB, n0, Cfg::B_ROWS, p.b_mn != 0);
+                    rc.lap(tr_issue);
+                    ++tr_stages;
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
             }
+            trace_add(p, TR_PROD_WAIT, tr_wait);
+            trace_add(p, TR_PROD_ISSUE, tr_issue);
+            trace_add(p, TR_PROD_STAGES, tr_stages);
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA issue
@@ -442,18 +496,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int s = 0;
             uint32_t ph = 0, acc_it = 0;
             bool ok = true;
+            RoleClock rc;
+            unsigned long long tr_wacc = 0, tr_wab = 0, tr_wsf = 0, tr_issue = 0, tr_kb = 0, tr_first = 0;
             WorkIter it(p, tile0, tile_step);
             Work wk;
             for (; ok && it.next(p, wk); ++acc_it) {
                 const int kb0 = wk.kb0, kb1 = wk.kb1;
                 const uint32_t b = Cfg::ACC_BUFS == 2 ? (acc_it & 1u) : 0u;
                 const uint32_t aph = Cfg::ACC_BUFS == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
+                rc.mark();
                 if (!W.wait(&tempty[b], aph ^ 1u)) { ok = false; break; }
+                rc.lap(tr_wacc);
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * BN;
                 for (int j = 0; j < kb1 - kb0; ++j) {
                     if (!W.wait(&full[s], ph)) { ok = false; break; }
+                    rc.lap(tr_wab);
+                    if (GB300_TRACE && tr_kb == 0) tr_first = since(t_entry);
                     if (Cfg::COPIER && !W.wait(&sfull[s], ph)) { ok = false; break; }
+                    rc.lap(tr_wsf);
                     tc_fence_after_sync();
                     const uint64_t ad = smem_desc(smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES), a_lbo, 1024, SWZ_128B);
                     const uint64_t bd = smem_desc(smem_addr(smem + Cfg::OFF_B + s * Cfg::B_BYTES), b_lbo, 1024, SWZ_128B);
@@ -478,6 +539,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     }
                     if constexpr (CG == 1) tc_commit<1>(smem_addr(&empty[s]));
                     else tc_commit_pair(smem_addr(&empty[s]), 0x3);
+                    rc.lap(tr_issue);
+                    ++tr_kb;
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
@@ -488,6 +551,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // after an abort: this wait is bounded by time only)
             tc_commit<CG>(smem_addr(drain));
             W.wait(drain, 0, false);
+            trace_add(p, TR_MMA_WAIT_ACC, tr_wacc);
+            trace_add(p, TR_MMA_WAIT_AB, tr_wab);
+            trace_add(p, TR_MMA_WAIT_SF, tr_wsf);
+            trace_add(p, TR_MMA_ISSUE, tr_issue);
+            trace_add(p, TR_MMA_KBLOCKS, tr_kb);
+            trace_add(p, TR_MMA_PIECES, acc_it);
+            trace_add(p, TR_MMA_FIRST, tr_first);
+            trace_add(p, TR_MMA_END, since(t_entry));
         }
     } else if (Cfg::COPIER && warp == Cfg::COPY_WARP) {
         // ---------------------------------------------------------- scale copies
@@ -498,19 +569,26 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 int s = 0;
                 uint32_t ph = 0;
                 bool ok = true;
+                RoleClock rc;
+                unsigned long long tr_wait = 0, tr_issue = 0;
                 WorkIter it(p, tile0, tile_step);
                 Work wk;
                 while (ok && it.next(p, wk)) {
                     for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
+                        rc.mark();
                         if (!W.wait(&sffull[s], ph)) { ok = false; break; }
+                        rc.lap(tr_wait);
                         tc_fence_after_sync();
                         const uint32_t sfa_t = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_SLOT;
                         copy_scales<Cfg>(smem, s, sfa_t, sfa_t + 4 * Cfg::SF_WORDS);
                         if constexpr (CG == 1) tc_commit<1>(smem_addr(&sfull[s]));
                         else tc_commit_pair(smem_addr(&sfull[s]), 0x1);
+                        rc.lap(tr_issue);
                         if (++s == STAGES) { s = 0; ph ^= 1u; }
                     }
                 }
+                trace_add(p, TR_CP_WAIT, tr_wait);
+                trace_add(p, TR_CP_ISSUE, tr_issue);
                 // every copy this thread issued has finished before teardown
                 if constexpr (CG == 1) tc_commit<1>(smem_addr(cdrain));
                 else tc_commit_pair(smem_addr(cdrain), 0x1);
@@ -533,6 +611,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         uint32_t acc_it = 0, ec = 0, n_early = 0;
         uint32_t lc0 = 0, lc1 = 0;                    // the lc[i] of the comment, kept in registers
         bool ok = true;
+        RoleClock rc;
+        unsigned long long tr_wacc = 0, tr_ld = 0, tr_wc = 0, tr_store = 0, tr_end = 0;
         // a TMA load of one 32 x 32 fp32 box into staging buffer i (issued by lane 0, counted by all)
         auto issue = [&](uint32_t i, const CUtensorMap *m, int c0, int c1) {
             if (lane == 0) {
@@ -580,7 +660,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (lane == 0) bulk_wait_group_read0();
                 issue(ec % Cfg::EPI_BUFS, &tmC, n_warp, m_warp);
             }
+            rc.mark();
             if (!__all_sync(0xffffffffu, W.wait(&tfull[b], aph))) break;
+            rc.lap(tr_wacc);
             tc_fence_after_sync();
             const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) + b * BN + h * Cfg::WCOLS;
 
@@ -612,7 +694,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
                 if (use_c) {
+                    rc.lap(tr_store);
                     if (!landed(cur)) return false;
+                    rc.lap(tr_wc);
                     add_box(cur, v);
                 } else if (lane == 0) {
                     // the store that last used this buffer (one or two boxes back) has read it
@@ -651,6 +735,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     bulk_commit_group();
                 }
                 ++ec;
+                rc.lap(tr_store);
                 return true;
             };
 
@@ -664,20 +749,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < Cfg::WCHUNKS; ++j) tie_registers(acc[j]);
                 release_accumulator();
+                rc.lap(tr_ld);
                 if (!await_partial()) { ok = false; break; }
+                rc.lap(tr_wc);
 #pragma unroll
                 for (int j = 0; j < Cfg::WCHUNKS; ++j)
                     if (ok) ok = store_box(j, acc[j]);
             } else {
                 if (!await_partial()) { ok = false; break; }
+                rc.lap(tr_wc);
                 for (int j = 0; j < Cfg::WCHUNKS && ok; ++j) {
                     uint32_t acc[32];
                     tmem_ld_32x32b_x32(taddr + EPI_COLS * j, acc);
                     tmem_ld_wait(acc);
                     if (j == Cfg::WCHUNKS - 1) release_accumulator();
+                    rc.lap(tr_ld);
                     ok = store_box(j, acc);
                 }
             }
+            if (GB300_TRACE) tr_end = since(t_entry);
             if (ok && wk.role == ROLE_EARLY) {
                 // publish the partial sum once every epilogue warp's stores have completed
                 if (lane == 0) {
@@ -695,7 +785,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 ++n_early;
             }
         }
-        if (lane == 0) bulk_wait_group0();
+        if (lane == 0) {
+            bulk_wait_group0();
+            trace_add(p, TR_EPI_WAIT_ACC, tr_wacc);
+            trace_add(p, TR_EPI_TMEM_LD, tr_ld);
+            trace_add(p, TR_EPI_WAIT_C, tr_wc);
+            trace_add(p, TR_EPI_STORE, tr_store);
+            trace_add(p, TR_EPI_PIECES, acc_it);
+            trace_max(p, TR_EPI_END, tr_end);
+        }
     }
 
     // ----------------------------------------------------------------- teardown
@@ -710,6 +808,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc<CG>(tmem_base, 512);
+    }
+    if (threadIdx.x == 0 && (p.clk_meter != nullptr || GB300_TRACE)) {
+        const unsigned long long dclk = (unsigned long long)(clock64() - t_entry);
+        const unsigned long long dns = globaltimer_ns() - ns_entry;
+        if (p.clk_meter) {
+            atomicAdd(p.clk_meter, dclk);
+            atomicAdd(p.clk_meter + 1, dns);
+        }
+        trace_add(p, TR_KERNEL_CLK, dclk);
+        trace_add(p, TR_KERNEL_NS, dns);
     }
 }
 

@@ -25,7 +25,15 @@ EXPORTS = ["gemm_plan_create", "gemm_run", "gemm_run_host", "gemm_plan_last_stat
            "gemm_plan_set_timeout", "gemm_plan_destroy", "gemm_status_string", "gemm_testing_set_fault",
            "gemm_run_noalloc", "gemm_plan_set_split_k", "gemm_chain_plan_create", "gemm_chain_run",
            "gemm_chain_run_host", "gemm_plan_set_stream_k", "gemm_measure_tensor_rate",
-           "gemm_testing_pair_tile_n"]
+           "gemm_testing_pair_tile_n", "gemm_plan_set_clock_meter", "gemm_plan_read_clock_meter",
+           "gemm_testing_trace_slots", "gemm_testing_set_trace"]
+
+# the per-role trace counters of one CTA, in slot order (a GB300_TRACE=1 library:
+# gemm_testing_set_trace); SM clock cycles unless the name says otherwise
+TRACE_FIELDS = ["kernel_clk", "kernel_ns", "prod_wait", "prod_issue", "prod_stages", "mma_wait_acc",
+                "mma_wait_ab", "mma_wait_sf", "mma_issue", "mma_kblocks", "mma_pieces", "mma_first", "mma_end",
+                "cp_wait", "cp_issue", "epi_wait_acc", "epi_tmem_ld", "epi_wait_c", "epi_store", "epi_pieces",
+                "epi_end"]
 
 
 class GemmError(RuntimeError):
@@ -48,18 +56,24 @@ class TensorRate(ctypes.Structure):
 _lib = None
 
 
+def library_variant() -> str:
+    """The build variant this process loads: GB300GEMM_VARIANT ("" = the default library)."""
+    return os.environ.get("GB300GEMM_VARIANT", "")
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.lib_path(library_variant())
 
 
 def lib():
     """The loaded CUDA library; raises if it has not been built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(_build.LIB):
-            raise RuntimeError(f"{_build.LIB} is missing: build it first (python -m "
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first (python -m "
                                "blackwell_tensor_core_tma_gb300.build); there is no CPU path")
-        L = ctypes.CDLL(_build.LIB)
+        L = ctypes.CDLL(path)
         vp, i64, st = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.gemm_plan_create.argtypes = [ctypes.POINTER(vp), i64, i64, i64, st, st, st, st, st, st, ctypes.c_uint]
         L.gemm_plan_create.restype = st
@@ -89,6 +103,14 @@ def lib():
         L.gemm_testing_pair_tile_n.restype = st
         L.gemm_measure_tensor_rate.argtypes = [st, st, st, i64, ctypes.POINTER(TensorRate)]
         L.gemm_measure_tensor_rate.restype = st
+        L.gemm_plan_set_clock_meter.argtypes = [vp, st]
+        L.gemm_plan_set_clock_meter.restype = st
+        L.gemm_plan_read_clock_meter.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+        L.gemm_plan_read_clock_meter.restype = st
+        L.gemm_testing_trace_slots.argtypes = []
+        L.gemm_testing_trace_slots.restype = st
+        L.gemm_testing_set_trace.argtypes = [vp, vp, i64]
+        L.gemm_testing_set_trace.restype = st
         L.gemm_chain_plan_create.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i64, st, st, ctypes.c_uint]
         L.gemm_chain_plan_create.restype = st
         for name in ("gemm_chain_run", "gemm_chain_run_host"):
@@ -190,6 +212,25 @@ def gemm_plan_set_stream_k(plan: int, enable: int):
     _check(lib().gemm_plan_set_stream_k(plan, int(enable)), "gemm_plan_set_stream_k")
 
 
+def gemm_plan_set_clock_meter(plan: int, enable: int):
+    _check(lib().gemm_plan_set_clock_meter(plan, int(enable)), "gemm_plan_set_clock_meter")
+
+
+def gemm_plan_read_clock_meter(plan: int) -> dict:
+    """Mean SM clock (MHz) over the CTA lifetimes counted since the meter was last read."""
+    mhz, sec = ctypes.c_double(), ctypes.c_double()
+    _check(lib().gemm_plan_read_clock_meter(plan, ctypes.byref(mhz), ctypes.byref(sec)), "gemm_plan_read_clock_meter")
+    return {"sm_mhz": mhz.value, "cta_seconds": sec.value}
+
+
+def gemm_testing_trace_slots() -> int:
+    return lib().gemm_testing_trace_slots()
+
+
+def gemm_testing_set_trace(plan: int, buf, nbytes: int):
+    _check(lib().gemm_testing_set_trace(plan, _ptr(buf), int(nbytes)), "gemm_testing_set_trace")
+
+
 def gemm_plan_destroy(plan: int):
     _check(lib().gemm_plan_destroy(plan), "gemm_plan_destroy")
 
@@ -248,6 +289,12 @@ class Plan:
 
     def set_stream_k(self, enable: bool):
         gemm_plan_set_stream_k(self.handle, int(enable))
+
+    def set_clock_meter(self, enable: bool):
+        gemm_plan_set_clock_meter(self.handle, int(enable))
+
+    def read_clock_meter(self) -> dict:
+        return gemm_plan_read_clock_meter(self.handle)
 
     def close(self):
         if self.handle:

@@ -207,6 +207,23 @@ gemm_status gemm_plan_set_split_k(gemm_plan_t p, int splits);
  */
 gemm_status gemm_plan_set_stream_k(gemm_plan_t p, int enable);
 
+/*
+ * SM clock meter of a plan's runs (a measurement aid; the pages have no counterpart and
+ * it does not change what is computed).  The SM clock under a dense tensor load sits
+ * well below its maximum and moves with the power limit, so a per-clock roofline needs
+ * the clock the kernel itself ran at.  enable = 1 allocates a 16-byte device counter on
+ * first use and clears it; every later gemm_run and gemm_run_host of the plan then has
+ * thread 0 of each CTA add its SM clock cycles (clock64) and globaltimer nanoseconds,
+ * from kernel entry to exit, into that counter (two atomic adds per CTA).  enable = 0
+ * stops counting; other values return GEMM_ERR_INVALID_ARG; chain plans return
+ * GEMM_ERR_UNSUPPORTED.  gemm_plan_read_clock_meter synchronises the device, reads and
+ * clears the counter, and returns *sm_mhz = cycles / nanoseconds * 1000 (the mean SM
+ * clock over every counted CTA lifetime) and *cta_seconds (those lifetimes summed); both
+ * are 0 when nothing was counted.  Runs that overlap on the GPU add into one counter.
+ */
+gemm_status gemm_plan_set_clock_meter(gemm_plan_t p, int enable);
+gemm_status gemm_plan_read_clock_meter(gemm_plan_t p, double *sm_mhz, double *cta_seconds);
+
 /* Release the plan (its status word and any host-run buffers).  NULL is a no-op. */
 gemm_status gemm_plan_destroy(gemm_plan_t p);
 

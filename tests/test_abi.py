@@ -14,7 +14,7 @@ def _declared():
     names = set()
     for h in ("gb300gemm.h", "gb300gemm_testing.h"):
         text = open(os.path.join(ROOT, "include", h)).read()
-        names |= set(re.findall(r"^\s*(?:gemm_status|const char \*)\s*\**(gemm_\w+)\s*\(", text, re.M))
+        names |= set(re.findall(r"^\s*(?:gemm_status|const char \*|int)\s*\**(gemm_\w+)\s*\(", text, re.M))
     return names
 
 
@@ -191,3 +191,24 @@ def test_product_code_does_not_reach_the_oracle():
             text = open(os.path.join(dirpath, f), encoding="utf-8").read()
             assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
             assert "liboracle" not in text and "gemm_oracle" not in text, f
+
+
+def test_trace_is_compiled_out_of_the_default_library(lib):
+    """The default build keeps no per-role trace: no counters, and setting one is refused."""
+    assert lib.gemm_testing_trace_slots() == 0
+    assert gemm.gemm_testing_trace_slots() == 0
+
+
+def test_trace_counter_names_follow_the_kernel_slots():
+    """The binding's counter names are the kernel's trace slots, in order (parsed from the
+    internal header), and the trace build reports that many slots per CTA."""
+    text = open(os.path.join(ROOT, "blackwell_tensor_core_tma_gb300", "csrc", "gemm_internal.h")).read()
+    body = re.search(r"enum TraceSlot : int \{(.*?)\};", text, re.S).group(1)
+    names = re.findall(r"^\s*TR_(\w+)", body, re.M)
+    slots = int(re.search(r"TRACE_SLOTS = (\d+)", body).group(1))
+    assert [n.lower() for n in names] == gemm.TRACE_FIELDS
+    assert len(names) <= slots
+    import ctypes
+    L = ctypes.CDLL(build.build(variant="trace"))
+    L.gemm_testing_trace_slots.restype = ctypes.c_int
+    assert L.gemm_testing_trace_slots() == slots
