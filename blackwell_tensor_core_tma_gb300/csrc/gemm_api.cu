@@ -65,6 +65,7 @@ struct gemm_plan {
     int *sk_flags;            // stream-K: one flag per (slot, CTA of the group)
     uint32_t epoch;           // stream-K: runs so far (the value a run's flags carry)
     int tile_n;
+    int epi_box;              // columns of the epilogue's C / D boxes (32 or 16)
     int tile_k;               // K elements per stage
     int num_kb;
     int sfa_stage_bytes, sfb_stage_bytes;   // block-scaled: packed scales per stage (per CTA)
@@ -161,15 +162,17 @@ bool encode_operand_maps(const gemm_plan *p, CUtensorMap *maps, const void *A, c
                        : encode_2d(&maps[0], tma_dtype(p->ab), eb, A, k_units, M, bk, TILE_M, CU_TENSOR_MAP_SWIZZLE_128B)) &&
               (p->b_mn ? encode_2d(&maps[1], tma_dtype(p->ab), eb, B, p->N, p->K, atom, bk, CU_TENSOR_MAP_SWIZZLE_128B)
                        : encode_2d(&maps[1], tma_dtype(p->ab), eb, B, k_units, p->N, bk, b_rows, CU_TENSOR_MAP_SWIZZLE_128B));
-    if (ok && C)
-        ok = encode_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, p->N, M, EPI_COLS, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+    // C and D boxes: 32 rows x epi_box columns, swizzled over their row (fp32: 128 or 64
+    // bytes, bf16: 64 or 32 bytes), as the epilogue stages them
+    const uint32_t box = (uint32_t)p->epi_box;
+    const CUtensorMapSwizzle sw32 = box == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUtensorMapSwizzle sw16 = box == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    if (ok && C) ok = encode_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, p->N, M, box, 32, sw32);
     if (ok) {
         if (p->d == GEMM_BF16)
-            ok = encode_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, p->N, M, EPI_COLS, 32,
-                           CU_TENSOR_MAP_SWIZZLE_64B);
+            ok = encode_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, p->N, M, box, 32, sw16);
         else
-            ok = encode_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, p->N, M, EPI_COLS, 32,
-                           CU_TENSOR_MAP_SWIZZLE_128B);
+            ok = encode_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, p->N, M, box, 32, sw32);
     }
     return ok;
 }
@@ -237,6 +240,7 @@ gemm_status configure_f16(gemm_plan *p) {
     p->stages = f16_stages(cfg);
     p->smem = f16_smem_bytes(cfg);
     p->tile_n = cfg.tile_n;
+    p->epi_box = EPI_COLS;
     p->tile_k = TILE_K16;
     p->num_kb = (int)((p->K + TILE_K16 - 1) / TILE_K16);
     p->tiles_n = (int)((p->N + p->tile_n - 1) / p->tile_n);
@@ -263,6 +267,7 @@ gemm_status configure_scaled(gemm_plan *p) {
     const ScaledShape sh = fam.shape(cg);
     p->cta_group = cg;
     p->tile_n = sh.tile_n;
+    p->epi_box = sh.epi_box;
     p->stages = sh.stages;
     p->smem = sh.smem;
     p->tile_k = sh.bk;

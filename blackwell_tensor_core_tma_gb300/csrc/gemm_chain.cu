@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // row `lane` of the 128-byte-swizzled fp32 box: 16-byte chunk c at (c ^ (row % 8))
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const float4 cv = *reinterpret_cast<const float4 *>(buf + lane * 128 + ((c ^ (lane & 7)) << 4));
+                        const float4 cv = ld_shared_v4f(smem_addr(buf + lane * 128 + ((c ^ (lane & 7)) << 4)));
                         v[4 * c + 0] += cv.x;
                         v[4 * c + 1] += cv.y;
                         v[4 * c + 2] += cv.z;
@@ -264,18 +264,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     // 64-byte rows, 64-byte swizzle: chunk c at (c ^ ((row / 2) % 4))
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        uint4 w;
-                        w.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
-                        w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
-                        w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
-                        w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
-                        *reinterpret_cast<uint4 *>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = w;
+                        st_shared_v4(smem_addr(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)),
+                                     pack_bf16x2(v[8 * c + 0], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                                     pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
                     }
                 } else {
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<float4 *>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                            make_float4(v[4 * c + 0], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                        st_shared_v4(smem_addr(buf + lane * 128 + ((c ^ (lane & 7)) << 4)), __float_as_uint(v[4 * c + 0]),
+                                     __float_as_uint(v[4 * c + 1]), __float_as_uint(v[4 * c + 2]),
+                                     __float_as_uint(v[4 * c + 3]));
                 }
                 fence_proxy_async_smem();
                 __syncwarp();

@@ -121,6 +121,7 @@ struct ScaledShape {
     int bk;          // K elements per stage
     int sfa_bytes;   // packed SFA bytes per stage (one 512-byte block per 4 scales of 128 rows)
     int sfb_bytes;   // packed SFB bytes per stage (every column of the tile)
+    int epi_box;     // columns of the epilogue's C / D boxes (32 or 16)
 };
 
 // A block-scaled kernel family: its four instances (CTA group 1 / 2 x D fp32 / bf16)

@@ -62,8 +62,10 @@ namespace gb300 {
 //           MMA thread then issues MMAs only)
 //   EPI_BUFS  staging buffers per epilogue warp: 2 = the next box's C loads while this
 //             box is stored; 1 = one box at a time (leaves shared memory for a stage)
+//   EPI_BOX   columns of a C / D staging box (32 rows each): 32 (4 KiB of fp32, 128-byte
+//             rows) or 16 (2 KiB, 64-byte rows: half the staging, room for a stage)
 template <int CG_, bool OUT_BF16_, int KIND_, int BN_, int STAGES_, int ACC_BUFS_ = 2, int EPI_WARPS_ = 4,
-          bool COPIER_ = false, int EPI_BUFS_ = 2>
+          bool COPIER_ = false, int EPI_BUFS_ = 2, int EPI_BOX_ = 32>
 struct TileCfg {
     static constexpr int CG = CG_;
     static constexpr bool OUT_BF16 = OUT_BF16_;
@@ -75,6 +77,9 @@ struct TileCfg {
     static constexpr int EPI_WARPS = EPI_WARPS_;
     static constexpr int EPI_BUFS = EPI_BUFS_;
     static_assert(EPI_BUFS == 1 || EPI_BUFS == 2, "epilogue staging buffers");
+    static constexpr int EPI_BOX = EPI_BOX_;
+    static_assert(EPI_BOX == 32 || EPI_BOX == 16, "epilogue box width");
+    static constexpr int BOXES = EPI_COLS / EPI_BOX;            // boxes per 32-column TMEM chunk
     static constexpr bool COPIER = COPIER_ && KIND_ != KIND_F16;
     static constexpr int COPY_WARP = 2 + EPI_WARPS;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS + (COPIER ? 32 : 0);
@@ -111,7 +116,7 @@ struct TileCfg {
     // with a copier warp the scales land on a barrier of their own (sffull), ahead of A and B
     static constexpr int TX_AB = CG * (A_BYTES + B_BYTES);
     static constexpr int TX_SF = CG * (SFA_BYTES + SFB_BYTES);
-    static constexpr int EPI_BUF = 32 * EPI_COLS * 4;           // one 32 x 32 fp32 box
+    static constexpr int EPI_BUF = 32 * EPI_BOX * 4;            // one 32-row fp32 box
     // Every region a swizzled TMA copy or a swizzled MMA descriptor addresses
     // starts on a 1024-byte boundary: the 128-byte swizzle permutes 16-byte
     // chunks by address bits 7..9, so an offset of 512 would shift the row phase.
@@ -317,6 +322,17 @@ __device__ __forceinline__ unsigned long long since(long long t_entry) {
 #else
     return 0ull;
 #endif
+}
+
+// Byte offset of 16-byte chunk c of staging row `row` under the TMA swizzle whose span is
+// the row (128-, 64- or 32-byte rows: the 128B, 64B or 32B mode, which XOR address bits
+// 4.. with bits 7..): for a warp whose lane i owns row i, each 8-lane phase of a 128-bit
+// access then covers all 32 banks once.
+template <int ROW_BYTES>
+__device__ __forceinline__ uint32_t swz_off(int row, int c) {
+    static_assert(ROW_BYTES == 128 || ROW_BYTES == 64 || ROW_BYTES == 32, "swizzle span");
+    const int x = ROW_BYTES == 128 ? (row & 7) : (ROW_BYTES == 64 ? ((row >> 1) & 3) : ((row >> 2) & 1));
+    return (uint32_t)(row * ROW_BYTES + ((c ^ x) << 4));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -613,7 +629,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         bool ok = true;
         RoleClock rc;
         unsigned long long tr_wacc = 0, tr_ld = 0, tr_wc = 0, tr_store = 0, tr_end = 0;
-        // a TMA load of one 32 x 32 fp32 box into staging buffer i (issued by lane 0, counted by all)
+        // a TMA load of one 32 x EPI_BOX fp32 box into staging buffer i (issued by lane 0, counted by all)
         auto issue = [&](uint32_t i, const CUtensorMap *m, int c0, int c1) {
             if (lane == 0) {
                 mbar_arrive_expect_tx(&cb[i], Cfg::EPI_BUF);
@@ -624,12 +640,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         auto landed = [&](uint32_t i) -> bool {
             return __all_sync(0xffffffffu, W.wait(&cb[i], ((i ? lc1 : lc0) - 1u) & 1u));
         };
-        // add the fp32 box in staging buffer i (row `lane`, 128-byte swizzle: 16-byte chunk c at c ^ (row % 8))
-        auto add_box = [&](uint32_t i, float (&v)[32]) {
-            const uint8_t *bb = ebuf + i * Cfg::EPI_BUF;
+        // add the fp32 box in staging buffer i (row `lane` of EPI_BOX * 4 bytes, swizzled)
+        auto add_box = [&](uint32_t i, float (&v)[Cfg::EPI_BOX]) {
+            const uint32_t bb = smem_addr(ebuf + i * Cfg::EPI_BUF);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 cv = *reinterpret_cast<const float4 *>(bb + lane * 128 + ((c ^ (lane & 7)) << 4));
+            for (int c = 0; c < Cfg::EPI_BOX / 4; ++c) {
+                const float4 cv = ld_shared_v4f(bb + swz_off<Cfg::EPI_BOX * 4>(lane, c));
                 v[4 * c + 0] += cv.x;
                 v[4 * c + 1] += cv.y;
                 v[4 * c + 2] += cv.z;
@@ -652,10 +668,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint32_t aph = Cfg::ACC_BUFS == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
             const int m_warp = wk.tm * TILE_M * CG + (int)rank * TILE_M + 32 * q;
             const int n_warp = wk.tn * BN + h * Cfg::WCOLS;
-            // 32 x 32 boxes that lie wholly outside D are neither loaded nor stored
-            const int chunks_in = m_warp < p.M ? max(0, min(Cfg::WCHUNKS, (p.N - n_warp + EPI_COLS - 1) / EPI_COLS)) : 0;
+            // 32 x EPI_BOX boxes that lie wholly outside D are neither loaded nor stored
+            const int boxes_in = m_warp < p.M ? max(0, min(Cfg::WCHUNKS * Cfg::BOXES,
+                                                           (p.N - n_warp + Cfg::EPI_BOX - 1) / Cfg::EPI_BOX))
+                                              : 0;
             // every piece but a partial sum (ROLE_EARLY) adds C, loaded box by box
-            const bool use_c = wk.role != ROLE_EARLY && p.has_c && chunks_in > 0;
+            const bool use_c = wk.role != ROLE_EARLY && p.has_c && boxes_in > 0;
             if (use_c) {                   // the piece's first C box loads while its accumulator is computed
                 if (lane == 0) bulk_wait_group_read0();
                 issue(ec % Cfg::EPI_BUFS, &tmC, n_warp, m_warp);
@@ -676,23 +694,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (got && lane == 0) fence_proxy_async_global();   // the flag before TMA traffic to D
                 return __all_sync(0xffffffffu, got);
             };
-            // one 32 x 32 box: add C, convert, stage in shared memory, then TMA-store it to D
-            // (reduce-add for split-K slices and for stream-K pieces that finish a tile)
-            auto store_box = [&](int j, const uint32_t (&acc)[32]) -> bool {
+            // box jb of the warp's slice (columns EPI_BOX * jb.., sub-box u of a 32-column
+            // chunk whose registers are acc): add C, convert, stage in shared memory, then
+            // TMA-store it to D (reduce-add for split-K slices and for stream-K pieces that
+            // finish a tile)
+            auto store_box = [&](int jb, const uint32_t (&acc)[32], int u) -> bool {
                 const uint32_t cur = ec % Cfg::EPI_BUFS;
                 uint8_t *buf = ebuf + cur * Cfg::EPI_BUF;
-                if (Cfg::EPI_BUFS == 2 && use_c && j + 1 < chunks_in) {
+                if (Cfg::EPI_BUFS == 2 && use_c && jb + 1 < boxes_in) {
                     if (lane == 0) bulk_wait_group_read0();   // the store from the other buffer has read it
-                    issue(cur ^ 1u, &tmC, n_warp + EPI_COLS * (j + 1), m_warp);
+                    issue(cur ^ 1u, &tmC, n_warp + Cfg::EPI_BOX * (jb + 1), m_warp);
                 }
-                if (j >= chunks_in) return true;
-                if (Cfg::EPI_BUFS == 1 && use_c && j > 0) {   // one buffer: this box's C loads now
+                if (jb >= boxes_in) return true;
+                if (Cfg::EPI_BUFS == 1 && use_c && jb > 0) {  // one buffer: this box's C loads now
                     if (lane == 0) bulk_wait_group_read0();   // the last store has read the buffer
-                    issue(0, &tmC, n_warp + EPI_COLS * j, m_warp);
+                    issue(0, &tmC, n_warp + Cfg::EPI_BOX * jb, m_warp);
                 }
-                float v[32];
+                float v[Cfg::EPI_BOX];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(acc[i]);
+                for (int i = 0; i < Cfg::EPI_BOX; ++i) v[i] = __uint_as_float(acc[u * Cfg::EPI_BOX + i]);
                 if (use_c) {
                     rc.lap(tr_store);
                     if (!landed(cur)) return false;
@@ -704,27 +724,26 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     else bulk_wait_group_read0();
                 }
                 __syncwarp();
+                const uint32_t sb = smem_addr(buf);
                 if constexpr (Cfg::OUT_BF16) {
-                    // 64-byte rows, 64-byte swizzle: chunk c at (c ^ ((row / 2) % 4))
+                    // rows of EPI_BOX * 2 bytes (64 or 32), swizzled over the row
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint4 w;
-                        w.x = pack_bf16x2(v[8 * c + 0], v[8 * c + 1]);
-                        w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
-                        w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
-                        w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
-                        *reinterpret_cast<uint4 *>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = w;
-                    }
+                    for (int c = 0; c < Cfg::EPI_BOX / 8; ++c)
+                        st_shared_v4(sb + swz_off<Cfg::EPI_BOX * 2>(lane, c), pack_bf16x2(v[8 * c + 0], v[8 * c + 1]),
+                                     pack_bf16x2(v[8 * c + 2], v[8 * c + 3]), pack_bf16x2(v[8 * c + 4], v[8 * c + 5]),
+                                     pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
                 } else {
+                    // rows of EPI_BOX * 4 bytes (128 or 64), swizzled over the row
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<float4 *>(buf + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                            make_float4(v[4 * c + 0], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                    for (int c = 0; c < Cfg::EPI_BOX / 4; ++c)
+                        st_shared_v4(sb + swz_off<Cfg::EPI_BOX * 4>(lane, c), __float_as_uint(v[4 * c + 0]),
+                                     __float_as_uint(v[4 * c + 1]), __float_as_uint(v[4 * c + 2]),
+                                     __float_as_uint(v[4 * c + 3]));
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    const int dx = n_warp + EPI_COLS * j;
+                    const int dx = n_warp + Cfg::EPI_BOX * jb;
                     if (wk.role == ROLE_EARLY) {
                         tma_store_2d(&tmD, smem_addr(buf), dx, m_warp);
                     } else if (p.splits > 1 || wk.role == ROLE_FINAL) {
@@ -754,7 +773,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 rc.lap(tr_wc);
 #pragma unroll
                 for (int j = 0; j < Cfg::WCHUNKS; ++j)
-                    if (ok) ok = store_box(j, acc[j]);
+#pragma unroll
+                    for (int u = 0; u < Cfg::BOXES; ++u)
+                        if (ok) ok = store_box(j * Cfg::BOXES + u, acc[j], u);
             } else {
                 if (!await_partial()) { ok = false; break; }
                 rc.lap(tr_wc);
@@ -764,7 +785,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     tmem_ld_wait(acc);
                     if (j == Cfg::WCHUNKS - 1) release_accumulator();
                     rc.lap(tr_ld);
-                    ok = store_box(j, acc);
+#pragma unroll
+                    for (int u = 0; u < Cfg::BOXES; ++u)
+                        if (ok) ok = store_box(j * Cfg::BOXES + u, acc, u);
                 }
             }
             if (GB300_TRACE) tr_end = since(t_entry);
@@ -867,8 +890,10 @@ cudaError_t max_active_clusters_tc(int *clusters) {
 template <class C1F, class C1B, class C2F, class C2B>
 struct ScaledInstances {
     static ScaledShape shape(int cta_group) {
-        return cta_group == 1 ? ScaledShape{C1F::BN, C1F::STAGES, C1F::SMEM_BYTES, C1F::BK, C1F::SFA_BYTES, C1F::SFB_BYTES}
-                              : ScaledShape{C2F::BN, C2F::STAGES, C2F::SMEM_BYTES, C2F::BK, C2F::SFA_BYTES, C2F::SFB_BYTES};
+        return cta_group == 1 ? ScaledShape{C1F::BN, C1F::STAGES, C1F::SMEM_BYTES, C1F::BK, C1F::SFA_BYTES, C1F::SFB_BYTES,
+                                            C1F::EPI_BOX}
+                              : ScaledShape{C2F::BN, C2F::STAGES, C2F::SMEM_BYTES, C2F::BK, C2F::SFA_BYTES, C2F::SFB_BYTES,
+                                            C2F::EPI_BOX};
     }
     static cudaError_t prepare(int cta_group, int out_bf16) {
         if (cta_group == 1) return out_bf16 ? prepare_tc<C1B>() : prepare_tc<C1F>();
@@ -892,6 +917,7 @@ struct ScaledInstances {
     static_assert(C1F::CG == 1 && C1B::CG == 1 && C2F::CG == 2 && C2B::CG == 2, "CTA groups");
     static_assert(!C1F::OUT_BF16 && C1B::OUT_BF16 && !C2F::OUT_BF16 && C2B::OUT_BF16, "D types");
     static_assert(C1F::SF_WORDS == C2F::SF_WORDS && C1F::BK == C2F::BK, "one packed scale layout per family");
+    static_assert(C1F::EPI_BOX == C1B::EPI_BOX && C2F::EPI_BOX == C2B::EPI_BOX, "one C / D box per CTA group");
 };
 
 }  // namespace gb300

@@ -24,13 +24,19 @@ using Mx1 = TileCfg<1, OUT_BF16, KIND_MXF8, 224, 4, 2, 4>;
 // pair ring depth and epilogue staging buffers per warp (tuning knobs): one buffer per
 // warp frees the shared memory of a fifth stage (measured on 8192^3: e4m3 +3 %, e2m1 +13 %)
 #ifndef GB300_MXF8_PAIR_STAGES
-#define GB300_MXF8_PAIR_STAGES 5
+#define GB300_MXF8_PAIR_STAGES 6
 #endif
 #ifndef GB300_MXF8_PAIR_EPI_BUFS
 #define GB300_MXF8_PAIR_EPI_BUFS 1
 #endif
+// columns of the epilogue's staging boxes: 16 halves the staging (8 warps x 2 KiB) so that
+// a sixth stage fits
+#ifndef GB300_MXF8_PAIR_EPI_BOX
+#define GB300_MXF8_PAIR_EPI_BOX 16
+#endif
 template <bool OUT_BF16>
-using Mx2 = TileCfg<2, OUT_BF16, KIND_MXF8, 256, GB300_MXF8_PAIR_STAGES, 1, 8, true, GB300_MXF8_PAIR_EPI_BUFS>;
+using Mx2 = TileCfg<2, OUT_BF16, KIND_MXF8, 256, GB300_MXF8_PAIR_STAGES, 1, 8, true, GB300_MXF8_PAIR_EPI_BUFS,
+                    GB300_MXF8_PAIR_EPI_BOX>;
 using MxF8 = ScaledInstances<Mx1<false>, Mx1<true>, Mx2<false>, Mx2<true>>;
 
 }  // namespace

@@ -193,6 +193,21 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *p) {
     return v;
 }
 
+// 16-byte shared-memory store and load, one st.shared.v4 / ld.shared.v4 per thread (a
+// warp's 32 accesses then take the four wavefronts of a 512-byte request when its 8-thread
+// phases hit distinct banks, which the epilogue's swizzled staging rows do)
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ float4 ld_shared_v4f(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // barrier over `threads` threads (a multiple of 32) on hardware barrier `id` (1..15)
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

@@ -26,7 +26,8 @@ EXPORTS = ["gemm_plan_create", "gemm_run", "gemm_run_host", "gemm_plan_last_stat
            "gemm_run_noalloc", "gemm_plan_set_split_k", "gemm_chain_plan_create", "gemm_chain_run",
            "gemm_chain_run_host", "gemm_plan_set_stream_k", "gemm_measure_tensor_rate",
            "gemm_testing_pair_tile_n", "gemm_plan_set_clock_meter", "gemm_plan_read_clock_meter",
-           "gemm_testing_trace_slots", "gemm_testing_set_trace"]
+           "gemm_testing_trace_slots", "gemm_testing_set_trace", "gemm_testing_tmem_ld_probe",
+           "gemm_testing_staging_probe"]
 
 # the per-role trace counters of one CTA, in slot order (a GB300_TRACE=1 library:
 # gemm_testing_set_trace); SM clock cycles unless the name says otherwise
@@ -111,6 +112,10 @@ def lib():
         L.gemm_testing_trace_slots.restype = st
         L.gemm_testing_set_trace.argtypes = [vp, vp, i64]
         L.gemm_testing_set_trace.restype = st
+        L.gemm_testing_tmem_ld_probe.argtypes = [vp, i64]
+        L.gemm_testing_tmem_ld_probe.restype = st
+        L.gemm_testing_staging_probe.argtypes = [st, st, i64, ctypes.POINTER(ctypes.c_double)]
+        L.gemm_testing_staging_probe.restype = st
         L.gemm_chain_plan_create.argtypes = [ctypes.POINTER(vp), i64, i64, i64, i64, st, st, ctypes.c_uint]
         L.gemm_chain_plan_create.restype = st
         for name in ("gemm_chain_run", "gemm_chain_run_host"):
@@ -229,6 +234,22 @@ def gemm_testing_trace_slots() -> int:
 
 def gemm_testing_set_trace(plan: int, buf, nbytes: int):
     _check(lib().gemm_testing_set_trace(plan, _ptr(buf), int(nbytes)), "gemm_testing_set_trace")
+
+
+def gemm_testing_tmem_ld_probe():
+    """Registers of the TMEM probe's five loads: uint32 array [warp 4][thread 32][62]."""
+    import numpy as np
+    out = np.zeros(128 * 62, dtype=np.uint32)
+    _check(lib().gemm_testing_tmem_ld_probe(out.ctypes.data, out.size), "gemm_testing_tmem_ld_probe")
+    return out.reshape(4, 32, 62)
+
+
+def gemm_testing_staging_probe(pattern: int, load: bool, iters: int = 4096) -> float:
+    """SM clocks per warp-wide 128-bit shared-memory access of an epilogue staging pattern."""
+    out = ctypes.c_double()
+    _check(lib().gemm_testing_staging_probe(int(pattern), int(load), int(iters), ctypes.byref(out)),
+           "gemm_testing_staging_probe")
+    return out.value
 
 
 def gemm_plan_destroy(plan: int):

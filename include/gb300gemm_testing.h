@@ -48,6 +48,35 @@ gemm_status gemm_testing_pair_tile_n(int64_t M, int64_t N, int64_t K, gemm_dtype
 int gemm_testing_trace_slots(void);
 gemm_status gemm_testing_set_trace(gemm_plan_t p, void *dev_buffer, int64_t bytes);
 
+/*
+ * TMEM data-movement probe: the tcgen05.ld example shapes of "Tensor Memory（TMEM）"
+ * (section "Shape 和 Repeat Factor": .16x128b.x1 / .x2 / .x4 / .x8 move 16 lanes x 128
+ * bits x num and give each thread 2 / 4 / 8 / 16 registers; section "每个 warp 能访问
+ * 哪些 TMEM lanes": warp w of a warpgroup reaches lanes 32w..32w+31), run on the GPU.
+ * One CTA of four warps writes (lane << 16) | column into every TMEM cell with
+ * tcgen05.st.32x32b (each warp its own window), then each warp reads its window at its
+ * first lane with .16x128b.x1 (column 0), .x2 (column 32), .x4 (column 64), .x8 (column
+ * 128) and .32x32b.x32 (column 256).  host_out receives, for warp w and thread t, the
+ * 62 registers of the five loads in that order (2 + 4 + 8 + 16 + 32 = 62 words) at
+ * index (32w + t) * 62; n_words must be at least 128 * 62.  Synchronises the device.
+ * GEMM_ERR_INVALID_ARG for NULL or too small a buffer, GEMM_ERR_UNSUPPORTED on another
+ * device, GEMM_ERR_CUDA if a CUDA call fails.
+ */
+gemm_status gemm_testing_tmem_ld_probe(uint32_t *host_out, int64_t n_words);
+
+/*
+ * Shared-memory cost of the epilogue's staging patterns, measured alone: one CTA of four
+ * warps, each issuing `iters` rounds of 128-bit accesses (load = 1: ld.shared.v4, 0:
+ * st.shared.v4) in its own 4 KiB buffer; *clk_per_access = SM clocks per warp-wide access
+ * (slowest warp).  pattern 0: bf16 D staging (64-byte rows, 16-byte chunk c of row r at
+ * c ^ ((r / 2) % 4), the TMA's 64-byte swizzle); 1: fp32 C / D staging (128-byte rows,
+ * chunk c at c ^ (r % 8), the 128-byte swizzle); 2: linear (a warp's 512 bytes
+ * contiguous); 3 and 4: the rows of 0 and 1 without the swizzle.  Synchronises the
+ * device.  GEMM_ERR_INVALID_ARG for a NULL output, a pattern outside 0..4, load not 0 or 1
+ * or iters outside 1..2^20; GEMM_ERR_UNSUPPORTED on another device; GEMM_ERR_CUDA.
+ */
+gemm_status gemm_testing_staging_probe(int pattern, int load, int64_t iters, double *clk_per_access);
+
 #ifdef __cplusplus
 }
 #endif
