@@ -244,13 +244,16 @@ struct Waiter {
     uint64_t timeout_ns;
 
     // wait for phase `parity` of `bar`; false if the kernel is giving up
-    // (another role aborted, unless honor_abort is false, or the limit ran out)
+    // (another role aborted, unless honor_abort is false, or the limit ran out).
+    // CLUSTER: acquire at cluster scope (a barrier other CTAs' threads release-arrive on)
+    template <bool CLUSTER = false>
     __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, bool honor_abort = true) const {
         const uint32_t a = smem_addr(bar);
-        if (mbar_try_wait(a, parity)) return true;
+        auto probe = [a, parity]() { return CLUSTER ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
+        if (probe()) return true;
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t it = 1;; ++it) {
-            if (mbar_try_wait(a, parity)) return true;
+            if (probe()) return true;
             if ((it & 15) == 0) {
                 if (honor_abort && *abort_flag) return false;
                 if (globaltimer_ns() - t0 > timeout_ns) {
@@ -521,7 +524,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 const uint32_t b = Cfg::ACC_BUFS == 2 ? (acc_it & 1u) : 0u;
                 const uint32_t aph = Cfg::ACC_BUFS == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
                 rc.mark();
-                if (!W.wait(&tempty[b], aph ^ 1u)) { ok = false; break; }
+                // the peer CTA's epilogue warps release-arrive on tempty: cluster-scope acquire
+                if (!W.wait<CG == 2>(&tempty[b], aph ^ 1u)) { ok = false; break; }
                 rc.lap(tr_wacc);
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + b * BN;

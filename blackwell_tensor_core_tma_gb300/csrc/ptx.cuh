@@ -64,16 +64,34 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// one probe of phase `parity`; cluster-scope acquire so that arrivals released
-// by the peer CTA of a pair are ordered before what follows.  The explicit
-// suspend-time hint bounds how long the thread sleeps inside the probe: with the
-// default limit, a thread whose barrier was completed by the cluster (a pair's
-// remote arrivals, a multicast commit) was seen to resume 1.3-1.5 us after the
-// completion, which stalled the MMA issuer at every tile boundary.
+// One probe of phase `parity` with CTA-scope acquire: for barriers completed by TMA
+// transactions, by tcgen05.commit (also the multicast commit of a CTA pair's leader) or by
+// arrivals of this CTA's own threads.  On a phase that has already completed it costs the
+// waiting thread about 50 clocks, against about 220 for the cluster-scope form below
+// (measured on GB300), which matters on the MMA issuer's path between k-blocks.  The
+// explicit suspend-time hint bounds how long the thread sleeps inside the probe: with the
+// default limit, a thread whose barrier was completed by the cluster (a pair's remote
+// arrivals, a multicast commit) was seen to resume 1.3-1.5 us after the completion, which
+// stalled the MMA issuer at every tile boundary.
 #ifndef GB300_MBAR_SUSPEND_NS
 #define GB300_MBAR_SUSPEND_NS 32
 #endif
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 P, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"((uint32_t)GB300_MBAR_SUSPEND_NS)
+        : "memory");
+    return ok != 0;
+}
+
+// The same with cluster-scope acquire: for a barrier that threads of another CTA of the
+// cluster arrive on with release semantics (a pair's epilogue warps freeing the leader's
+// accumulator), so that what they did before arriving is ordered before what follows.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred P;\n\t"
