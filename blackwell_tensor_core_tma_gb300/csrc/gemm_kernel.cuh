@@ -64,8 +64,11 @@ namespace gb300 {
 //             box is stored; 1 = one box at a time (leaves shared memory for a stage)
 //   EPI_BOX   columns of a C / D staging box (32 rows each): 32 (4 KiB of fp32, 128-byte
 //             rows) or 16 (2 KiB, 64-byte rows: half the staging, room for a stage)
+//   COPIERS   with COPIER: warps that share a stage's scale copies (1 or 2; each
+//             tcgen05.cp costs its issuing thread ~70 clocks, so 12 copies per k-block
+//             outlast the k-block's MMAs on one thread)
 template <int CG_, bool OUT_BF16_, int KIND_, int BN_, int STAGES_, int ACC_BUFS_ = 2, int EPI_WARPS_ = 4,
-          bool COPIER_ = false, int EPI_BUFS_ = 2, int EPI_BOX_ = 32>
+          bool COPIER_ = false, int EPI_BUFS_ = 2, int EPI_BOX_ = 32, int COPIERS_ = 1>
 struct TileCfg {
     static constexpr int CG = CG_;
     static constexpr bool OUT_BF16 = OUT_BF16_;
@@ -81,8 +84,10 @@ struct TileCfg {
     static_assert(EPI_BOX == 32 || EPI_BOX == 16, "epilogue box width");
     static constexpr int BOXES = EPI_COLS / EPI_BOX;            // boxes per 32-column TMEM chunk
     static constexpr bool COPIER = COPIER_ && KIND_ != KIND_F16;
-    static constexpr int COPY_WARP = 2 + EPI_WARPS;
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS + (COPIER ? 32 : 0);
+    static constexpr int COPY_WARP = 2 + EPI_WARPS;             // the first copier warp
+    static constexpr int COPIERS = COPIER ? COPIERS_ : 0;
+    static_assert(COPIERS_ == 1 || COPIERS_ == 2, "copier warps");
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS + 32 * COPIERS;
     static constexpr int WCOLS = BN * 4 / EPI_WARPS;             // columns one epilogue warp handles
     static constexpr int WCHUNKS = WCOLS / EPI_COLS;
     static_assert(ACC_BUFS == 1 || ACC_BUFS == 2, "accumulator buffers");
@@ -238,6 +243,27 @@ struct WorkIter {
     }
 };
 
+// The bounded part of a barrier wait, out of line: reached only when the first probe
+// found the phase still open.  Kept out of the inlined fast path, a completed wait costs
+// the waiting thread ~86 clocks instead of ~200 (measured on GB300), which matters on the
+// MMA issuer's path between k-blocks.
+template <bool CLUSTER>
+__device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, bool honor_abort, volatile int *abort_flag,
+                                            int *status, uint64_t timeout_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (CLUSTER ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
+        if ((it & 15) == 0) {
+            if (honor_abort && *abort_flag) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                *abort_flag = 1;
+                atomicExch(status, (int)GEMM_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
 struct Waiter {
     volatile int *abort_flag;
     int *status;
@@ -249,20 +275,8 @@ struct Waiter {
     template <bool CLUSTER = false>
     __device__ __forceinline__ bool wait(uint64_t *bar, uint32_t parity, bool honor_abort = true) const {
         const uint32_t a = smem_addr(bar);
-        auto probe = [a, parity]() { return CLUSTER ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity); };
-        if (probe()) return true;
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t it = 1;; ++it) {
-            if (probe()) return true;
-            if ((it & 15) == 0) {
-                if (honor_abort && *abort_flag) return false;
-                if (globaltimer_ns() - t0 > timeout_ns) {
-                    *abort_flag = 1;
-                    atomicExch(status, (int)GEMM_ERR_TIMEOUT);
-                    return false;
-                }
-            }
-        }
+        if (CLUSTER ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
+        return mbar_wait_slow<CLUSTER>(a, parity, honor_abort, abort_flag, status, timeout_ns);
     }
 
     // wait until the global flag *f holds v (acquire); false if the kernel is giving up
@@ -346,16 +360,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // SMEM -> TMEM copies of stage s's scales, each 512-byte SMEM block (32 lanes x 16
 // bytes: one word of 128 rows) replicated to the 4 lane windows: SFA word w in columns
-// sfa_t + 4w.., SFB (word w, column group h) in sfb_t + 4(w*HALVES + h)..
-template <class Cfg>
-__device__ __forceinline__ void copy_scales(uint8_t *smem, int s, uint32_t sfa_t, uint32_t sfb_t) {
+// sfa_t + 4w.., SFB (word w, column group h) in sfb_t + 4(w*HALVES + h)..  The stage's
+// blocks are numbered SFA first, then SFB; with NPART issuing threads, part `part`
+// issues the blocks whose number is part modulo NPART.
+template <class Cfg, int NPART = 1>
+__device__ __forceinline__ void copy_scales(uint8_t *smem, int s, uint32_t sfa_t, uint32_t sfb_t, int part = 0) {
     const uint32_t sf_src = smem_addr(smem + Cfg::OFF_SF + s * (Cfg::SFA_BYTES + Cfg::SFB_BYTES));
 #pragma unroll
     for (int i = 0; i < Cfg::SF_WORDS; ++i)
-        tmem_cp_32x128b_warpx4<Cfg::CG>(sfa_t + 4 * i, smem_desc(sf_src + 512 * i, 512, 128, SWZ_NONE));
+        if (i % NPART == part)
+            tmem_cp_32x128b_warpx4<Cfg::CG>(sfa_t + 4 * i, smem_desc(sf_src + 512 * i, 512, 128, SWZ_NONE));
 #pragma unroll
     for (int i = 0; i < Cfg::SF_WORDS * Cfg::HALVES; ++i)
-        tmem_cp_32x128b_warpx4<Cfg::CG>(sfb_t + 4 * i, smem_desc(sf_src + Cfg::SFA_BYTES + 512 * i, 512, 128, SWZ_NONE));
+        if ((Cfg::SF_WORDS + i) % NPART == part)
+            tmem_cp_32x128b_warpx4<Cfg::CG>(sfb_t + 4 * i,
+                                            smem_desc(sf_src + Cfg::SFA_BYTES + 512 * i, 512, 128, SWZ_NONE));
 }
 
 template <class Cfg>
@@ -414,10 +433,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         mbar_init(epi_sync, Cfg::EPI_WARPS);
         if constexpr (Cfg::COPIER) {
             for (int i = 0; i < STAGES; ++i) {
-                mbar_init(&sfull[i], 1);
+                mbar_init(&sfull[i], Cfg::COPIERS);      // one commit per copier warp
                 mbar_init(&sffull[i], 1);
             }
-            mbar_init(cdrain, 1);
+            mbar_init(cdrain, Cfg::COPIERS);
         }
         *abort_flag = 0;
         fence_mbarrier_init();
@@ -580,9 +599,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             trace_add(p, TR_MMA_FIRST, tr_first);
             trace_add(p, TR_MMA_END, since(t_entry));
         }
-    } else if (Cfg::COPIER && warp == Cfg::COPY_WARP) {
+    } else if (Cfg::COPIER && warp >= Cfg::COPY_WARP) {
         // ---------------------------------------------------------- scale copies
         if constexpr (Cfg::COPIER) {
+            const int part = warp - Cfg::COPY_WARP;      // this warp's share of each stage's copies
             if (rank == 0 && lane == 0) {
                 // stage s's slot is rewritten only after sffull[s] of the next round, i.e. after
                 // the producer saw empty[s]: the MMAs that read the slot have completed
@@ -600,7 +620,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         rc.lap(tr_wait);
                         tc_fence_after_sync();
                         const uint32_t sfa_t = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_SLOT;
-                        copy_scales<Cfg>(smem, s, sfa_t, sfa_t + 4 * Cfg::SF_WORDS);
+                        copy_scales<Cfg, Cfg::COPIERS>(smem, s, sfa_t, sfa_t + 4 * Cfg::SF_WORDS, part);
                         if constexpr (CG == 1) tc_commit<1>(smem_addr(&sfull[s]));
                         else tc_commit_pair(smem_addr(&sfull[s]), 0x1);
                         rc.lap(tr_issue);

@@ -27,8 +27,13 @@ using Cfg1 = TileCfg<1, OUT_BF16, KIND_MXF4, 128, 5, 2, 4>;
 #ifndef GB300_MXF4_PAIR_EPI_BUFS
 #define GB300_MXF4_PAIR_EPI_BUFS 1
 #endif
+// warps sharing the scale copies (two: e2m1 with UE4M3 scales +16 % per clock at 8192^3, e4m3 +1 %)
+#ifndef GB300_MXF4_PAIR_COPIERS
+#define GB300_MXF4_PAIR_COPIERS 2
+#endif
 template <bool OUT_BF16>
-using Cfg2 = TileCfg<2, OUT_BF16, KIND_MXF4, 256, GB300_MXF4_PAIR_STAGES, 1, 8, true, GB300_MXF4_PAIR_EPI_BUFS>;
+using Cfg2 = TileCfg<2, OUT_BF16, KIND_MXF4, 256, GB300_MXF4_PAIR_STAGES, 1, 8, true, GB300_MXF4_PAIR_EPI_BUFS,
+                     32, GB300_MXF4_PAIR_COPIERS>;
 using Family = ScaledInstances<Cfg1<false>, Cfg1<true>, Cfg2<false>, Cfg2<true>>;
 
 }  // namespace

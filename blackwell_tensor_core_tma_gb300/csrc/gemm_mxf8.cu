@@ -34,9 +34,13 @@ using Mx1 = TileCfg<1, OUT_BF16, KIND_MXF8, 224, 4, 2, 4>;
 #ifndef GB300_MXF8_PAIR_EPI_BOX
 #define GB300_MXF8_PAIR_EPI_BOX 16
 #endif
+// warps sharing the scale copies (two: e2m1 with UE4M3 scales +16 % per clock at 8192^3, e4m3 +1 %)
+#ifndef GB300_MXF8_PAIR_COPIERS
+#define GB300_MXF8_PAIR_COPIERS 2
+#endif
 template <bool OUT_BF16>
 using Mx2 = TileCfg<2, OUT_BF16, KIND_MXF8, 256, GB300_MXF8_PAIR_STAGES, 1, 8, true, GB300_MXF8_PAIR_EPI_BUFS,
-                    GB300_MXF8_PAIR_EPI_BOX>;
+                    GB300_MXF8_PAIR_EPI_BOX, GB300_MXF8_PAIR_COPIERS>;
 using MxF8 = ScaledInstances<Mx1<false>, Mx1<true>, Mx2<false>, Mx2<true>>;
 
 }  // namespace
