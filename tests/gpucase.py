@@ -76,6 +76,52 @@ def check_full(w, x, D, c_none=False):
     _assert_within(w, D, D_ref, S, c, "full")
 
 
+def _input_key(w, x, extra=()) -> str:
+    """Checksum of everything a full oracle product depends on: the input bytes, the problem's
+    shape, types and layouts, and the oracle's own C source."""
+    import hashlib
+    import os
+    h = hashlib.sha256()
+    for k in sorted(x):
+        if x[k] is not None:
+            h.update(k.encode())
+            h.update(np.ascontiguousarray(x[k]).tobytes())
+    h.update(repr((type(w).__name__, sorted(vars(w).items()), extra)).encode())
+    with open(os.path.join(os.path.dirname(oracle.__file__), "gemm_oracle.c"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:32]
+
+
+def cached(key: str, compute):
+    """compute() (a tuple of arrays), kept on disk under $GB300GEMM_ORACLE_CACHE/<key>.npz when
+    that variable names a directory; without it nothing is written."""
+    import os
+    d = os.environ.get("GB300GEMM_ORACLE_CACHE")
+    path = os.path.join(d, key + ".npz") if d else None
+    if path and os.path.exists(path):
+        with np.load(path) as z:
+            return tuple(z[f"a{i}"] for i in range(len(z.files)))
+    out = compute()
+    if path:
+        os.makedirs(d, exist_ok=True)
+        tmp = path + ".tmp.npz"
+        np.savez(tmp, **{f"a{i}": a for i, a in enumerate(out)})
+        os.replace(tmp, path)
+    return out
+
+
+def full_ratio(w, x, D) -> float:
+    """Every element of D against the oracle's full product (fp64; cached by input checksum):
+    asserts the accept rule and returns the largest error / tolerance ratio."""
+    D_ref, S = cached(_input_key(w, x), lambda: oracle.gemm(
+        x["A"], x["B"], x["C"], w.M, w.N, w.K, w.ab, a_row_major=w.a_row_major, b_row_major=w.b_row_major,
+        SFA=x.get("SFA"), SFB=x.get("SFB"), block_scaled=w.block_scaled))
+    c = x["C"].astype(np.float64)
+    _assert_within(w, D, D_ref, S, c, "every element")
+    tol = tolerance(w, D_ref, S, c)
+    return float(np.max(np.abs(D - D_ref) / np.maximum(tol, 1e-300)))
+
+
 def sample_entries(M: int, N: int, tile_m: int, tile_n: int, n_random: int = 4096, seed: int = 0):
     """Tile corners and edges, one full row and column, and random entries."""
     rng = np.random.default_rng(seed)
