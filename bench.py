@@ -244,6 +244,16 @@ def workload(args):
 
 # --------------------------------------------------------------- our arm
 
+def gemm_config(w) -> dict:
+    """The workload part of the JSON line's config, shared by both arms."""
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "ab": w.ab, "c": "fp32",
+            "a_row_major": w.a_row_major, "b_row_major": w.b_row_major, "d": w.d}
+
+
+def chain_config(w) -> dict:
+    return {"workload": w.name, "M": w.M, "K": w.K, "N1": w.N1, "N2": w.N2, "ab": w.ab, "c": "fp32", "d": w.d}
+
+
 def timed_e2e(step, flops, world, dev, stream, steps, blocks=3):
     """End-to-end rate through the host-buffer entry point: `blocks` separately timed blocks of
     `steps` calls (each copying its inputs up and its result down), after two untimed calls.
@@ -437,12 +447,9 @@ def run_ours(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(max_ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.ab == "bf16" else w.ab,
         "data": "synthetic (seeded splitmix64; recipe of the workload)",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "ab": w.ab, "c": "fp32",
-                   "a_row_major": w.a_row_major, "b_row_major": w.b_row_major,
-                   "d": w.d, "cta_group": info["cta_group"], "tile": [info["tile_m"], info["tile_n"],
-                                                                      info["tile_k"]],
-                   "stages": info["stages"], "grid": info["grid"], "replicas": world,
-                   "l2": "no flush: inputs (A+B+C) larger than the 129 MB L2"},
+        "config": dict(gemm_config(w), cta_group=info["cta_group"],
+                       tile=[info["tile_m"], info["tile_n"], info["tile_k"]], stages=info["stages"],
+                       grid=info["grid"], replicas=world, l2="no flush: inputs (A+B+C) larger than the 129 MB L2"),
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": args.steps * info["launches_per_run"],
@@ -547,10 +554,8 @@ def run_ours_chain(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(max_ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.ab,
         "data": "synthetic (seeded splitmix64; recipe of the workload)",
-        "config": {"workload": w.name, "M": w.M, "K": w.K, "N1": w.N1, "N2": w.N2, "ab": w.ab, "c": "fp32",
-                   "d": w.d, "tile": [128, info["tile_n"], info["tile_k"]], "stages": info["stages"],
-                   "grid": info["grid"], "replicas": world,
-                   "l2": "no flush: inputs (A alone) larger than the 129 MB L2"},
+        "config": dict(chain_config(w), tile=[128, info["tile_n"], info["tile_k"]], stages=info["stages"],
+                       grid=info["grid"], replicas=world, l2="no flush: inputs (A alone) larger than the 129 MB L2"),
         "roofline": roofline,
         "e2e": e2e,
         "gpu_launches": args.steps * info["launches_per_run"],
@@ -647,7 +652,7 @@ def run_reference(args, rank, world):
         "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded splitmix64)",
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "ab": w.ab, "d": w.d},
+        "config": gemm_config(w),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.threads(),
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -686,7 +691,7 @@ def run_reference_chain(args, w, world):
         "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded splitmix64)",
-        "config": {"workload": w.name, "M": w.M, "K": w.K, "N1": w.N1, "N2": w.N2, "ab": w.ab, "d": w.d},
+        "config": chain_config(w),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.threads(),
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

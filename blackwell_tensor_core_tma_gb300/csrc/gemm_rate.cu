@@ -8,8 +8,8 @@
 // SM, operands resident in shared memory (and scales in TMEM) before the clock starts,
 // one thread issuing `iters` groups of four back-to-back tcgen05.mma into one TMEM
 // accumulator — the instruction shape, operand layout and accumulate chain of the
-// GEMM's own main loop ("Blackwell Tensor Core", tcgen05.mma issued by one thread,
-// accumulator in TMEM; "Tensor Memory（TMEM）", allocation) — and a commit that marks
+// GEMM's own main loop ("Tensor Core 数据布局的演进", section on Blackwell: A and B from
+// shared memory, the accumulator in TMEM; "Tensor Memory（TMEM）", allocation) — and a commit that marks
 // the end.  Each CTA records the SM clocks and the globaltimer nanoseconds between its
 // first issue and the commit's arrival; the ratio of the two is the SM clock of the
 // run.  Operand values do not enter the per-clock rate, but they do enter the power the

@@ -67,8 +67,7 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
 // One probe of phase `parity` with CTA-scope acquire: for barriers completed by TMA
 // transactions, by tcgen05.commit (also the multicast commit of a CTA pair's leader) or by
 // arrivals of this CTA's own threads.  On a phase that has already completed it costs the
-// waiting thread about 50 clocks, against about 220 for the cluster-scope form below
-// (measured on GB300), which matters on the MMA issuer's path between k-blocks.  The
+// thread about 55 clocks, the cluster-scope form below about 77 (measured on GB300).  The
 // explicit suspend-time hint bounds how long the thread sleeps inside the probe: with the
 // default limit, a thread whose barrier was completed by the cluster (a pair's remote
 // arrivals, a multicast commit) was seen to resume 1.3-1.5 us after the completion, which

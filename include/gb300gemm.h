@@ -310,8 +310,9 @@ gemm_status gemm_chain_run_host(gemm_plan_t p, const void *A, const void *B, con
  * instruction shape (M = 128 * cta_group, N = 256, 32 bytes of K per
  * instruction: K = 16 for f16/bf16, 32 for e4m3, 64 for e2m1) from operands
  * already in shared memory into one TMEM accumulator, and times the stream
- * with the SM clock and the globaltimer ("Blackwell Tensor Core": one thread
- * issues tcgen05.mma, the accumulator lives in TMEM).  ab / block_scaled pick
+ * with the SM clock and the globaltimer ("Tensor Core 数据布局的演进", section on
+ * Blackwell: tcgen05.mma reads A and B from shared memory and accumulates in TMEM;
+ * "Tensor Memory（TMEM）": the accumulator's columns are allocated per CTA).  ab / block_scaled pick
  * the kind as for gemm_plan_create.  1 <= iters <= 2^20.  Synchronises the
  * device first and again before returning; meant for an otherwise idle GPU.
  * Errors: GEMM_ERR_INVALID_ARG (out NULL, cta_group not 1 or 2, iters out of
