@@ -57,7 +57,7 @@ enum TraceSlot : int {
     TR_PROD_STAGES,      // producer: stages filled (count)
     TR_MMA_WAIT_ACC,     // MMA issuer: waits for a free accumulator (tempty)
     TR_MMA_WAIT_AB,      // MMA issuer: waits for a stage's operands (full[s])
-    TR_MMA_WAIT_SF,      // MMA issuer: waits for a stage's scales in TMEM (sfull[s], copier kernels)
+    TR_MMA_WAIT_SF,      // MMA issuer: (unused: with copier warps full[s] covers the stage's scales)
     TR_MMA_ISSUE,        // MMA issuer: scale copies (no copier), MMAs and commits
     TR_MMA_KBLOCKS,      // MMA issuer: k-blocks consumed (count)
     TR_MMA_PIECES,       // MMA issuer: work pieces (count)

@@ -23,10 +23,12 @@
 //               block scaling it first moves the stage's scales SMEM -> TMEM
 //               with tcgen05.cp (same page: SFA, SFB: GMEM --TMA--> SMEM
 //               --tcgen05.cp--> TMEM --tcgen05.mma-->).
-//   warp 2+EPI  (block-scaled instances with COPIER) waits for the stage's scales
-//               (sffull[s]), copies them SMEM -> TMEM ahead of the MMA issuer and
-//               signals the copies' completion on sfull[s], so that copies and MMAs
-//               come from two threads and overlap.
+//   warps 2+EPI.. (block-scaled instances with COPIER, COPIERS warps) wait for the
+//               stage's scales (sffull[s]), share the copies SMEM -> TMEM ahead of the
+//               MMA issuer and commit their completion to the stage's full[s], which
+//               then stands for operands and scales both (one wait per k-block for the
+//               MMA issuer), so that copies and MMAs come from different threads and
+//               overlap.
 //   warps 2..5  epilogue warps (2..9 with EPI_WARPS = 8): warp w reads TMEM lanes 32*(w%4)..+31
 //               ("Tensor Memory（TMEM）": each warp of a warpgroup reaches its
 //               own 32-lane window) with tcgen05.ld + tcgen05.wait::ld, adds C
@@ -134,9 +136,10 @@ struct TileCfg {
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0 && OFF_B % 1024 == 0, "operand stages 1024-aligned");
     static_assert(OFF_EPI % 1024 == 0 && EPI_BUF % 1024 == 0, "epilogue staging 1024-aligned");
     // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], cload[EPI_WARPS][2], drain,
-    // epi_sync, then with COPIER: sfull[STAGES] (the stage's scales are in TMEM), cdrain,
-    // sffull[STAGES] (the stage's scales are in shared memory)
-    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 * EPI_WARPS + 2 + (COPIER ? 2 * STAGES + 1 : 0);
+    // epi_sync, then with COPIER: cdrain, sffull[STAGES] (the stage's scales are in shared
+    // memory).  With COPIER, full[s] also counts the copier warps' commits: the stage's
+    // scales are in TMEM.
+    static constexpr int NBAR = 2 * STAGES + 2 + 2 + 2 * EPI_WARPS + 2 + (COPIER ? STAGES + 1 : 0);
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;         // tmem base slot, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;     // + alignment slack
     // TMEM columns: accumulators [0, ACC_BUFS*BN), then one scale slot per stage: SFA
@@ -404,8 +407,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint64_t *cload = tempty + 2;
     uint64_t *drain = cload + 2 * Cfg::EPI_WARPS;
     uint64_t *epi_sync = drain + 1;                       // every epilogue warp stored its part of a partial sum
-    uint64_t *sfull = epi_sync + 1;                       // COPIER only
-    uint64_t *cdrain = sfull + STAGES;                    // COPIER only
+    uint64_t *cdrain = epi_sync + 1;                      // COPIER only
     uint64_t *sffull = cdrain + 1;                        // COPIER only
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 4);
@@ -421,7 +423,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             prefetch_tensormap(&tmSFB);
         }
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            // the producer's arrival (with the operands' transaction bytes) and, with COPIER,
+            // one commit per copier warp once the stage's scales are in TMEM
+            mbar_init(&full[s], 1 + Cfg::COPIERS);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -432,10 +436,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         mbar_init(drain, 1);
         mbar_init(epi_sync, Cfg::EPI_WARPS);
         if constexpr (Cfg::COPIER) {
-            for (int i = 0; i < STAGES; ++i) {
-                mbar_init(&sfull[i], Cfg::COPIERS);      // one commit per copier warp
-                mbar_init(&sffull[i], 1);
-            }
+            for (int i = 0; i < STAGES; ++i) mbar_init(&sffull[i], 1);
             mbar_init(cdrain, Cfg::COPIERS);
         }
         *abort_flag = 0;
@@ -552,13 +553,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     if (!W.wait(&full[s], ph)) { ok = false; break; }
                     rc.lap(tr_wab);
                     if (GB300_TRACE && tr_kb == 0) tr_first = since(t_entry);
-                    if (Cfg::COPIER && !W.wait(&sfull[s], ph)) { ok = false; break; }
-                    rc.lap(tr_wsf);
                     tc_fence_after_sync();
                     const uint64_t ad = smem_desc(smem_addr(smem + Cfg::OFF_A + s * Cfg::A_BYTES), a_lbo, 1024, SWZ_128B);
                     const uint64_t bd = smem_desc(smem_addr(smem + Cfg::OFF_B + s * Cfg::B_BYTES), b_lbo, 1024, SWZ_128B);
                     if constexpr (Cfg::SCALED) {
-                        // stage s's scale slot (filled here, or by the copier warp before sfull[s])
+                        // stage s's scale slot (filled here, or by the copier warps before their
+                        // commits completed full[s])
                         const uint32_t sfa_t = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_SLOT;
                         const uint32_t sfb_t = sfa_t + 4 * Cfg::SF_WORDS;
                         if constexpr (!Cfg::COPIER) copy_scales<Cfg>(smem, s, sfa_t, sfb_t);
@@ -621,8 +621,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                         tc_fence_after_sync();
                         const uint32_t sfa_t = tmem_base + Cfg::SF_COL0 + s * Cfg::SF_SLOT;
                         copy_scales<Cfg, Cfg::COPIERS>(smem, s, sfa_t, sfa_t + 4 * Cfg::SF_WORDS, part);
-                        if constexpr (CG == 1) tc_commit<1>(smem_addr(&sfull[s]));
-                        else tc_commit_pair(smem_addr(&sfull[s]), 0x1);
+                        // full[s] of the leader: the MMA issuer's one wait covers the copies
+                        if constexpr (CG == 1) tc_commit<1>(smem_addr(&full[s]));
+                        else tc_commit_pair(smem_addr(&full[s]), 0x1);
                         rc.lap(tr_issue);
                         if (++s == STAGES) { s = 0; ph ^= 1u; }
                     }
