@@ -123,16 +123,18 @@ const ScaledFamily &scaled_family(int family) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 2-D row-major tensor [outer][inner] with a box of box_outer x box_inner elements
+// 2-D row-major tensor [outer][inner] with a box of box_outer x box_inner elements; `promo`
+// is the L2 fill granularity of the copies (lines fetched around each box row)
 bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, int ebytes, const void *ptr, uint64_t inner, uint64_t outer,
-               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw,
+               CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
     if (!encoder()) return false;      // the driver's encoder is looked up on first use
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * (uint64_t)ebytes};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(m, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          sw, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -167,7 +169,11 @@ bool encode_operand_maps(const gemm_plan *p, CUtensorMap *maps, const void *A, c
     const uint32_t box = (uint32_t)p->epi_box;
     const CUtensorMapSwizzle sw32 = box == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     const CUtensorMapSwizzle sw16 = box == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
-    if (ok && C) ok = encode_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, p->N, M, box, 32, sw32);
+    // C is read once, with an evict-first hint: a 64-byte box row fills only its own 64 bytes
+    // of L2 (a 256-byte fill would be evicted before the neighbouring boxes read it)
+    if (ok && C)
+        ok = encode_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, p->N, M, box, 32, sw32,
+                       box == 32 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B);
     if (ok) {
         if (p->d == GEMM_BF16)
             ok = encode_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, p->N, M, box, 32, sw16);
