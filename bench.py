@@ -52,12 +52,14 @@ MEASURED_TRAFFIC = {
 }
 
 
+# the kernel's sources and the host code that encodes its tensor maps (box shapes, swizzle and
+# L2 fill granularity change the DRAM traffic as much as the kernel does)
 KERNEL_SOURCES = {
-    "f16": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_f16.cu"],
-    "mxf8": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_mxf8.cu"],
-    "mxf4": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_mxf4.cu"],
-    "nvf4": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_nvf4.cu"],
-    "chain": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_chain.cu"],
+    "f16": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_f16.cu", "gemm_api.cu"],
+    "mxf8": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_mxf8.cu", "gemm_api.cu"],
+    "mxf4": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_mxf4.cu", "gemm_api.cu"],
+    "nvf4": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_nvf4.cu", "gemm_api.cu"],
+    "chain": ["gemm_kernel.cuh", "ptx.cuh", "gemm_internal.h", "gemm_chain.cu", "gemm_api.cu"],
 }
 
 
@@ -94,7 +96,7 @@ def strip_comments(src: str) -> str:
 
 
 def kernel_source_hash(family: str = "f16") -> str:
-    """Hash of the CUDA sources (comments stripped) the GEMM kernel of a family is built from."""
+    """Hash of the CUDA sources (comments stripped) a family's kernel is built and launched from."""
     import hashlib
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[family]:

@@ -27,6 +27,18 @@ using namespace gb300;
 #define GB300_GROUP_M_SINGLE 16
 #endif
 
+// stream-K needs at least this many k-blocks per tile (32 lost 10 % on block-scaled e4m3 4096^3,
+// whose 128-element k-blocks make K = 4096 only 32 of them)
+#ifndef GB300_SK_MIN_KB
+#define GB300_SK_MIN_KB 64
+#endif
+
+// L2 fill granularity of the 32-column C boxes (128-byte rows; 128-byte fills saved 3 % of the
+// DRAM reads at 8192^3 and changed no timing, so the default stays 256)
+#ifndef GB300_C_PROMO32
+#define GB300_C_PROMO32 CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+#endif
+
 // gemm_run_host splits a product into at most this many row chunks
 #ifndef GB300_HOST_CHUNKS
 #define GB300_HOST_CHUNKS 8
@@ -173,7 +185,7 @@ bool encode_operand_maps(const gemm_plan *p, CUtensorMap *maps, const void *A, c
     // of L2 (a 256-byte fill would be evicted before the neighbouring boxes read it)
     if (ok && C)
         ok = encode_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, p->N, M, box, 32, sw32,
-                       box == 32 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_64B);
+                       box == 32 ? GB300_C_PROMO32 : CU_TENSOR_MAP_L2_PROMOTION_L2_64B);
     if (ok) {
         if (p->d == GEMM_BF16)
             ok = encode_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, p->N, M, box, 32, sw16);
@@ -338,7 +350,7 @@ gemm_status choose_splits(gemm_plan *p) {
     // waves (below 4 the idle part of the last wave is a large share; above, the power the
     // idle SMs leave lets the busy ones clock higher)
     p->sk = s == 1 && p->sk_request && p->d == GEMM_F32 && p->tiles >= units && p->tiles % units != 0 &&
-            p->num_kb >= 64 && p->tiles < 4 * units;
+            p->num_kb >= GB300_SK_MIN_KB && p->tiles < 4 * units;
     if (p->sk) {
         p->sk_dp_tiles = (p->tiles / units - 1) * units;
         p->grid = p->cta_group * units;
