@@ -39,15 +39,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture
 # summarised in profiles/; valid only for the kernel sources the capture ran on
 MEASURED_TRAFFIC = {
-    "bf16_8192x8192x8192_bf16out": {"bytes": 1134567000 + 124033792, "src": "afaf0f27063c43cc",
-                                    "ncu": "profiles/gemm_tc_kernel_bf16_8192x8192x8192_bf16out_full.md"},
-    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 835111168 + 235629824, "src": "7e7d92e5866b89fe",
+    "bf16_8192x8192x8192_bf16out": {"bytes": 1139914240 + 123201024, "src": "a2c6296cda029fdf",
+                                    "ncu": "profiles/gemm_tc_kernel_bf16_8192x8192x8192_bf16out_launches.md"},
+    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 610507776 + 234525440, "src": "d30c7b6d9022fc55",
                                           "ncu": "profiles/gemm_tc_kernel_mxf8_8192x8192x8192_launches.md"},
-    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 483523328 + 218187776, "src": "527f3953ed66539b",
+    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 485758976 + 217974784, "src": "dc410bf7a45fbc9e",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 495379968 + 219619840, "src": "b05a1725a1fc2e85",
+    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 496706560 + 219912960, "src": "3b1938cd4cb898ee",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312903424 + 12218624, "src": "8155b09d3c4e1d80",
+    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312781056 + 12135936, "src": "a0a677128a3c896e",
                                               "ncu": "profiles/chain_kernel_bf16_32768x4096_256x256_launches.md"},
 }
 
