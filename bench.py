@@ -556,7 +556,8 @@ def run_ours_chain(args, rank, world, local_rank):
         "warmup": args.warmup, "ms_per_step": round(max_ms, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.ab,
         "data": "synthetic (seeded splitmix64; recipe of the workload)",
-        "config": dict(chain_config(w), tile=[128, info["tile_n"], info["tile_k"]], stages=info["stages"],
+        "config": dict(chain_config(w), cta_group=info["cta_group"],
+                       tile=[info["tile_m"], info["tile_n"], info["tile_k"]], stages=info["stages"],
                        grid=info["grid"], replicas=world, l2="no flush: inputs (A alone) larger than the 129 MB L2"),
         "roofline": roofline,
         "e2e": e2e,

@@ -799,18 +799,28 @@ gemm_status gemm_chain_plan_create(gemm_plan_t *out, int64_t M, int64_t N1, int6
     if ((unsigned)ab > GEMM_E2M1 || (unsigned)d > GEMM_E2M1) return GEMM_ERR_INVALID_ARG;
     if ((flags & GEMM_FLAG_FORCE_1CTA) && (flags & GEMM_FLAG_FORCE_2CTA)) return GEMM_ERR_INVALID_ARG;
     if ((ab != GEMM_F16 && ab != GEMM_BF16) || (d != GEMM_F32 && d != GEMM_BF16)) return GEMM_ERR_UNSUPPORTED;
-    // both products' accumulators share the 512 tensor-memory columns of one SM; single CTAs only
-    if (N1 > CHAIN_MAX_N || N2 > CHAIN_MAX_N || (flags & GEMM_FLAG_FORCE_2CTA)) return GEMM_ERR_UNSUPPORTED;
+    // both products' accumulators share the 512 tensor-memory columns of one SM
+    if (N1 > CHAIN_MAX_N || N2 > CHAIN_MAX_N) return GEMM_ERR_UNSUPPORTED;
     // 16-byte rows: A and B hold K elements, E N1, C N2 fp32, D N2
     if ((K * 2) % 16 != 0 || (N1 * 2) % 16 != 0 || (N2 * 4) % 16 != 0 || (N2 * elem_bits(d) / 8) % 16 != 0)
         return GEMM_ERR_ALIGNMENT;
+    // CTA pairs (256-row tiles, each CTA taking in half of B's and E's rows) unless the rows fit
+    // one CTA tile or an operand's padded N is not a multiple of 32 (the pair's MMA shapes are
+    // kept to N = 32, 64, ..., 256)
+    const int64_t n1p = (N1 + 15) / 16 * 16, n2p = (N2 + 15) / 16 * 16;
+    const bool pair_ok = n1p % 32 == 0 && n2p % 32 == 0;
+    if ((flags & GEMM_FLAG_FORCE_2CTA) && !pair_ok) return GEMM_ERR_UNSUPPORTED;
 
     int dev = 0;
     cudaDeviceProp prop;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess)
         return GEMM_ERR_CUDA;
     if (prop.major != 10 || prop.minor != 3) return GEMM_ERR_UNSUPPORTED;
-    if (chain_prepare(d == GEMM_BF16) != cudaSuccess) return GEMM_ERR_CUDA;
+    const int cg = (flags & GEMM_FLAG_FORCE_2CTA) || (!(flags & GEMM_FLAG_FORCE_1CTA) && pair_ok && M > TILE_M) ? 2 : 1;
+    if (chain_prepare(d == GEMM_BF16, cg) != cudaSuccess) return GEMM_ERR_CUDA;
+    int clusters = 0;
+    if (chain_max_active_clusters(d == GEMM_BF16, cg, &clusters) != cudaSuccess || clusters <= 0)
+        return GEMM_ERR_CUDA;
 
     gemm_plan *p = new (std::nothrow) gemm_plan();
     if (!p) return GEMM_ERR_CUDA;
@@ -827,17 +837,17 @@ gemm_status gemm_chain_plan_create(gemm_plan_t *out, int64_t M, int64_t N1, int6
     p->sm_count = prop.multiProcessorCount;
     p->timeout_ns = 1000000000ull;
     p->family = FAMILY_CHAIN;
-    p->cta_group = 1;
-    p->stages = 4;
-    p->smem = chain_smem_bytes();
-    p->tile_n = (int)((N2 + 15) / 16 * 16);
+    p->cta_group = cg;
+    p->stages = chain_stages(cg);
+    p->smem = chain_smem_bytes(cg);
+    p->tile_n = (int)n2p;
     p->tile_k = TILE_K16;
     p->num_kb = (int)((K + TILE_K16 - 1) / TILE_K16);
-    p->tiles_m = (int)((M + TILE_M - 1) / TILE_M);
+    p->tiles_m = (int)((M + TILE_M * cg - 1) / (TILE_M * cg));
     p->tiles_n = 1;
     p->tiles = p->tiles_m;
-    p->capacity = p->sm_count;
-    p->grid = p->tiles < p->sm_count ? p->tiles : p->sm_count;
+    p->capacity = clusters;
+    p->grid = cg * (p->tiles < clusters ? p->tiles : clusters);
     p->splits = 1;
     if (cudaMalloc(&p->status, sizeof(int)) != cudaSuccess) {
         delete p;
@@ -860,10 +870,11 @@ gemm_status encode_chain_maps(gemm_plan *p, const void *A, const void *B, const 
     if (!encoder()) return GEMM_ERR_CUDA;
     std::memset(p->maps, 0, sizeof p->maps);
     const CUtensorMapDataType dt = tma_dtype(p->ab);
-    const uint32_t n1p = (uint32_t)((p->N + 15) / 16 * 16), n2p = (uint32_t)p->tile_n;
+    // B and E boxes: the rows one CTA holds (all of them, or half in a CTA pair)
+    const uint32_t n1p = (uint32_t)((p->N + 15) / 16 * 16), n2p = (uint32_t)p->tile_n, cg = (uint32_t)p->cta_group;
     bool ok = encode_2d(&p->maps[0], dt, 2, A, p->K, p->M, TILE_K16, TILE_M, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_2d(&p->maps[1], dt, 2, B, p->K, p->N, TILE_K16, n1p, CU_TENSOR_MAP_SWIZZLE_128B) &&
-              encode_2d(&p->maps[4], dt, 2, E, p->N, p->N2, TILE_K16, n2p, CU_TENSOR_MAP_SWIZZLE_128B);
+              encode_2d(&p->maps[1], dt, 2, B, p->K, p->N, TILE_K16, n1p / cg, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              encode_2d(&p->maps[4], dt, 2, E, p->N, p->N2, TILE_K16, n2p / cg, CU_TENSOR_MAP_SWIZZLE_128B);
     if (ok && C)
         ok = encode_2d(&p->maps[2], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, C, p->N2, p->M, EPI_COLS, 32,
                        CU_TENSOR_MAP_SWIZZLE_128B);
@@ -907,13 +918,14 @@ gemm_status gemm_chain_run(gemm_plan_t p, const void *A, const void *B, const vo
     cp.has_c = C != nullptr;
     cp.f16 = p->ab == GEMM_F16;
     const uint32_t bf = p->ab == GEMM_BF16 ? 1u : 0u;
-    cp.idesc1 = idesc_f16(bf, (uint32_t)TILE_M, (uint32_t)cp.n1p);
-    cp.idesc2 = idesc_f16(bf, (uint32_t)TILE_M, (uint32_t)cp.n2p);
+    cp.idesc1 = idesc_f16(bf, (uint32_t)(TILE_M * p->cta_group), (uint32_t)cp.n1p);
+    cp.idesc2 = idesc_f16(bf, (uint32_t)(TILE_M * p->cta_group), (uint32_t)cp.n2p);
     cp.status = p->status;
     cp.timeout_ns = p->timeout_ns;
     cp.fault = p->fault;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
-    if (chain_launch(p->d == GEMM_BF16, p->grid, p->maps, cp, stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (chain_launch(p->d == GEMM_BF16, p->cta_group, p->grid, p->maps, cp, stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
     if (p->flags & GEMM_FLAG_SYNC) {
         if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
         return gemm_plan_last_status(p);

@@ -6,12 +6,18 @@
 //                    16-bit elements per 32-bit column, the lower K index in the low half
 //     D = C + P·E    tcgen05.mma with A = P read from TMEM and E from shared memory,
 //                    fp32 accumulator in TMEM columns [256, 512)
-// so the intermediate never leaves the SM.  One CTA owns a 128-row tile at a
-// time and walks the tiles persistently.  Warp roles (192 threads):
-//   warp 0     TMA producer: per tile the K blocks of A and B, then the K blocks
-//              of E, through one STAGES-deep ring (a stage holds A 128 x 64 and
-//              B N1 x 64, or E N2 x 64; 128-byte swizzled rows).
-//   warp 1     allocates the 512 TMEM columns; lane 0 issues both products' MMAs.
+// so the intermediate never leaves the SM.  One CTA (CG = 1) or one CTA pair
+// (CG = 2, cta_group::2: 256 rows, each CTA holding its 128 rows of A, T, P and D
+// and half of B's and E's rows) owns a tile at a time and walks the tiles
+// persistently.  Pairs halve the B and E bytes each SM takes in per row of A: the
+// chain's main loop is bound by what one SM can take in (B is re-read by every
+// tile), not by the L2.  Warp roles (192 threads per CTA):
+//   warp 0     TMA producer (each CTA): per tile the K blocks of A and B, then the
+//              K blocks of E, through one STAGES-deep ring (a stage holds A 128 x 64
+//              and N1/CG rows of B, or N2/CG rows of E; 128-byte swizzled rows); a
+//              pair's copies count on the leader's full[s].
+//   warp 1     allocates the 512 TMEM columns; lane 0 (of the leader) issues both
+//              products' MMAs.
 //   warps 2-5  per tile: round T into P (tcgen05.ld, cvt, tcgen05.st), then the D
 //              epilogue (tcgen05.ld, + C, convert, TMA store), each warp in its own
 //              32-lane TMEM window.
@@ -22,14 +28,16 @@
 namespace gb300 {
 namespace {
 
-template <bool OUT_BF16_>
+template <bool OUT_BF16_, int CG_>
 struct ChainCfg {
     static constexpr bool OUT_BF16 = OUT_BF16_;
+    static constexpr int CG = CG_;
     static constexpr int THREADS = 192;
-    static constexpr int STAGES = 4;
     static constexpr int BK = 64;                                     // 16-bit K elements per stage
     static constexpr int A_BYTES = TILE_M * 128;                      // 16 KiB
-    static constexpr int STAGE_BYTES = A_BYTES + CHAIN_MAX_N * 128;   // 48 KiB: A and B, or E
+    // A and this CTA's rows of B, or of E: 48 KiB (single CTAs), 32 KiB (pairs)
+    static constexpr int STAGE_BYTES = A_BYTES + CHAIN_MAX_N / CG * 128;
+    static constexpr int STAGES = CG == 1 ? 4 : 6;
     static constexpr int EPI_BUF = 32 * EPI_COLS * 4;                 // one 32 x 32 fp32 box
     static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
     static constexpr int OFF_BAR = OFF_EPI + 4 * 2 * EPI_BUF;
@@ -40,6 +48,7 @@ struct ChainCfg {
     static constexpr uint32_t T_COL = 0, D_COL = 256;
     static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && OFF_EPI % 1024 == 0, "1024-byte aligned");
     static_assert(SMEM_BYTES <= 232448, "shared-memory budget");
+    static_assert(CG == 1 || CG == 2, "CTA group");
 };
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -54,19 +63,21 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                  const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                  const __grid_constant__ CUtensorMap tmE, const ChainParams p) {
     constexpr int STAGES = Cfg::STAGES;
+    constexpr int CG = Cfg::CG;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::OFF_BAR);
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
     uint64_t *tfull = bars + 2 * STAGES;   // first product complete (MMA -> epilogue)
-    uint64_t *pready = tfull + 1;          // P written into TMEM (epilogue -> MMA)
+    uint64_t *pready = tfull + 1;          // P written into TMEM (epilogue warps of the pair -> MMA)
     uint64_t *dfull = tfull + 2;           // second product complete (MMA -> epilogue, MMA)
-    uint64_t *dempty = tfull + 3;          // D read out of TMEM (epilogue -> MMA)
+    uint64_t *dempty = tfull + 3;          // D read out of TMEM (epilogue warps of the pair -> MMA)
     uint64_t *cload = tfull + 4;
     uint64_t *drain = cload + 8;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
@@ -84,22 +95,28 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(tfull, 1);
-        mbar_init(pready, 4);
+        mbar_init(pready, 4 * CG);
         mbar_init(dfull, 1);
-        mbar_init(dempty, 4);
+        mbar_init(dempty, 4 * CG);
         for (int i = 0; i < 8; ++i) mbar_init(&cload[i], 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
     if (warp == 1) {
-        tmem_alloc<1>(smem_addr(tmem_slot), 512);
-        tmem_relinquish<1>();
+        tmem_alloc<CG>(smem_addr(tmem_slot), 512);
+        tmem_relinquish<CG>();
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    const int tile0 = blockIdx.x / CG, tile_step = gridDim.x / CG;
+    // an epilogue warp's arrival on a barrier the leader's MMA thread waits for
+    auto arrive_leader = [&](uint64_t *bar) {
+        if constexpr (CG == 1) mbar_arrive(bar);
+        else mbar_arrive_remote(mapa_shared(smem_addr(bar), 0));
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -107,20 +124,25 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
-                const int m0 = t * TILE_M;
+            // a pair's copies land in each CTA's own ring and count on the leader's full[s]
+            auto load = [&](uint32_t dst, const CUtensorMap *m, uint32_t fb, int c0, int c1) {
+                if constexpr (CG == 1) tma_load_2d(dst, m, fb, c0, c1);
+                else tma_load_2d_pair(dst, m, mapa_shared(fb, 0), c0, c1);
+            };
+            for (int t = tile0; ok && t < p.tiles; t += tile_step) {
+                const int m0 = t * TILE_M * CG + (int)rank * TILE_M;
                 for (int kb = 0; kb < p.num_kb1 + p.num_kb2; ++kb) {
                     if (!W.wait(&empty[s], ph ^ 1u)) { ok = false; break; }
-                    const bool withhold = p.fault == 1 && t == (int)blockIdx.x && kb == 0;
+                    const bool withhold = p.fault == 1 && t == tile0 && kb == 0;
                     uint8_t *st = smem + s * Cfg::STAGE_BYTES;
                     const uint32_t fb = smem_addr(&full[s]);
-                    if (kb < p.num_kb1) {         // A rows m0.., B rows 0..n1p of K block kb
-                        if (!withhold) mbar_arrive_expect_tx(&full[s], Cfg::A_BYTES + p.n1p * 128);
-                        tma_load_2d(smem_addr(st), &tmA, fb, kb * Cfg::BK, m0);
-                        tma_load_2d(smem_addr(st + Cfg::A_BYTES), &tmB, fb, kb * Cfg::BK, 0);
-                    } else {                      // E rows 0..n2p of K block kb - num_kb1
-                        mbar_arrive_expect_tx(&full[s], p.n2p * 128);
-                        tma_load_2d(smem_addr(st), &tmE, fb, (kb - p.num_kb1) * Cfg::BK, 0);
+                    if (kb < p.num_kb1) {         // A rows m0.., this CTA's n1p/CG rows of B, K block kb
+                        if (rank == 0 && !withhold) mbar_arrive_expect_tx(&full[s], CG * Cfg::A_BYTES + p.n1p * 128);
+                        load(smem_addr(st), &tmA, fb, kb * Cfg::BK, m0);
+                        load(smem_addr(st + Cfg::A_BYTES), &tmB, fb, kb * Cfg::BK, (int)rank * (p.n1p / CG));
+                    } else {                      // this CTA's n2p/CG rows of E, K block kb - num_kb1
+                        if (rank == 0) mbar_arrive_expect_tx(&full[s], p.n2p * 128);
+                        load(smem_addr(st), &tmE, fb, (kb - p.num_kb1) * Cfg::BK, (int)rank * (p.n2p / CG));
                     }
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
@@ -128,13 +150,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------- MMA issue
-        if (lane == 0) {
+        if (rank == 0 && lane == 0) {
             const uint32_t t_tmem = tmem_base + Cfg::T_COL;
             const uint32_t d_tmem = tmem_base + Cfg::D_COL;
             int s = 0;
             uint32_t ph = 0, it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x, ++it) {
+            // completion of a stage (both CTAs' rings) and of each product (both CTAs' epilogues)
+            auto commit_all = [&](uint64_t *bar) {
+                if constexpr (CG == 1) tc_commit<1>(smem_addr(bar));
+                else tc_commit_pair(smem_addr(bar), 0x3);
+            };
+            for (int t = tile0; ok && t < p.tiles; t += tile_step, ++it) {
                 // T's columns are free once the previous tile's second product (which read
                 // P from them) has completed
                 if (it > 0 && !W.wait(dfull, (it - 1) & 1u)) break;
@@ -147,14 +174,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint64_t bd = smem_desc(st + Cfg::A_BYTES, 16, 1024, SWZ_128B);
 #pragma unroll
                     for (int k = 0; k < Cfg::BK / 16; ++k)   // 32 bytes of K = 2 descriptor units
-                        mma_f16<1>(t_tmem, ad + 2 * k, bd + 2 * k, p.idesc1, (kb != 0) | (k != 0));
-                    tc_commit<1>(smem_addr(&empty[s]));
+                        mma_f16<CG>(t_tmem, ad + 2 * k, bd + 2 * k, p.idesc1, (kb != 0) | (k != 0));
+                    commit_all(&empty[s]);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                tc_commit<1>(smem_addr(tfull));
-                // P is in TMEM, and the previous tile's D has been read out
-                if (!W.wait(pready, it & 1u) || !W.wait(dempty, (it & 1u) ^ 1u)) break;
+                commit_all(tfull);
+                // P is in TMEM, and the previous tile's D has been read out (in both CTAs: the
+                // peer's epilogue warps release-arrive, so acquire at cluster scope)
+                if (!W.wait<CG == 2>(pready, it & 1u) || !W.wait<CG == 2>(dempty, (it & 1u) ^ 1u)) break;
                 tc_fence_after_sync();
                 for (int j = 0; j < p.num_kb2; ++j) {
                     if (!W.wait(&full[s], ph)) { ok = false; break; }
@@ -163,16 +191,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < Cfg::BK / 16; ++k) {
                         const int kk = j * Cfg::BK + 16 * k;   // K index of the second product
-                        if (kk < p.n1p) mma_f16_ts(d_tmem, t_tmem + kk / 2, ed + 2 * k, p.idesc2, kk != 0);
+                        if (kk < p.n1p) mma_f16_ts<CG>(d_tmem, t_tmem + kk / 2, ed + 2 * k, p.idesc2, kk != 0);
                     }
-                    tc_commit<1>(smem_addr(&empty[s]));
+                    commit_all(&empty[s]);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
-                tc_commit<1>(smem_addr(dfull));
+                commit_all(dfull);
             }
             // every MMA this thread issued has finished before teardown
-            tc_commit<1>(smem_addr(drain));
+            tc_commit<CG>(smem_addr(drain));
             W.wait(drain, 0, false);
         }
     } else {
@@ -189,8 +217,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         // ec % 2, and its C load is that buffer's (ec / 2)-th
         uint32_t it = 0, ec = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x, ++it) {
-            const int m_warp = t * TILE_M + 32 * q;
+        for (int t = tile0; ok && t < p.tiles; t += tile_step, ++it) {
+            const int m_warp = t * TILE_M * CG + (int)rank * TILE_M + 32 * q;
             // P = round(T): chunk c of 32 fp32 columns becomes 16 columns of packed pairs at
             // column 16c, over columns whose T values this warp has already read
             if (!__all_sync(0xffffffffu, W.wait(tfull, it & 1u))) break;
@@ -210,7 +238,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(pready);
+            if (lane == 0) arrive_leader(pready);
 
             // D = C + P·E: 32 x 32 boxes that lie wholly outside D are neither loaded nor stored
             const int chunks_in = m_warp < p.M ? (p.N2 + EPI_COLS - 1) / EPI_COLS : 0;
@@ -230,7 +258,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if (j == d_chunks - 1) {      // D's columns are free once every chunk is in registers
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(dempty);
+                    if (lane == 0) arrive_leader(dempty);
                 }
                 if (j >= chunks_in) continue;
                 const uint32_t cur = ec & 1u;
@@ -295,32 +323,77 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         for (int i = 0; i < 64; ++i) __nanosleep(1000);
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (CG == 2) cluster_sync(); else __syncthreads();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc<1>(tmem_base, 512);
+        tmem_dealloc<CG>(tmem_base, 512);
     }
 }
 
-template <bool OUT_BF16>
+template <class Cfg>
 cudaError_t launch_chain(int grid, const CUtensorMap *maps, const ChainParams &p, cudaStream_t stream) {
-    using Cfg = ChainCfg<OUT_BF16>;
-    chain_kernel<Cfg><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(maps[0], maps[1], maps[2], maps[3], maps[4], p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute attr[1];
+    lc.gridDim = dim3(grid, 1, 1);
+    lc.blockDim = dim3(Cfg::THREADS, 1, 1);
+    lc.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    lc.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = Cfg::CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    void *args[6] = {(void *)&maps[0], (void *)&maps[1], (void *)&maps[2], (void *)&maps[3], (void *)&maps[4],
+                     (void *)&p};
+    return cudaLaunchKernelExC(&lc, reinterpret_cast<const void *>(&chain_kernel<Cfg>), args);
+}
+
+template <class Cfg>
+const void *chain_fn() {
+    return reinterpret_cast<const void *>(&chain_kernel<Cfg>);
+}
+
+const void *chain_fn(int out_bf16, int cta_group) {
+    if (cta_group == 2) return out_bf16 ? chain_fn<ChainCfg<true, 2>>() : chain_fn<ChainCfg<false, 2>>();
+    return out_bf16 ? chain_fn<ChainCfg<true, 1>>() : chain_fn<ChainCfg<false, 1>>();
 }
 
 }  // namespace
 
-int chain_smem_bytes() { return ChainCfg<false>::SMEM_BYTES; }
-
-cudaError_t chain_prepare(int out_bf16) {
-    const void *fn = out_bf16 ? reinterpret_cast<const void *>(&chain_kernel<ChainCfg<true>>)
-                              : reinterpret_cast<const void *>(&chain_kernel<ChainCfg<false>>);
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, chain_smem_bytes());
+int chain_smem_bytes(int cta_group) {
+    return cta_group == 2 ? ChainCfg<false, 2>::SMEM_BYTES : ChainCfg<false, 1>::SMEM_BYTES;
 }
 
-cudaError_t chain_launch(int out_bf16, int grid, const CUtensorMap *maps, const ChainParams &p, cudaStream_t stream) {
-    return out_bf16 ? launch_chain<true>(grid, maps, p, stream) : launch_chain<false>(grid, maps, p, stream);
+int chain_stages(int cta_group) { return cta_group == 2 ? ChainCfg<false, 2>::STAGES : ChainCfg<false, 1>::STAGES; }
+
+cudaError_t chain_prepare(int out_bf16, int cta_group) {
+    return cudaFuncSetAttribute(chain_fn(out_bf16, cta_group), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                chain_smem_bytes(cta_group));
+}
+
+cudaError_t chain_max_active_clusters(int out_bf16, int cta_group, int *clusters) {
+    cudaLaunchConfig_t lc = {};
+    cudaLaunchAttribute attr[1];
+    lc.gridDim = dim3(2 * 1024, 1, 1);
+    lc.blockDim = dim3(192, 1, 1);
+    lc.dynamicSmemBytes = chain_smem_bytes(cta_group);
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cta_group;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(clusters, chain_fn(out_bf16, cta_group), &lc);
+}
+
+cudaError_t chain_launch(int out_bf16, int cta_group, int grid, const CUtensorMap *maps, const ChainParams &p,
+                         cudaStream_t stream) {
+    if (cta_group == 2)
+        return out_bf16 ? launch_chain<ChainCfg<true, 2>>(grid, maps, p, stream)
+                        : launch_chain<ChainCfg<false, 2>>(grid, maps, p, stream);
+    return out_bf16 ? launch_chain<ChainCfg<true, 1>>(grid, maps, p, stream)
+                    : launch_chain<ChainCfg<false, 1>>(grid, maps, p, stream);
 }
 
 }  // namespace gb300

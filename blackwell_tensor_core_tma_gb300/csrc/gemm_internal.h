@@ -149,7 +149,7 @@ struct ChainParams {
     int n1p, n2p;        // N1 and N2 rounded up to the MMA's N granule (16)
     int num_kb1;         // 64-element K blocks of the first product
     int num_kb2;         // 64-element K blocks of the second product (over n1p)
-    int tiles;           // 128-row tiles of D
+    int tiles;           // tiles of D (128 rows per CTA, 256 per CTA pair)
     int has_c;
     int f16;             // operands (and the rounded intermediate) fp16, else bf16
     uint32_t idesc1, idesc2;
@@ -158,9 +158,13 @@ struct ChainParams {
     int fault;
 };
 constexpr int CHAIN_MAX_N = 256;   // N1 and N2 limits: both products' accumulators share 512 TMEM columns
-int chain_smem_bytes();
-cudaError_t chain_prepare(int out_bf16);
-cudaError_t chain_launch(int out_bf16, int grid, const CUtensorMap *maps, const ChainParams &p, cudaStream_t stream);
+int chain_smem_bytes(int cta_group);
+int chain_stages(int cta_group);
+cudaError_t chain_prepare(int out_bf16, int cta_group);
+cudaError_t chain_max_active_clusters(int out_bf16, int cta_group, int *clusters);
+// grid: CTAs (a multiple of cta_group); tiles of 128 * cta_group rows
+cudaError_t chain_launch(int out_bf16, int cta_group, int grid, const CUtensorMap *maps, const ChainParams &p,
+                         cudaStream_t stream);
 
 constexpr int EPI_COLS = 32;  // epilogue chunk width (columns)
 

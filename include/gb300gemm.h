@@ -286,9 +286,13 @@ gemm_status gemm_run_noalloc(int64_t M, int64_t N, int64_t K, gemm_dtype ab, gem
  * E is N1 x N2 column-major (element (j,n) at E[n*N1 + j]), C is M x N2 fp32
  * row-major or NULL, D is M x N2 row-major fp32 or bf16.  ab (A, B, E and P) is
  * GEMM_F16 or GEMM_BF16.  1 <= N1, N2 <= 256 (both products' accumulators share
- * one SM's 512 tensor-memory columns; otherwise GEMM_ERR_UNSUPPORTED, as is
- * GEMM_FLAG_FORCE_2CTA); K and N1 multiples of 8, N2 a multiple of 4 (fp32 D)
- * or 8 (bf16 D), else GEMM_ERR_ALIGNMENT.  The plan works with
+ * one SM's 512 tensor-memory columns; otherwise GEMM_ERR_UNSUPPORTED); K and N1
+ * multiples of 8, N2 a multiple of 4 (fp32 D) or 8 (bf16 D), else
+ * GEMM_ERR_ALIGNMENT.  The plan runs CTA pairs (256-row tiles, each CTA holding
+ * half of B's and E's rows) when M > 128 and N1 and N2, rounded up to multiples of
+ * 16, are multiples of 32, else single CTAs; GEMM_FLAG_FORCE_1CTA and
+ * GEMM_FLAG_FORCE_2CTA choose the form (GEMM_FLAG_FORCE_2CTA with an N1 or N2 that
+ * does not round to a multiple of 32: GEMM_ERR_UNSUPPORTED).  The plan works with
  * gemm_plan_last_status, gemm_plan_get_info, gemm_plan_set_timeout and
  * gemm_plan_destroy; gemm_run / gemm_run_host reject it (GEMM_ERR_INVALID_ARG),
  * and gemm_plan_set_split_k accepts only 0 or 1.  Pointers, streams, errors and

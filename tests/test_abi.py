@@ -106,7 +106,8 @@ def test_no_cpu_fallback_without_library(monkeypatch, tmp_path):
     ((128, 264, 64, 64), {}, gemm.GEMM_ERR_UNSUPPORTED),                    # N1 > 256
     ((128, 64, 272, 64), {}, gemm.GEMM_ERR_UNSUPPORTED),                    # N2 > 256
     ((128, 64, 64, 64), {"ab": "e4m3"}, gemm.GEMM_ERR_UNSUPPORTED),
-    ((128, 64, 64, 64), {"flags": gemm.GEMM_FLAG_FORCE_2CTA}, gemm.GEMM_ERR_UNSUPPORTED),
+    ((128, 64, 48, 64), {"flags": gemm.GEMM_FLAG_FORCE_2CTA}, gemm.GEMM_ERR_UNSUPPORTED),  # pair N2 not % 32
+    ((128, 40, 64, 64), {"flags": gemm.GEMM_FLAG_FORCE_2CTA}, gemm.GEMM_ERR_UNSUPPORTED),  # pair N1 pads to 48
     ((128, 64, 64, 60), {}, gemm.GEMM_ERR_ALIGNMENT),                       # K rows of 120 bytes
     ((128, 60, 64, 64), {}, gemm.GEMM_ERR_ALIGNMENT),                       # E rows of N1 = 60
     ((128, 64, 12, 64), {"d": "bf16"}, gemm.GEMM_ERR_ALIGNMENT),            # bf16 D rows of 24 bytes

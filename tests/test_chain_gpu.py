@@ -23,18 +23,38 @@ def _cuda():
     gemm.lib()
 
 
+def _pads_to_32(n):
+    return (n + 15) // 16 * 16 % 32 == 0
+
+
+@pytest.mark.parametrize("flags", [0, gemm.GEMM_FLAG_FORCE_1CTA], ids=["default", "1cta"])
 @pytest.mark.parametrize("M,K,N1,N2,ab,d", [
     (128, 64, 16, 8, "bf16", "f32"),          # one tile, one K block, the smallest N1 and N2
     (300, 520, 200, 136, "bf16", "f32"),      # ragged M and K, N1 and N2 not multiples of 32
     (1000, 2048, 256, 256, "bf16", "bf16"),   # the full TMEM split, bf16 D
     (260, 1024, 72, 40, "f16", "f32"),        # fp16 operands and intermediate
     (512, 136, 248, 256, "f16", "bf16"),      # N1 rounds up to 256 inside the kernel
+    (300, 520, 192, 96, "bf16", "f32"),       # pairs: the last pair tile holds 44 rows, its second CTA none
+    (1000, 264, 32, 64, "f16", "bf16"),       # pairs: the narrowest products (16 and 32 rows of B and E per CTA)
+    (777, 1000, 160, 224, "bf16", "f32"),     # pairs: ragged M and K, N1 and N2 multiples of 32
 ])
-def test_chain_parity(M, K, N1, N2, ab, d):
+def test_chain_parity(M, K, N1, N2, ab, d, flags):
+    """Both tile forms: CTA pairs (the default when M spans more than one 128-row tile and N1 and
+    N2 pad to multiples of 32) and single CTAs."""
     w = synth.scaled_chain(CW, M, N1, N2, K, ab=ab, d=d)
-    x, D, info, st, intact = gpucase.run_chain(w, guard=512)
+    x, D, info, st, intact = gpucase.run_chain(w, flags=flags, guard=512)
     assert st == gemm.GEMM_OK and intact
-    assert info["cta_group"] == 1 and info["launches_per_run"] == 1
+    pair = flags == 0 and M > 128 and _pads_to_32(N1) and _pads_to_32(N2)
+    assert info["cta_group"] == (2 if pair else 1) and info["launches_per_run"] == 1
+    gpucase.check_chain(w, x, D)
+
+
+@pytest.mark.parametrize("M,K,N1,N2", [(128, 64, 64, 32), (100, 200, 256, 256), (64, 128, 96, 128)])
+def test_chain_forced_pairs_on_one_tile(M, K, N1, N2):
+    """A pair forced onto rows that fit one CTA tile: the second CTA's rows all lie outside D."""
+    w = synth.scaled_chain(CW, M, N1, N2, K)
+    x, D, info, st, intact = gpucase.run_chain(w, flags=gemm.GEMM_FLAG_FORCE_2CTA, guard=256)
+    assert st == gemm.GEMM_OK and intact and info["cta_group"] == 2
     gpucase.check_chain(w, x, D)
 
 
@@ -48,7 +68,7 @@ def test_chain_c_none_and_repeat():
 def test_chain_full_size_sampled_rows():
     w = CW
     x, D, info, st, intact = gpucase.run_chain(w, guard=1024)
-    assert st == gemm.GEMM_OK and intact
+    assert st == gemm.GEMM_OK and intact and info["cta_group"] == 2
     rng = np.random.default_rng(0)
     edges = [r for t in range(0, w.M, 128 * 37) for r in (t, t + 31, t + 32, t + 127) if r < w.M]
     rows = np.unique(np.concatenate([edges, [w.M - 1], rng.integers(0, w.M, 160)]))
@@ -85,8 +105,8 @@ def test_chain_timeout_and_recovery():
 
 
 @pytest.mark.parametrize("M,K,N1,N2,d,c_none", [
-    (1000, 520, 200, 136, "bf16", False),     # ragged, bf16 D
-    (640, 1024, 256, 256, "f32", True),       # C absent
+    (1000, 520, 200, 136, "bf16", False),     # ragged, bf16 D (single CTAs)
+    (640, 1024, 256, 256, "f32", True),       # C absent (CTA pairs)
 ])
 def test_chain_host_run(M, K, N1, N2, d, c_none):
     """gemm_chain_run_host: the same result from pinned host buffers as from device buffers."""

@@ -92,10 +92,38 @@ def _chain_cases(n=20, seed=7):
 CHAIN_CASES = _chain_cases()
 
 
+def _chain_pair_cases(n=12, seed=8):
+    """Shapes the plan runs as CTA pairs: more than 128 rows, N1 and N2 multiples of 32."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        d = "bf16" if rng.integers(2) else "f32"
+        ab = "bf16" if rng.integers(2) else "f16"
+        M = int(rng.integers(129, 1400))
+        K = int(rng.integers(1, 1200)) // 8 * 8 or 8
+        N1 = 32 * int(rng.integers(1, 9))
+        N2 = 32 * int(rng.integers(1, 9))
+        out.append((M, K, N1, N2, ab, d, bool(rng.integers(2))))
+    return out
+
+
+CHAIN_PAIR_CASES = _chain_pair_cases()
+
+
 @pytest.mark.parametrize("M,K,N1,N2,ab,d,with_c", CHAIN_CASES,
                          ids=[f"{c[0]}x{c[1]}-{c[2]}x{c[3]}-{c[4]}-{c[5]}-{'C' if c[6] else 'noC'}" for c in CHAIN_CASES])
 def test_random_chain(M, K, N1, N2, ab, d, with_c):
     cw = synth.scaled_chain(synth.CHAIN_WORKLOADS["chain_bf16_32768x4096_256x256_bf16out"], M, N1, N2, K, ab=ab, d=d)
     x, D, info, st, intact = gpucase.run_chain(cw, c_none=not with_c, guard=128)
     assert st == gemm.GEMM_OK and intact
+    gpucase.check_chain(cw, x, D, c_none=not with_c)
+
+
+@pytest.mark.parametrize("M,K,N1,N2,ab,d,with_c", CHAIN_PAIR_CASES,
+                         ids=[f"{c[0]}x{c[1]}-{c[2]}x{c[3]}-{c[4]}-{c[5]}-{'C' if c[6] else 'noC'}"
+                              for c in CHAIN_PAIR_CASES])
+def test_random_chain_pairs(M, K, N1, N2, ab, d, with_c):
+    cw = synth.scaled_chain(synth.CHAIN_WORKLOADS["chain_bf16_32768x4096_256x256_bf16out"], M, N1, N2, K, ab=ab, d=d)
+    x, D, info, st, intact = gpucase.run_chain(cw, c_none=not with_c, guard=128)
+    assert st == gemm.GEMM_OK and intact and info["cta_group"] == 2
     gpucase.check_chain(cw, x, D, c_none=not with_c)
