@@ -360,6 +360,8 @@ def run_ours(args, rank, world, local_rank):
     flags = {0: 0, 1: gemm.GEMM_FLAG_FORCE_1CTA, 2: gemm.GEMM_FLAG_FORCE_2CTA}[args.cta_group]
     plan = gemm.Plan(w.M, w.N, w.K, w.ab, w.d, w.block_scaled, flags, a_row_major=w.a_row_major,
                      b_row_major=w.b_row_major)
+    if args.stream_k is not None:
+        plan.set_stream_k(args.stream_k)
     info = plan.info
     stream = torch.cuda.Stream(device=dev)
 
@@ -487,6 +489,8 @@ def run_ours_chain(args, rank, world, local_rank):
     d_t = torch.bfloat16 if w.d == "bf16" else torch.float32
     D = torch.empty((w.M, w.N2), dtype=d_t, device=dev)
     plan = gemm.ChainPlan(w.M, w.N1, w.N2, w.K, w.ab, w.d)
+    if args.stream_k is not None:
+        plan.set_stream_k(args.stream_k)
     info = plan.info
     stream = torch.cuda.Stream(device=dev)
 
@@ -714,6 +718,8 @@ def main(argv=None):
                                                   "other sizes (profiling)")
     ap.add_argument("--cta-group", type=int, choices=[0, 1, 2], default=0,
                     help="force single CTAs (1) or CTA pairs (2); 0 = the plan's choice")
+    ap.add_argument("--stream-k", type=int, choices=[0, 1], default=None,
+                    help="gemm_plan_set_stream_k: 0 = never, 1 = where the plan's rule takes it (the default)")
     ap.add_argument("--a-col-major", action="store_true", help="store A column-major (M contiguous)")
     ap.add_argument("--b-row-major", action="store_true", help="store B row-major (N contiguous)")
     ap.add_argument("--e2e-steps", type=int, default=10)

@@ -5,8 +5,9 @@ then nvcc links them (with the static CUDA runtime) into a shared library
 next to this file.  Nothing is installed anywhere else.
 
 Variant "trace" (libgb300gemm_trace.so, compiled with GB300_TRACE=1) keeps the
-kernels' per-role clock counters (gemm_testing_set_trace); the default library
-compiles them out.  The binding loads the variant named by the environment
+kernels' per-role clock counters (gemm_testing_set_trace); variant "checks"
+(libgb300gemm_checks.so) keeps the kernels' on-device coordinate checks and uses
+other ring depths; the default library compiles both out.  The binding loads the variant named by the environment
 variable GB300GEMM_VARIANT (unset: the default library).
 """
 
@@ -23,7 +24,14 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libgb300gemm.so")
-VARIANTS = {"": [], "trace": ["-DGB300_TRACE=1"]}
+# "checks": the kernels' on-device coordinate checks (GEMM_ERR_CHECK), with ring depths other
+# than the default ones so that a run of the tests on it also exercises other ring phases
+VARIANTS = {
+    "": [],
+    "trace": ["-DGB300_TRACE=1"],
+    "checks": ["-DGB300_CHECKS=1", "-DGB300_F16_CG1_STAGES=3", "-DGB300_F16_CG2_STAGES=5",
+               "-DGB300_MXF8_PAIR_STAGES=5", "-DGB300_MXF4_PAIR_STAGES=4", "-DGB300_NVF4_PAIR_STAGES=4"],
+}
 
 
 def lib_path(variant: str = "") -> str:

@@ -75,6 +75,7 @@ struct gemm_plan {
     int sk;                   // stream-K chosen
     int sk_dp_tiles;          // stream-K: tiles the units take whole before their spans
     int *sk_flags;            // stream-K: one flag per (slot, CTA of the group)
+    float *sk_part;           // chain stream-K: one partial T per (slot, CTA of the group)
     uint32_t epoch;           // stream-K: runs so far (the value a run's flags carry)
     int tile_n;
     int epi_box;              // columns of the epilogue's C / D boxes (32 or 16)
@@ -379,6 +380,37 @@ gemm_status choose_splits(gemm_plan *p) {
     return GEMM_OK;
 }
 
+// Chain plans: stream-K over the first product (on request only: gemm_plan_set_stream_k)
+// when the tiles make more than one wave but not a whole number of them (fewer than 4) and
+// K is long enough that a handed-over partial T (n1p fp32 columns of 128 rows per CTA) is
+// small next to the work it balances.  Measured on 32768 x 4096, N1 = N2 = 256 (pairs, 128
+// tiles on 76 units) and 20480 x 1024: 8-10 % slower than whole tiles, so it is off by default.
+#ifndef GB300_CHAIN_SK_MIN_KB
+#define GB300_CHAIN_SK_MIN_KB 16
+#endif
+gemm_status choose_chain_schedule(gemm_plan *p) {
+    const int units = p->grid / p->cta_group;
+    p->sk = p->sk_request && p->tiles > units && p->tiles % units != 0 && p->tiles < 4 * units &&
+            p->num_kb >= GB300_CHAIN_SK_MIN_KB;
+    if (!p->sk) return GEMM_OK;
+    p->sk_dp_tiles = (p->tiles / units - 1) * units;
+    if (!p->sk_flags) {
+        const size_t row = (size_t)((p->N + 31) / 32 * 32);     // whole 32-column chunks of T
+        const size_t fl = (size_t)units * p->cta_group * sizeof(int);
+        const size_t pt = (size_t)units * p->cta_group * TILE_M * row * sizeof(float);
+        if (cudaMalloc(&p->sk_flags, fl) != cudaSuccess || cudaMemset(p->sk_flags, 0, fl) != cudaSuccess ||
+            cudaMalloc(&p->sk_part, pt) != cudaSuccess) {
+            cudaFree(p->sk_flags);
+            cudaFree(p->sk_part);
+            p->sk_flags = nullptr;
+            p->sk_part = nullptr;
+            p->sk = 0;
+            return GEMM_ERR_CUDA;
+        }
+    }
+    return GEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -391,6 +423,7 @@ const char *gemm_status_string(gemm_status s) {
     case GEMM_ERR_ALIGNMENT: return "pointer or row stride not a multiple of 16 bytes";
     case GEMM_ERR_CUDA: return "CUDA call failed";
     case GEMM_ERR_TIMEOUT: return "a bounded wait inside the kernel ran out";
+    case GEMM_ERR_CHECK: return "an on-device check of a copy coordinate failed";
     default: return "unknown status";
     }
 }
@@ -766,8 +799,8 @@ gemm_status gemm_plan_set_split_k(gemm_plan_t p, int splits) {
 
 gemm_status gemm_plan_set_stream_k(gemm_plan_t p, int enable) {
     if (!p || enable < 0 || enable > 1) return GEMM_ERR_INVALID_ARG;
-    if (p->family == FAMILY_CHAIN) return GEMM_OK;
     p->sk_request = enable;
+    if (p->family == FAMILY_CHAIN) return choose_chain_schedule(p);
     return choose_splits(p);
 }
 
@@ -785,6 +818,7 @@ gemm_status gemm_plan_destroy(gemm_plan_t p) {
     cudaFree(p->ws_a);
     cudaFree(p->ws_b);
     cudaFree(p->sk_flags);
+    cudaFree(p->sk_part);
     cudaFree(p->clk_meter);
     delete p;
     return GEMM_OK;
@@ -849,13 +883,13 @@ gemm_status gemm_chain_plan_create(gemm_plan_t *out, int64_t M, int64_t N1, int6
     p->capacity = clusters;
     p->grid = cg * (p->tiles < clusters ? p->tiles : clusters);
     p->splits = 1;
+    p->sk_request = 0;
     if (cudaMalloc(&p->status, sizeof(int)) != cudaSuccess) {
         delete p;
         return GEMM_ERR_CUDA;
     }
-    if (cudaMemset(p->status, 0, sizeof(int)) != cudaSuccess) {
-        cudaFree(p->status);
-        delete p;
+    if (cudaMemset(p->status, 0, sizeof(int)) != cudaSuccess || choose_chain_schedule(p) != GEMM_OK) {
+        gemm_plan_destroy(p);
         return GEMM_ERR_CUDA;
     }
     *out = p;
@@ -923,6 +957,15 @@ gemm_status gemm_chain_run(gemm_plan_t p, const void *A, const void *B, const vo
     cp.status = p->status;
     cp.timeout_ns = p->timeout_ns;
     cp.fault = p->fault;
+    if (p->sk) {
+        cp.sk = 1;
+        cp.sk_dp_tiles = p->sk_dp_tiles;
+        cp.sk_units = p->grid / p->cta_group;
+        cp.epoch = (int)(++p->epoch & 0x7FFFFFFF);
+        if (cp.epoch == 0) cp.epoch = p->epoch = 1;
+        cp.sk_flags = p->sk_flags;
+        cp.sk_part = p->sk_part;
+    }
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(cuda_stream);
     if (chain_launch(p->d == GEMM_BF16, p->cta_group, p->grid, p->maps, cp, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;
@@ -1017,9 +1060,10 @@ gemm_status gemm_testing_set_trace(gemm_plan_t p, void *dev_buffer, int64_t byte
 }
 
 // Test hook (declared in include/gb300gemm_testing.h): make the next runs'
-// producer withhold one arrival so that a bounded wait runs out.
+// producer withhold one arrival so that a bounded wait runs out (1), or shift its A
+// rows past the tiled extent (2).
 gemm_status gemm_testing_set_fault(gemm_plan_t p, int fault) {
-    if (!p || fault < 0 || fault > 1) return GEMM_ERR_INVALID_ARG;
+    if (!p || fault < 0 || fault > 2 || (fault == 2 && p->family == FAMILY_CHAIN)) return GEMM_ERR_INVALID_ARG;
     p->fault = fault;
     return GEMM_OK;
 }

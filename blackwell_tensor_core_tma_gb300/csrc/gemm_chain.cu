@@ -6,7 +6,8 @@
 //                    16-bit elements per 32-bit column, the lower K index in the low half
 //     D = C + P·E    tcgen05.mma with A = P read from TMEM and E from shared memory,
 //                    fp32 accumulator in TMEM columns [256, 512)
-// so the intermediate never leaves the SM.  One CTA (CG = 1) or one CTA pair
+// so the intermediate never leaves the SM (except, with stream-K, the partial T of a
+// tile cut between two units, which goes through global memory once).  One CTA (CG = 1) or one CTA pair
 // (CG = 2, cta_group::2: 256 rows, each CTA holding its 128 rows of A, T, P and D
 // and half of B's and E's rows) owns a tile at a time and walks the tiles
 // persistently.  Pairs halve the B and E bytes each SM takes in per row of A: the
@@ -41,8 +42,8 @@ struct ChainCfg {
     static constexpr int EPI_BUF = 32 * EPI_COLS * 4;                 // one 32 x 32 fp32 box
     static constexpr int OFF_EPI = STAGES * STAGE_BYTES;
     static constexpr int OFF_BAR = OFF_EPI + 4 * 2 * EPI_BUF;
-    // full[STAGES], empty[STAGES], tfull, pready, dfull, dempty, cload[4][2], drain
-    static constexpr int NBAR = 2 * STAGES + 4 + 8 + 1;
+    // full[STAGES], empty[STAGES], tfull, pready, dfull, dempty, cload[4][2], drain, epi_sync
+    static constexpr int NBAR = 2 * STAGES + 4 + 8 + 2;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;               // tmem base slot, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;           // + alignment slack
     static constexpr uint32_t T_COL = 0, D_COL = 256;
@@ -56,6 +57,54 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+
+// The pieces one unit (CTA or CTA pair) processes, in order (every role walks the same
+// sequence; Work and the roles are the GEMM kernels').  Without stream-K: whole tiles
+// unit0, unit0 + step, ...  With stream-K: the whole tiles below sk_dp_tiles the same way,
+// then the unit's span of the remaining tiles' first-product k-blocks.  A ROLE_TILE or
+// ROLE_FINAL piece ends with the rounding, the second product and D; a ROLE_EARLY piece
+// (the end of a tile whose start another unit computes) only hands its partial T over.
+struct ChainIter {
+    int unit, step, u;
+    int64_t g, g_end;
+    __device__ __forceinline__ ChainIter(const ChainParams &p, int unit0, int step0)
+        : unit(unit0), step(step0), u(unit0) {
+        g = g_end = 0;
+        if (p.sk) {
+            const int64_t base = (int64_t)p.sk_dp_tiles * p.num_kb1;
+            const int64_t total = (int64_t)(p.tiles - p.sk_dp_tiles) * p.num_kb1;
+            g = base + (int64_t)unit0 * total / p.sk_units;
+            g_end = base + (int64_t)(unit0 + 1) * total / p.sk_units;
+        }
+    }
+    __device__ __forceinline__ bool next(const ChainParams &p, Work &w) {
+        if (u < (p.sk ? p.sk_dp_tiles : p.tiles)) {
+            w.tm = u;
+            w.tn = 0;
+            w.kb0 = 0;
+            w.kb1 = p.num_kb1;
+            w.role = ROLE_TILE;
+            w.slot = 0;
+            u += step;
+            return true;
+        }
+        if (!p.sk || g >= g_end) return false;
+        const int t = (int)(g / p.num_kb1);
+        const int k0 = (int)(g - (int64_t)t * p.num_kb1);
+        const int k1 = (int)min((int64_t)p.num_kb1, (int64_t)k0 + (g_end - g));
+        w.tm = t;
+        w.tn = 0;
+        w.kb0 = k0;
+        w.kb1 = k1;
+        // a span is at least one tile long, so only its first piece can start inside a tile
+        // (this unit publishes it: slot = unit) and only its last can end inside one (the
+        // next unit publishes the rest: slot = unit + 1)
+        w.role = (k0 == 0 && k1 == p.num_kb1) ? ROLE_TILE : (k0 > 0 ? ROLE_EARLY : ROLE_FINAL);
+        w.slot = k0 > 0 ? unit : unit + 1;
+        g += k1 - k0;
+        return true;
+    }
+};
 
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
@@ -80,6 +129,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
     uint64_t *dempty = tfull + 3;          // D read out of TMEM (epilogue warps of the pair -> MMA)
     uint64_t *cload = tfull + 4;
     uint64_t *drain = cload + 8;
+    uint64_t *epi_sync = drain + 1;        // every epilogue warp stored its rows of a partial T
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Cfg::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + Cfg::OFF_MISC + 4);
     const Waiter W{abort_flag, p.status, p.timeout_ns};
@@ -100,6 +150,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         mbar_init(dempty, 4 * CG);
         for (int i = 0; i < 8; ++i) mbar_init(&cload[i], 1);
         mbar_init(drain, 1);
+        mbar_init(epi_sync, 4);
         *abort_flag = 0;
         fence_mbarrier_init();
     }
@@ -129,23 +180,34 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 if constexpr (CG == 1) tma_load_2d(dst, m, fb, c0, c1);
                 else tma_load_2d_pair(dst, m, mapa_shared(fb, 0), c0, c1);
             };
-            for (int t = tile0; ok && t < p.tiles; t += tile_step) {
-                const int m0 = t * TILE_M * CG + (int)rank * TILE_M;
-                for (int kb = 0; kb < p.num_kb1 + p.num_kb2; ++kb) {
+            ChainIter itr(p, tile0, tile_step);
+            Work wk;
+            bool first_piece = true;
+            while (ok && itr.next(p, wk)) {
+                const int m0 = wk.tm * TILE_M * CG + (int)rank * TILE_M;
+                // the piece's first-product k-blocks, then (unless it only hands a partial T
+                // over) the second product's
+                const int n1 = wk.kb1 - wk.kb0, n = n1 + (wk.role == ROLE_EARLY ? 0 : p.num_kb2);
+                for (int i = 0; i < n; ++i) {
                     if (!W.wait(&empty[s], ph ^ 1u)) { ok = false; break; }
-                    const bool withhold = p.fault == 1 && t == tile0 && kb == 0;
+                    const bool withhold = p.fault == 1 && first_piece && i == 0;
                     uint8_t *st = smem + s * Cfg::STAGE_BYTES;
                     const uint32_t fb = smem_addr(&full[s]);
+                    const int kb = i < n1 ? wk.kb0 + i : p.num_kb1 + (i - n1);
                     if (kb < p.num_kb1) {         // A rows m0.., this CTA's n1p/CG rows of B, K block kb
                         if (rank == 0 && !withhold) mbar_arrive_expect_tx(&full[s], CG * Cfg::A_BYTES + p.n1p * 128);
-                        load(smem_addr(st), &tmA, fb, kb * Cfg::BK, m0);
-                        load(smem_addr(st + Cfg::A_BYTES), &tmB, fb, kb * Cfg::BK, (int)rank * (p.n1p / CG));
+                        const int x = checked_x<2>(p.status, kb * Cfg::BK, p.num_kb1 * Cfg::BK);
+                        load(smem_addr(st), &tmA, fb, x, checked_y(p.status, m0, p.tiles * TILE_M * CG));
+                        load(smem_addr(st + Cfg::A_BYTES), &tmB, fb, x,
+                             checked_y(p.status, (int)rank * (p.n1p / CG), p.n1p));
                     } else {                      // this CTA's n2p/CG rows of E, K block kb - num_kb1
                         if (rank == 0) mbar_arrive_expect_tx(&full[s], p.n2p * 128);
-                        load(smem_addr(st), &tmE, fb, (kb - p.num_kb1) * Cfg::BK, (int)rank * (p.n2p / CG));
+                        load(smem_addr(st), &tmE, fb, checked_x<2>(p.status, (kb - p.num_kb1) * Cfg::BK, p.num_kb2 * Cfg::BK),
+                             checked_y(p.status, (int)rank * (p.n2p / CG), p.n2p));
                     }
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
+                first_piece = false;
             }
         }
     } else if (warp == 1) {
@@ -154,19 +216,24 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             const uint32_t t_tmem = tmem_base + Cfg::T_COL;
             const uint32_t d_tmem = tmem_base + Cfg::D_COL;
             int s = 0;
-            uint32_t ph = 0, it = 0;
+            // it counts pieces (the phases of tfull, pready and dfull), nd the pieces with a
+            // second product (the phases of dempty: a piece that only hands its partial T over
+            // has no D, and its epilogue does not arrive on dempty)
+            uint32_t ph = 0, it = 0, nd = 0;
             bool ok = true;
             // completion of a stage (both CTAs' rings) and of each product (both CTAs' epilogues)
             auto commit_all = [&](uint64_t *bar) {
                 if constexpr (CG == 1) tc_commit<1>(smem_addr(bar));
                 else tc_commit_pair(smem_addr(bar), 0x3);
             };
-            for (int t = tile0; ok && t < p.tiles; t += tile_step, ++it) {
-                // T's columns are free once the previous tile's second product (which read
-                // P from them) has completed
+            ChainIter itr(p, tile0, tile_step);
+            Work wk;
+            for (; ok && itr.next(p, wk); ++it) {
+                // T's columns are free once the previous piece's second product (which read
+                // P from them) has completed, or its partial T has been read out
                 if (it > 0 && !W.wait(dfull, (it - 1) & 1u)) break;
                 tc_fence_after_sync();
-                for (int kb = 0; kb < p.num_kb1; ++kb) {
+                for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
                     if (!W.wait(&full[s], ph)) { ok = false; break; }
                     tc_fence_after_sync();
                     const uint32_t st = smem_addr(smem + s * Cfg::STAGE_BYTES);
@@ -174,7 +241,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint64_t bd = smem_desc(st + Cfg::A_BYTES, 16, 1024, SWZ_128B);
 #pragma unroll
                     for (int k = 0; k < Cfg::BK / 16; ++k)   // 32 bytes of K = 2 descriptor units
-                        mma_f16<CG>(t_tmem, ad + 2 * k, bd + 2 * k, p.idesc1, (kb != 0) | (k != 0));
+                        mma_f16<CG>(t_tmem, ad + 2 * k, bd + 2 * k, p.idesc1, (kb != wk.kb0) | (k != 0));
                     commit_all(&empty[s]);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
@@ -182,9 +249,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 commit_all(tfull);
                 // P is in TMEM, and the previous tile's D has been read out (in both CTAs: the
                 // peer's epilogue warps release-arrive, so acquire at cluster scope)
-                if (!W.wait<CG == 2>(pready, it & 1u) || !W.wait<CG == 2>(dempty, (it & 1u) ^ 1u)) break;
+                if (!W.wait<CG == 2>(pready, it & 1u)) break;
+                if (wk.role != ROLE_EARLY && !W.wait<CG == 2>(dempty, (nd++ & 1u) ^ 1u)) break;
                 tc_fence_after_sync();
-                for (int j = 0; j < p.num_kb2; ++j) {
+                for (int j = 0; j < (wk.role == ROLE_EARLY ? 0 : p.num_kb2); ++j) {
                     if (!W.wait(&full[s], ph)) { ok = false; break; }
                     tc_fence_after_sync();
                     const uint64_t ed = smem_desc(smem_addr(smem + s * Cfg::STAGE_BYTES), 16, 1024, SWZ_128B);
@@ -215,18 +283,65 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         const int d_chunks = (p.n2p + EPI_COLS - 1) / EPI_COLS;
         // ec counts the 32 x 32 boxes this warp has stored; box ec uses staging buffer
         // ec % 2, and its C load is that buffer's (ec / 2)-th
-        uint32_t it = 0, ec = 0;
+        // n_early counts the partial T this CTA has published (the phases of epi_sync)
+        uint32_t it = 0, ec = 0, n_early = 0;
         bool ok = true;
-        for (int t = tile0; ok && t < p.tiles; t += tile_step, ++it) {
-            const int m_warp = t * TILE_M * CG + (int)rank * TILE_M + 32 * q;
-            // P = round(T): chunk c of 32 fp32 columns becomes 16 columns of packed pairs at
-            // column 16c, over columns whose T values this warp has already read
+        ChainIter itr(p, tile0, tile_step);
+        Work wk;
+        for (; ok && itr.next(p, wk); ++it) {
+            const int m_warp = wk.tm * TILE_M * CG + (int)rank * TILE_M + 32 * q;
             if (!__all_sync(0xffffffffu, W.wait(tfull, it & 1u))) break;
             tc_fence_after_sync();
+            // stream-K: the partial T of slot wk.slot, this CTA's 128 rows stored column by column
+            // (t_chunks * 32 columns), so that a warp's 32 rows of one column are 128
+            // consecutive bytes; `part` points at this thread's row of column 0
+            float *part = wk.role == ROLE_TILE ? nullptr
+                                               : p.sk_part + (size_t)(wk.slot * CG + (int)rank) * TILE_M * (32 * t_chunks) +
+                                                     32 * q + lane;
+            if (wk.role == ROLE_EARLY) {
+                // hand the partial T over: store it, then publish it once every epilogue
+                // warp's stores are visible
+                for (int c = 0; c < t_chunks; ++c) {
+                    uint32_t acc[32];
+                    tmem_ld_32x32b_x32(tmem_base + lanes + Cfg::T_COL + 32 * c, acc);
+                    tmem_ld_wait(acc);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) part[(size_t)(32 * c + i) * TILE_M] = __uint_as_float(acc[i]);
+                }
+                __threadfence();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    arrive_leader(pready);                 // T's columns have been read
+                    mbar_arrive(epi_sync);
+                }
+                if (e == 0) {
+                    ok = __all_sync(0xffffffffu, W.wait(epi_sync, n_early & 1u));
+                    if (ok && lane == 0) {
+                        __threadfence();
+                        st_release_gpu(p.sk_flags + wk.slot * CG + (int)rank, p.epoch);
+                    }
+                }
+                ++n_early;
+                if (!__all_sync(0xffffffffu, W.wait(dfull, it & 1u))) break;
+                continue;
+            }
+            if (wk.role == ROLE_FINAL) {
+                // the rest of this tile's first product, from the unit whose span starts inside it
+                const bool got = W.wait_flag(p.sk_flags + wk.slot * CG + (int)rank, p.epoch);
+                if (!__all_sync(0xffffffffu, got)) break;
+            }
+            // P = round(T): chunk c of 32 fp32 columns becomes 16 columns of packed pairs at
+            // column 16c, over columns whose T values this warp has already read
             for (int c = 0; c < t_chunks; ++c) {
                 uint32_t acc[32];
                 tmem_ld_32x32b_x32(tmem_base + lanes + Cfg::T_COL + 32 * c, acc);
                 tmem_ld_wait(acc);
+                if (wk.role == ROLE_FINAL) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)   // __ldcg: from L2, not a stale L1 line
+                        acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __ldcg(part + (size_t)(32 * c + i) * TILE_M));
+                }
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -246,8 +361,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             if (use_c && lane == 0) {      // the first C box loads while the second product runs
                 bulk_wait_group_read0();
                 mbar_arrive_expect_tx(&cb[ec & 1u], Cfg::EPI_BUF);
-                tma_load_2d_hint(smem_addr(ebuf + (ec & 1u) * Cfg::EPI_BUF), &tmC, smem_addr(&cb[ec & 1u]), 0, m_warp,
-                                 stream_pol);
+                tma_load_2d_hint(smem_addr(ebuf + (ec & 1u) * Cfg::EPI_BUF), &tmC, smem_addr(&cb[ec & 1u]), 0,
+                                 checked_y(p.status, m_warp, p.M), stream_pol);
             }
             if (!__all_sync(0xffffffffu, W.wait(dfull, it & 1u))) break;
             tc_fence_after_sync();
@@ -267,8 +382,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     const uint32_t nx = cur ^ 1u;
                     bulk_wait_group_read0();                  // the store from buffer nx has read it
                     mbar_arrive_expect_tx(&cb[nx], Cfg::EPI_BUF);
-                    tma_load_2d_hint(smem_addr(ebuf + nx * Cfg::EPI_BUF), &tmC, smem_addr(&cb[nx]), EPI_COLS * (j + 1),
-                                     m_warp, stream_pol);
+                    tma_load_2d_hint(smem_addr(ebuf + nx * Cfg::EPI_BUF), &tmC, smem_addr(&cb[nx]),
+                                     checked_x<4>(p.status, EPI_COLS * (j + 1), p.N2), checked_y(p.status, m_warp, p.M),
+                                     stream_pol);
                 }
                 float v[32];
 #pragma unroll
@@ -306,7 +422,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d_hint(&tmD, smem_addr(buf), EPI_COLS * j, m_warp, stream_pol);
+                    tma_store_2d_hint(&tmD, smem_addr(buf), checked_x<Cfg::OUT_BF16 ? 2 : 4>(p.status, EPI_COLS * j, p.N2),
+                                      checked_y(p.status, m_warp, p.M), stream_pol);
                     bulk_commit_group();
                 }
                 ++ec;

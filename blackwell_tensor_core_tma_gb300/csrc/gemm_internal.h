@@ -156,6 +156,16 @@ struct ChainParams {
     int *status;
     uint64_t timeout_ns;
     int fault;
+    // stream-K over the first product's k-blocks (sk != 0; as in KParams): a tile cut
+    // between two spans is finished by the unit whose span covers its first k-block; the
+    // other stores its partial T (fp32, n1p columns rounded up to 32, of each of its CTA's 128 rows) in
+    // sk_part[unit * CG + rank] and publishes `epoch` in sk_flags[unit * CG + rank]
+    int sk;
+    int sk_dp_tiles;
+    int sk_units;
+    int epoch;
+    int *sk_flags;
+    float *sk_part;
 };
 constexpr int CHAIN_MAX_N = 256;   // N1 and N2 limits: both products' accumulators share 512 TMEM columns
 int chain_smem_bytes(int cta_group);

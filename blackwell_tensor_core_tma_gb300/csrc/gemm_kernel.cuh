@@ -260,7 +260,7 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t a, uint32_t parity, bool ho
             if (honor_abort && *abort_flag) return false;
             if (globaltimer_ns() - t0 > timeout_ns) {
                 *abort_flag = 1;
-                atomicExch(status, (int)GEMM_ERR_TIMEOUT);
+                atomicCAS(status, 0, (int)GEMM_ERR_TIMEOUT);   // the first error recorded stands
                 return false;
             }
         }
@@ -293,7 +293,7 @@ struct Waiter {
                 if (*abort_flag) return false;
                 if (globaltimer_ns() - t0 > timeout_ns) {
                     *abort_flag = 1;
-                    atomicExch(status, (int)GEMM_ERR_TIMEOUT);
+                    atomicCAS(status, 0, (int)GEMM_ERR_TIMEOUT);   // the first error recorded stands
                     return false;
                 }
             }
@@ -342,6 +342,47 @@ __device__ __forceinline__ unsigned long long since(long long t_entry) {
 #else
     return 0ull;
 #endif
+}
+
+// On-device checks of a GB300_CHECKS=1 build (the "checks" library variant; other builds
+// compile them out).  Every TMA coordinate the kernels compute is checked against the
+// tiling it comes from: the innermost coordinate starts on a 16-byte boundary (the
+// copy is illegal otherwise), no coordinate is negative, and each lies inside the
+// operand's extent rounded up to whole tiles (a copy beyond it only reads the fill
+// value, so such a coordinate means a wrong tile or k-block index).  A failed check
+// records GEMM_ERR_CHECK as the run's status (the first error recorded stands) and the
+// coordinate is clamped to a legal value, so that the copy can neither fault nor hang.
+#ifndef GB300_CHECKS
+#define GB300_CHECKS 0
+#endif
+__device__ __forceinline__ void check_fail(int *status) {
+#if GB300_CHECKS
+    atomicCAS(status, 0, (int)GEMM_ERR_CHECK);
+#endif
+}
+
+// innermost coordinate x (elements of ELEM_BYTES bytes) of a copy inside [0, limit)
+template <int ELEM_BYTES>
+__device__ __forceinline__ int checked_x(int *status, int x, int limit) {
+#if GB300_CHECKS
+    constexpr int ALIGN = ELEM_BYTES >= 16 ? 1 : 16 / ELEM_BYTES;
+    if (x < 0 || x % ALIGN != 0 || x >= limit) {
+        check_fail(status);
+        x = x < 0 ? 0 : x - x % ALIGN;
+    }
+#endif
+    return x;
+}
+
+// outer coordinate y of a copy inside [0, limit)
+__device__ __forceinline__ int checked_y(int *status, int y, int limit) {
+#if GB300_CHECKS
+    if (y < 0 || y >= limit) {
+        check_fail(status);
+        if (y < 0) y = 0;
+    }
+#endif
+    return y;
 }
 
 // Byte offset of 16-byte chunk c of staging row `row` under the TMA swizzle whose span is
@@ -500,20 +541,30 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                     auto load = [&](uint32_t dst, const CUtensorMap *m, int c0, int c1) { load_on(dst, m, c0, c1, bar); };
                     // an operand tile: K-major, one box of BK x rows; MN-major, rows / ATOM_MN
                     // boxes of ATOM_MN x BK, one per 128-byte atom column
-                    auto load_operand = [&](uint32_t dst, const CUtensorMap *m, int row0, int rows, bool mn) {
+                    // (row_lim: the operand's rows rounded up to whole tiles; checks builds only)
+                    auto load_operand = [&](uint32_t dst, const CUtensorMap *m, int row0, int rows, bool mn,
+                                            int row_lim) {
+                        constexpr int EB = Cfg::ELEM_BITS == 16 ? 2 : 1;   // bytes of a tensor-map element
                         if (!Cfg::MN_OK || !mn) {
-                            load(dst, m, kb * Cfg::TMA_BK, row0);
+                            load(dst, m, checked_x<EB>(p.status, kb * Cfg::TMA_BK, p.num_kb * Cfg::TMA_BK),
+                                 checked_y(p.status, row0, row_lim));
                         } else {
                             for (int i = 0; i < rows / Cfg::ATOM_MN; ++i)
-                                load(dst + i * Cfg::ATOM_BYTES, m, row0 + i * Cfg::ATOM_MN, kb * Cfg::BK);
+                                load(dst + i * Cfg::ATOM_BYTES, m, checked_x<EB>(p.status, row0 + i * Cfg::ATOM_MN, row_lim),
+                                     checked_y(p.status, kb * Cfg::BK, p.num_kb * Cfg::BK));
                         }
                     };
                     if constexpr (Cfg::SCALED) {    // the scales first: the copier warp starts on them
-                        load_on(sf_dst, &tmSFA, 0, sfa_row, sbar);
-                        load_on(sf_dst + Cfg::SFA_BYTES, &tmSFB, 0, sfb_row, sbar);
+                        load_on(sf_dst, &tmSFA, 0,
+                                checked_y(p.status, sfa_row, p.tiles_m * CG * p.num_kb * (Cfg::SFA_BYTES / 128)), sbar);
+                        load_on(sf_dst + Cfg::SFA_BYTES, &tmSFB, 0,
+                                checked_y(p.status, sfb_row, p.tiles_n * p.num_kb * (Cfg::SFB_BYTES / 128)), sbar);
                     }
-                    load_operand(a_dst, &tmA, m0, TILE_M, p.a_mn != 0);
-                    load_operand(b_dst, &tmB, n0, Cfg::B_ROWS, p.b_mn != 0);
+                    // test hook (fault 2): A rows shifted past the tiled extent, which only reads the
+                    // fill value (wrong D, no fault) and which a checks build reports
+                    const int a_row = m0 + (p.fault == 2 ? p.tiles_m * TILE_M * CG : 0);
+                    load_operand(a_dst, &tmA, a_row, TILE_M, p.a_mn != 0, p.tiles_m * TILE_M * CG);
+                    load_operand(b_dst, &tmB, n0, Cfg::B_ROWS, p.b_mn != 0, p.tiles_n * BN);
                     rc.lap(tr_issue);
                     ++tr_stages;
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -658,7 +709,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
         auto issue = [&](uint32_t i, const CUtensorMap *m, int c0, int c1) {
             if (lane == 0) {
                 mbar_arrive_expect_tx(&cb[i], Cfg::EPI_BUF);
-                tma_load_2d_hint(smem_addr(ebuf + i * Cfg::EPI_BUF), m, smem_addr(&cb[i]), c0, c1, stream_pol);
+                tma_load_2d_hint(smem_addr(ebuf + i * Cfg::EPI_BUF), m, smem_addr(&cb[i]),
+                                 checked_x<4>(p.status, c0, p.N), checked_y(p.status, c1, p.M), stream_pol);
             }
             if (i) ++lc1; else ++lc0;
         };
@@ -713,6 +765,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
             // a stream-K piece that starts its tile waits until its tile's other piece has
             // stored its partial sum into D and published it (the flag carries this run's
             // epoch); this one then adds into D
+            if (GB300_CHECKS && wk.role != ROLE_TILE && (wk.slot < 0 || wk.slot >= p.sk_units)) {
+                check_fail(p.status);           // a stream-K flag outside the plan's flag buffer
+                ok = false;
+                break;
+            }
             auto await_partial = [&]() -> bool {
                 if (wk.role != ROLE_FINAL) return true;
                 const bool got = W.wait_flag(p.sk_flags + wk.slot * CG + (int)rank, p.epoch);
@@ -768,13 +825,15 @@ __global__ void __launch_bounds__(Cfg::THREADS, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    const int dx = n_warp + Cfg::EPI_BOX * jb;
+                    // a store must not start at a negative coordinate
+                    const int dx = checked_x<Cfg::OUT_BF16 ? 2 : 4>(p.status, n_warp + Cfg::EPI_BOX * jb, p.N);
+                    const int dy = checked_y(p.status, m_warp, p.M);
                     if (wk.role == ROLE_EARLY) {
-                        tma_store_2d(&tmD, smem_addr(buf), dx, m_warp);
+                        tma_store_2d(&tmD, smem_addr(buf), dx, dy);
                     } else if (p.splits > 1 || wk.role == ROLE_FINAL) {
-                        tma_reduce_add_2d(&tmD, smem_addr(buf), dx, m_warp);
+                        tma_reduce_add_2d(&tmD, smem_addr(buf), dx, dy);
                     } else {
-                        tma_store_2d_hint(&tmD, smem_addr(buf), dx, m_warp, stream_pol);
+                        tma_store_2d_hint(&tmD, smem_addr(buf), dx, dy, stream_pol);
                     }
                     bulk_commit_group();
                 }

@@ -13,7 +13,8 @@ import os
 
 from . import build as _build
 
-GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ALIGNMENT, GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT = range(6)
+GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_UNSUPPORTED, GEMM_ERR_ALIGNMENT, GEMM_ERR_CUDA, GEMM_ERR_TIMEOUT, \
+    GEMM_ERR_CHECK = range(7)
 GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_F32, GEMM_E2M1 = range(5)
 GEMM_SCALE_NONE, GEMM_SCALE_UE8M0_32, GEMM_SCALE_UE4M3_16 = range(3)
 GEMM_FLAG_SYNC, GEMM_FLAG_FORCE_1CTA, GEMM_FLAG_FORCE_2CTA, GEMM_FLAG_DETERMINISTIC = 0x1, 0x2, 0x4, 0x8

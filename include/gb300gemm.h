@@ -68,7 +68,9 @@ typedef enum {
     GEMM_ERR_UNSUPPORTED = 2,   /* dtype / layout combination or device not handled */
     GEMM_ERR_ALIGNMENT = 3,     /* a base pointer or row stride is not a multiple of 16 bytes */
     GEMM_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed */
-    GEMM_ERR_TIMEOUT = 5        /* a bounded wait inside a kernel ran out; the kernel gave up */
+    GEMM_ERR_TIMEOUT = 5,       /* a bounded wait inside a kernel ran out; the kernel gave up */
+    GEMM_ERR_CHECK = 6          /* an on-device check of a copy coordinate failed (the checks
+                                   build of the library only; see gb300gemm_testing.h) */
 } gemm_status;
 
 typedef enum {
@@ -203,7 +205,12 @@ gemm_status gemm_plan_set_split_k(gemm_plan_t p, int splits);
  * with split-K.  enable = 1 (the default) uses it where it was measured to pay — fp32 D,
  * at least 64 K blocks per tile and fewer than 4 waves — and 0 never; other values
  * return GEMM_ERR_INVALID_ARG.  Runs of one stream-K plan must not overlap on the GPU
- * (they share the flags).
+ * (they share the flags).  Chain plans (gemm_chain_plan_create) take it only on
+ * request (enable = 1; it measured slower than whole tiles on the shapes tried): they
+ * then share out the first product's K blocks the same way when their tiles make more
+ * than one wave but fewer than 4 and not a whole number, with at least 16 K blocks per
+ * tile; the finishing CTA adds the other span's partial T (handed over through a
+ * plan-owned buffer of 128 x N1 fp32 values per CTA of the grid) before rounding.
  */
 gemm_status gemm_plan_set_stream_k(gemm_plan_t p, int enable);
 

@@ -7,8 +7,12 @@
  * arrival on the shared-memory ring, the MMA issuer's wait for that stage
  * runs out after the plan's timeout (gemm_plan_set_timeout), the kernel
  * records GEMM_ERR_TIMEOUT, stops its other roles, frees its tensor memory
- * and returns.  fault = 0 restores normal runs.  Returns
- * GEMM_ERR_INVALID_ARG for a NULL plan or another fault value.
+ * and returns.  With fault = 2 (GEMM plans) the producer computes A's row
+ * coordinates one tiled extent too far: the copies read only the fill value
+ * (D comes out wrong, nothing faults) and the checks build of the library
+ * reports GEMM_ERR_CHECK.  fault = 0 restores normal runs.  Returns
+ * GEMM_ERR_INVALID_ARG for a NULL plan, another fault value, or fault = 2 on a
+ * chain plan.
  */
 #ifndef GB300GEMM_TESTING_H
 #define GB300GEMM_TESTING_H

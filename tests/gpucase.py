@@ -165,8 +165,10 @@ def _assert_within(w, D, D_ref, S, c, what):
 
 # ------------------------------------------------------------ two-product chain
 
-def run_chain(w, flags: int = 0, c_none: bool = False, guard: int = 0, inputs=None, reps: int = 1):
-    """Run a ChainWorkload through gemm_chain_run; returns (inputs, D as fp64, plan info, status, guard intact)."""
+def run_chain(w, flags: int = 0, c_none: bool = False, guard: int = 0, inputs=None, reps: int = 1,
+              stream_k=None):
+    """Run a ChainWorkload through gemm_chain_run; returns (inputs, D as fp64, plan info, status, guard intact).
+    stream_k: None keeps the plan's choice, 0 or 1 is passed to gemm_plan_set_stream_k."""
     import torch
     x = inputs if inputs is not None else synth.make_chain_inputs(w)
     A, B, E = to_device(x["A"]), to_device(x["B"]), to_device(x["E"])
@@ -177,6 +179,8 @@ def run_chain(w, flags: int = 0, c_none: bool = False, guard: int = 0, inputs=No
     buf = torch.full((n + 2 * g,), float("nan"), dtype=tdt, device="cuda")
     D = buf[g:g + n].view(w.M, w.N2)
     with gemm.ChainPlan(w.M, w.N1, w.N2, w.K, w.ab, w.d, flags) as plan:
+        if stream_k is not None:
+            plan.set_stream_k(stream_k)
         for _ in range(reps):
             plan.run(A, B, E, C, D, torch.cuda.current_stream())
         torch.cuda.synchronize()

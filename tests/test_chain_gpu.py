@@ -58,6 +58,25 @@ def test_chain_forced_pairs_on_one_tile(M, K, N1, N2):
     gpucase.check_chain(w, x, D)
 
 
+@pytest.mark.parametrize("M,K,N1,N2,ab,d,flags", [
+    (20480, 1024, 256, 256, "bf16", "bf16", 0),                            # 80 pair tiles on 76 pairs
+    (20000, 1000, 192, 96, "f16", "f32", 0),                               # ragged M and K, 79 pair tiles
+    (20480, 1024, 128, 64, "bf16", "f32", gemm.GEMM_FLAG_FORCE_1CTA),      # 160 single tiles on 152 CTAs
+    (45000, 2048, 64, 160, "bf16", "bf16", 0),                             # 176 pair tiles: two whole rounds first
+])
+def test_chain_stream_k(M, K, N1, N2, ab, d, flags):
+    """Stream-K over the first product (on request: chain plans default to whole tiles): a tile
+    cut between two units is finished by the one that computed its first k-blocks, after adding
+    the other's partial T (the oracle's bound covers the different grouping of the fp32 sums);
+    the same shapes without stream-K agree within it too."""
+    w = synth.scaled_chain(CW, M, N1, N2, K, ab=ab, d=d)
+    x = synth.make_chain_inputs(w)
+    for sk in (1, 0):
+        _, D, info, st, intact = gpucase.run_chain(w, flags=flags, guard=256, inputs=x, stream_k=sk, reps=2)
+        assert st == gemm.GEMM_OK and intact and info["stream_k"] == sk
+        gpucase.check_chain(w, x, D)
+
+
 def test_chain_c_none_and_repeat():
     w = synth.scaled_chain(CW, 640, 128, 96, 384)
     x, D, info, st, intact = gpucase.run_chain(w, c_none=True, guard=256, reps=3)
@@ -68,7 +87,7 @@ def test_chain_c_none_and_repeat():
 def test_chain_full_size_sampled_rows():
     w = CW
     x, D, info, st, intact = gpucase.run_chain(w, guard=1024)
-    assert st == gemm.GEMM_OK and intact and info["cta_group"] == 2
+    assert st == gemm.GEMM_OK and intact and info["cta_group"] == 2 and info["stream_k"] == 0
     rng = np.random.default_rng(0)
     edges = [r for t in range(0, w.M, 128 * 37) for r in (t, t + 31, t + 32, t + 127) if r < w.M]
     rows = np.unique(np.concatenate([edges, [w.M - 1], rng.integers(0, w.M, 160)]))
