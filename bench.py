@@ -39,15 +39,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture
 # summarised in profiles/; valid only for the kernel sources the capture ran on
 MEASURED_TRAFFIC = {
-    "bf16_8192x8192x8192_bf16out": {"bytes": 1139914240 + 123201024, "src": "a2c6296cda029fdf",
+    "bf16_8192x8192x8192_bf16out": {"bytes": 1272258048 + 126285056, "src": "ded2cd43022940ec",
                                     "ncu": "profiles/gemm_tc_kernel_bf16_8192x8192x8192_bf16out_launches.md"},
-    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 610507776 + 234525440, "src": "d30c7b6d9022fc55",
+    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 601085440 + 235996160, "src": "2ae679566da2e08f",
                                           "ncu": "profiles/gemm_tc_kernel_mxf8_8192x8192x8192_launches.md"},
-    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 485758976 + 217974784, "src": "dc410bf7a45fbc9e",
+    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 483755520 + 217433856, "src": "a2c6bfac6c72f49f",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 496706560 + 219912960, "src": "3b1938cd4cb898ee",
+    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 495844096 + 219528960, "src": "c1321fe9c2776aa4",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312781056 + 12135936, "src": "a0a677128a3c896e",
+    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312790016 + 11189248, "src": "c33c93d8a8f47904",
                                               "ncu": "profiles/chain_kernel_bf16_32768x4096_256x256_launches.md"},
 }
 
