@@ -58,54 +58,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return r;
 }
 
-// The pieces one unit (CTA or CTA pair) processes, in order (every role walks the same
-// sequence; Work and the roles are the GEMM kernels').  Without stream-K: whole tiles
-// unit0, unit0 + step, ...  With stream-K: the whole tiles below sk_dp_tiles the same way,
-// then the unit's span of the remaining tiles' first-product k-blocks.  A ROLE_TILE or
-// ROLE_FINAL piece ends with the rounding, the second product and D; a ROLE_EARLY piece
-// (the end of a tile whose start another unit computes) only hands its partial T over.
-struct ChainIter {
-    int unit, step, u;
-    int64_t g, g_end;
-    __device__ __forceinline__ ChainIter(const ChainParams &p, int unit0, int step0)
-        : unit(unit0), step(step0), u(unit0) {
-        g = g_end = 0;
-        if (p.sk) {
-            const int64_t base = (int64_t)p.sk_dp_tiles * p.num_kb1;
-            const int64_t total = (int64_t)(p.tiles - p.sk_dp_tiles) * p.num_kb1;
-            g = base + (int64_t)unit0 * total / p.sk_units;
-            g_end = base + (int64_t)(unit0 + 1) * total / p.sk_units;
-        }
-    }
-    __device__ __forceinline__ bool next(const ChainParams &p, Work &w) {
-        if (u < (p.sk ? p.sk_dp_tiles : p.tiles)) {
-            w.tm = u;
-            w.tn = 0;
-            w.kb0 = 0;
-            w.kb1 = p.num_kb1;
-            w.role = ROLE_TILE;
-            w.slot = 0;
-            u += step;
-            return true;
-        }
-        if (!p.sk || g >= g_end) return false;
-        const int t = (int)(g / p.num_kb1);
-        const int k0 = (int)(g - (int64_t)t * p.num_kb1);
-        const int k1 = (int)min((int64_t)p.num_kb1, (int64_t)k0 + (g_end - g));
-        w.tm = t;
-        w.tn = 0;
-        w.kb0 = k0;
-        w.kb1 = k1;
-        // a span is at least one tile long, so only its first piece can start inside a tile
-        // (this unit publishes it: slot = unit) and only its last can end inside one (the
-        // next unit publishes the rest: slot = unit + 1)
-        w.role = (k0 == 0 && k1 == p.num_kb1) ? ROLE_TILE : (k0 > 0 ? ROLE_EARLY : ROLE_FINAL);
-        w.slot = k0 > 0 ? unit : unit + 1;
-        g += k1 - k0;
-        return true;
-    }
-};
-
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, 1)
     chain_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,

@@ -154,13 +154,17 @@ struct TileCfg {
     static_assert(!SCALED || (SF_WORDS >= 1 && SF_PER_MMA >= 1 && 4 % SF_PER_MMA == 0), "scale vector");
 };
 
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int group_m, int &tm, int &tn, int tiles_n) {
+// The work schedule below is plain integer code that also runs on the host, where a test
+// hook (gemm_schedule.cu) enumerates it without a device.
+#define GB300_HD __host__ __device__ __forceinline__
+
+GB300_HD void tile_coords(int t, int tiles_m, int group_m, int &tm, int &tn, int tiles_n) {
     // groups of group_m M-tiles walk N together so that a wave of CTAs shares
     // A rows and B columns in L2
     const int per_group = group_m * tiles_n;
     const int g = t / per_group;
     const int first_m = g * group_m;
-    const int gsize = min(tiles_m - first_m, group_m);
+    const int gsize = tiles_m - first_m < group_m ? tiles_m - first_m : group_m;
     const int r = t - g * per_group;
     tm = first_m + r % gsize;
     tn = r / gsize;
@@ -169,7 +173,7 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int group_m, int
 // Work unit u = (tile, K slice): the splits slices of a tile are consecutive units, so
 // they run at about the same time on neighbouring CTAs.  Slice s covers k-blocks
 // [s * num_kb / splits, (s + 1) * num_kb / splits), never empty (splits <= num_kb).
-__device__ __forceinline__ void unit_coords(int u, const KParams &p, int &tm, int &tn, int &kb0, int &kb1) {
+GB300_HD void unit_coords(int u, const KParams &p, int &tm, int &tn, int &kb0, int &kb1) {
     const int t = u / p.splits, s = u - t * p.splits;
     tile_coords(t, p.tiles_m, p.group_m, tm, tn, p.tiles_n);
     kb0 = (int)((int64_t)s * p.num_kb / p.splits);
@@ -182,7 +186,7 @@ __device__ __forceinline__ void unit_coords(int u, const KParams &p, int &tm, in
 #ifndef GB300_SERPENTINE_K
 #define GB300_SERPENTINE_K 1
 #endif
-__device__ __forceinline__ int kb_at(int j, int kb0, int kb1, uint32_t round) {
+GB300_HD int kb_at(int j, int kb0, int kb1, uint32_t round) {
     return (GB300_SERPENTINE_K && (round & 1u)) ? kb1 - 1 - j : kb0 + j;
 }
 
@@ -196,6 +200,32 @@ struct Work {
     int tm, tn, kb0, kb1, role, slot;
 };
 
+// Stream-K spans: the k-blocks of tiles [dp_tiles, tiles) in (tile, k-block) order, cut into
+// `units` equal spans; unit u's span is [g, g_end).
+GB300_HD void span_of(int unit, int tiles, int dp_tiles, int num_kb, int units, int64_t &g, int64_t &g_end) {
+    const int64_t base = (int64_t)dp_tiles * num_kb;
+    const int64_t total = (int64_t)(tiles - dp_tiles) * num_kb;
+    g = base + (int64_t)unit * total / units;
+    g_end = base + (int64_t)(unit + 1) * total / units;
+}
+
+// The next piece of a span (g advances past it): k-blocks [kb0, kb1) of flat tile index t
+// (returned).  A span is at least one tile long, so only its first piece can start inside a
+// tile (the end of a tile that the previous unit starts: ROLE_EARLY, published in this
+// unit's slot) and only its last can end inside one (ROLE_FINAL: it waits for the next
+// unit's slot).
+GB300_HD int span_piece(int64_t &g, int64_t g_end, int num_kb, int unit, Work &w) {
+    const int t = (int)(g / num_kb);
+    const int k0 = (int)(g - (int64_t)t * num_kb);
+    const int k1 = (int64_t)k0 + (g_end - g) < (int64_t)num_kb ? (int)((int64_t)k0 + (g_end - g)) : num_kb;
+    w.kb0 = k0;
+    w.kb1 = k1;
+    w.role = (k0 == 0 && k1 == num_kb) ? ROLE_TILE : (k0 > 0 ? ROLE_EARLY : ROLE_FINAL);
+    w.slot = k0 > 0 ? unit : unit + 1;
+    g += k1 - k0;
+    return t;
+}
+
 // The pieces one unit (CTA or CTA pair) processes, in order; every role of the kernel
 // walks the same sequence.  Without stream-K: units tile0, tile0 + step, ... of the
 // (tile x split) list.  With stream-K: first the whole tiles tile0, tile0 + step, ...
@@ -203,16 +233,11 @@ struct Work {
 struct WorkIter {
     int unit, step, u;
     int64_t g, g_end;
-    __device__ __forceinline__ WorkIter(const KParams &p, int unit0, int step0) : unit(unit0), step(step0), u(unit0) {
+    GB300_HD WorkIter(const KParams &p, int unit0, int step0) : unit(unit0), step(step0), u(unit0) {
         g = g_end = 0;
-        if (p.sk) {
-            const int64_t base = (int64_t)p.sk_dp_tiles * p.num_kb;
-            const int64_t total = (int64_t)(p.num_tiles - p.sk_dp_tiles) * p.num_kb;
-            g = base + (int64_t)unit0 * total / p.sk_units;
-            g_end = base + (int64_t)(unit0 + 1) * total / p.sk_units;
-        }
+        if (p.sk) span_of(unit0, p.num_tiles, p.sk_dp_tiles, p.num_kb, p.sk_units, g, g_end);
     }
-    __device__ __forceinline__ bool next(const KParams &p, Work &w) {
+    GB300_HD bool next(const KParams &p, Work &w) {
         if (!p.sk) {
             if (u >= p.num_tiles * p.splits) return false;
             unit_coords(u, p, w.tm, w.tn, w.kb0, w.kb1);
@@ -231,17 +256,38 @@ struct WorkIter {
             return true;
         }
         if (g >= g_end) return false;
-        const int t = (int)(g / p.num_kb);
-        const int k0 = (int)(g - (int64_t)t * p.num_kb);
-        const int k1 = (int)min((int64_t)p.num_kb, (int64_t)k0 + (g_end - g));
+        const int t = span_piece(g, g_end, p.num_kb, unit, w);
         tile_coords(t, p.tiles_m, p.group_m, w.tm, w.tn, p.tiles_n);
-        w.kb0 = k0;
-        w.kb1 = k1;
-        // a span is at least one tile long, so only its first piece can start inside a tile
-        // (the next span's boundary: this unit's slot) and only its last can end inside one
-        w.role = (k0 == 0 && k1 == p.num_kb) ? ROLE_TILE : (k0 > 0 ? ROLE_EARLY : ROLE_FINAL);
-        w.slot = k0 > 0 ? unit : unit + 1;
-        g += k1 - k0;
+        return true;
+    }
+};
+
+// The pieces one unit (CTA or CTA pair) of the two-product chain (gemm_chain.cu) processes,
+// in order.  Tiles are 1-D (rows of D).  Without stream-K: whole tiles unit0, unit0 + step, ...
+// With stream-K: the whole tiles below sk_dp_tiles the same way, then the unit's span of the
+// remaining tiles' first-product k-blocks.  A ROLE_TILE or ROLE_FINAL piece ends with the
+// rounding, the second product and D; a ROLE_EARLY piece only hands its partial T over.
+struct ChainIter {
+    int unit, step, u;
+    int64_t g, g_end;
+    GB300_HD ChainIter(const ChainParams &p, int unit0, int step0) : unit(unit0), step(step0), u(unit0) {
+        g = g_end = 0;
+        if (p.sk) span_of(unit0, p.tiles, p.sk_dp_tiles, p.num_kb1, p.sk_units, g, g_end);
+    }
+    GB300_HD bool next(const ChainParams &p, Work &w) {
+        if (u < (p.sk ? p.sk_dp_tiles : p.tiles)) {
+            w.tm = u;
+            w.tn = 0;
+            w.kb0 = 0;
+            w.kb1 = p.num_kb1;
+            w.role = ROLE_TILE;
+            w.slot = 0;
+            u += step;
+            return true;
+        }
+        if (!p.sk || g >= g_end) return false;
+        w.tm = span_piece(g, g_end, p.num_kb1, unit, w);
+        w.tn = 0;
         return true;
     }
 };

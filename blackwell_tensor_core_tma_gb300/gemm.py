@@ -28,7 +28,7 @@ EXPORTS = ["gemm_plan_create", "gemm_run", "gemm_run_host", "gemm_plan_last_stat
            "gemm_chain_run_host", "gemm_plan_set_stream_k", "gemm_measure_tensor_rate",
            "gemm_testing_pair_tile_n", "gemm_plan_set_clock_meter", "gemm_plan_read_clock_meter",
            "gemm_testing_trace_slots", "gemm_testing_set_trace", "gemm_testing_tmem_ld_probe",
-           "gemm_testing_staging_probe"]
+           "gemm_testing_staging_probe", "gemm_testing_schedule"]
 
 # the per-role trace counters of one CTA, in slot order (a GB300_TRACE=1 library:
 # gemm_testing_set_trace); SM clock cycles unless the name says otherwise
@@ -103,6 +103,9 @@ def lib():
         L.gemm_run_noalloc.restype = st
         L.gemm_testing_pair_tile_n.argtypes = [i64, i64, i64, st, st, ctypes.POINTER(ctypes.c_int)]
         L.gemm_testing_pair_tile_n.restype = st
+        ip = ctypes.POINTER(ctypes.c_int)
+        L.gemm_testing_schedule.argtypes = [st] * 10 + [ip, st, ip]
+        L.gemm_testing_schedule.restype = st
         L.gemm_measure_tensor_rate.argtypes = [st, st, st, i64, ctypes.POINTER(TensorRate)]
         L.gemm_measure_tensor_rate.restype = st
         L.gemm_plan_set_clock_meter.argtypes = [vp, st]
@@ -349,3 +352,20 @@ class ChainPlan(Plan):
 
     def run_host(self, A, B, E, C, D, stream=None):
         return gemm_chain_run_host(self.handle, A, B, E, C, D, stream)
+
+
+def gemm_testing_schedule(chain: bool, tiles_m: int, tiles_n: int, group_m: int, num_kb: int, splits: int,
+                          sk_dp_tiles: int, sk_units: int, unit: int, units: int) -> list:
+    """The pieces (tm, tn, kb0, kb1, role, slot) one unit of the persistent grid processes, from
+    the kernels' own schedule code run on the host (no device needed)."""
+    n = ctypes.c_int()
+    args = (int(bool(chain)), tiles_m, tiles_n, group_m, num_kb, splits, sk_dp_tiles, sk_units, unit, units)
+    cap = 64
+    while True:
+        buf = (ctypes.c_int * (6 * cap))()
+        st = lib().gemm_testing_schedule(*args, buf, cap, ctypes.byref(n))
+        if st != GEMM_OK:
+            raise GemmError(st, "gemm_testing_schedule")
+        if n.value <= cap:
+            return [tuple(buf[6 * i:6 * i + 6]) for i in range(n.value)]
+        cap = n.value

@@ -81,6 +81,23 @@ gemm_status gemm_testing_tmem_ld_probe(uint32_t *host_out, int64_t n_words);
  */
 gemm_status gemm_testing_staging_probe(int pattern, int load, int64_t iters, double *clk_per_access);
 
+/*
+ * The persistent kernels' work schedule, run on the host (no device needed): the pieces
+ * that unit `unit` (a CTA, or a CTA pair) of a grid of `units` processes, in order, six
+ * ints each in out[6 * i ..]: tile row tm, tile column tn (0 for the chain), k-blocks
+ * [kb0, kb1), role (0 a whole tile or split-K slice, 1 the end of a tile that the previous
+ * unit's span starts, 2 the start of a tile that the next unit's span ends) and flag slot.
+ * chain = 0: the GEMM kernels (tiles_m x tiles_n tiles rasterised in groups of group_m
+ * tile rows, splits K slices per tile); chain = 1: the two-product chain (tiles_m tiles;
+ * tiles_n, group_m and splits ignored).  sk_units > 0 selects stream-K: the first
+ * sk_dp_tiles tiles (a multiple of units) whole, then equal spans of the rest, with
+ * sk_units == units and splits == 1.  At most max_pieces are written; *n_pieces gets the
+ * count.  GEMM_ERR_INVALID_ARG for NULL pointers or values outside these ranges.
+ */
+gemm_status gemm_testing_schedule(int chain, int tiles_m, int tiles_n, int group_m, int num_kb, int splits,
+                                  int sk_dp_tiles, int sk_units, int unit, int units, int *out, int max_pieces,
+                                  int *n_pieces);
+
 #ifdef __cplusplus
 }
 #endif
