@@ -39,15 +39,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture
 # summarised in profiles/; valid only for the kernel sources the capture ran on
 MEASURED_TRAFFIC = {
-    "bf16_8192x8192x8192_bf16out": {"bytes": 1272258048 + 126285056, "src": "ded2cd43022940ec",
+    "bf16_8192x8192x8192_bf16out": {"bytes": 1150125568 + 124247808, "src": "75d80999b0321b76",
                                     "ncu": "profiles/gemm_tc_kernel_bf16_8192x8192x8192_bf16out_launches.md"},
-    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 601085440 + 235996160, "src": "2ae679566da2e08f",
+    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 609625856 + 234899456, "src": "5c4a4907ca02d314",
                                           "ncu": "profiles/gemm_tc_kernel_mxf8_8192x8192x8192_launches.md"},
-    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 483755520 + 217433856, "src": "a2c6bfac6c72f49f",
+    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 484349696 + 217867520, "src": "2234cd6b9880b778",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 495844096 + 219528960, "src": "c1321fe9c2776aa4",
+    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 496391424 + 219592960, "src": "210fee83283db6a2",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312790016 + 11189248, "src": "c33c93d8a8f47904",
+    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312839168 + 11273216, "src": "72a0c97ada588dce",
                                               "ncu": "profiles/chain_kernel_bf16_32768x4096_256x256_launches.md"},
 }
 
