@@ -30,7 +30,8 @@ VARIANTS = {
     "": [],
     "trace": ["-DGB300_TRACE=1"],
     "checks": ["-DGB300_CHECKS=1", "-DGB300_F16_CG1_STAGES=3", "-DGB300_F16_CG2_STAGES=5",
-               "-DGB300_MXF8_PAIR_STAGES=5", "-DGB300_MXF4_PAIR_STAGES=4", "-DGB300_NVF4_PAIR_STAGES=4"],
+               "-DGB300_MXF8_PAIR_STAGES=5", "-DGB300_MXF8_NARROW_STAGES=4", "-DGB300_MXF4_PAIR_STAGES=4",
+               "-DGB300_NVF4_PAIR_STAGES=4"],
 }
 
 

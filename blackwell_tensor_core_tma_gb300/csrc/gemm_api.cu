@@ -72,6 +72,7 @@ struct gemm_plan {
     int split_request;        // 0 = choose automatically, n >= 1 = asked for
     int sk_request;           // stream-K: 1 = where it balances the waves (default), 0 = never
     int wide_epi;             // fp16/bf16 pairs, fp32 D, short K: the 8-epilogue-warp kernel
+    bool narrow;              // block-scaled pairs: the family's narrow pair form (e4m3: 256 x 224 tiles)
     int sk;                   // stream-K chosen
     int sk_dp_tiles;          // stream-K: tiles the units take whole before their spans
     int *sk_flags;            // stream-K: one flag per (slot, CTA of the group)
@@ -233,6 +234,29 @@ int pair_tile_n(int64_t M, int64_t N, int64_t K, bool f32, int units) {
     return eff(F16_NARROW_N) > 1.02 * eff(TILE_N) ? F16_NARROW_N : TILE_N;
 }
 
+// The column width of an e4m3 CTA-pair tile: 256 (one accumulator, drained to registers
+// before the next tile starts) or 224 (two accumulators, the next tile accumulating while the
+// epilogue drains).  Estimated efficiency = used share of the tile columns x busy share of the
+// rounds (0.89 where stream-K balances them) x, for 256, the tile boundary it waits at (~3.8
+// k-blocks' time per tile after the first of a unit) or, for 224, the 7 % more operand bytes
+// per FLOP; 224 must win by 5 %.  Measured (one GPU call, 200 runs): 4096^3 224 +16 %,
+// 4096 x 4096 x 8192 +6 %; 8192^3 -3 %, 6144^3 -2 %, 3072 x 3072 x 8192 -3 %: the rule
+// takes 224 for the first two only.
+int e4m3_pair_tile_n(int64_t M, int64_t N, int64_t K, bool f32, int units) {
+    const int64_t tiles_m = (M + 2 * TILE_M - 1) / (2 * TILE_M), kb = (K + 127) / 128;
+    auto eff = [&](int bn) {
+        const int64_t tn = (N + bn - 1) / bn, tiles = tiles_m * tn;
+        const int64_t rounds = (tiles + units - 1) / units;
+        const bool sk = f32 && kb >= GB300_SK_MIN_KB && tiles >= units && tiles % units != 0 && tiles < 4 * units;
+        double e = (double)N / (double)(tn * bn);
+        e *= sk ? 0.89 : (double)tiles / (double)(rounds * units);
+        if (bn == MXF8_NARROW_N) e *= 0.93;
+        else e *= 1.0 - 3.8 / (double)kb * (1.0 - 1.0 / (double)rounds);
+        return e;
+    };
+    return eff(MXF8_NARROW_N) > 1.05 * eff(TILE_N) ? MXF8_NARROW_N : TILE_N;
+}
+
 gemm_status configure_f16(gemm_plan *p) {
     int cg = (p->M >= 1024 && p->N >= 1024) ? 2 : 1;
     if (p->flags & GEMM_FLAG_FORCE_1CTA) cg = 1;
@@ -282,8 +306,18 @@ gemm_status configure_scaled(gemm_plan *p) {
         cg = 2;
     }
     const int bf = p->d == GEMM_BF16;
-    if (fam.prepare(cg, bf) != cudaSuccess) return GEMM_ERR_CUDA;
-    const ScaledShape sh = fam.shape(cg);
+    // e4m3 pairs: the narrow form where it fills the rounds clearly better (an N-contiguous B
+    // needs whole 128-element atoms per CTA, which its 112 rows are not)
+    p->narrow = false;
+    if (cg == 2 && fam.has_narrow && !p->b_mn) {
+        int units = p->sm_count / 2, clusters = 0;
+        if (fam.prepare(cg, bf, false) == cudaSuccess && fam.max_active_clusters(cg, bf, false, &clusters) == cudaSuccess &&
+            clusters > 0)
+            units = clusters;
+        p->narrow = e4m3_pair_tile_n(p->M, p->N, p->K, p->d == GEMM_F32, units) == MXF8_NARROW_N;
+    }
+    if (fam.prepare(cg, bf, p->narrow) != cudaSuccess) return GEMM_ERR_CUDA;
+    const ScaledShape sh = fam.shape(cg, p->narrow);
     p->cta_group = cg;
     p->tile_n = sh.tile_n;
     p->epi_box = sh.epi_box;
@@ -299,7 +333,7 @@ gemm_status configure_scaled(gemm_plan *p) {
     int units = p->sm_count / cg;
     if (cg == 2) {
         int clusters = 0;
-        if (fam.max_active_clusters(cg, bf, &clusters) == cudaSuccess && clusters > 0) units = clusters;
+        if (fam.max_active_clusters(cg, bf, p->narrow, &clusters) == cudaSuccess && clusters > 0) units = clusters;
     }
     p->capacity = units;
     p->grid = cg * (p->tiles < units ? p->tiles : units);
@@ -559,7 +593,7 @@ gemm_status gemm_run(gemm_plan_t p, const void *A, const void *B, const void *C,
         if (sf_pack(SFA, SFB, p->ws_a, p->ws_b, kp.M, kp.N, sfk, p->tiles_m * p->cta_group, p->tiles_n, p->tile_n,
                     n_wg, unit_scale(p->family), stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
-        if (scaled_family(p->family).launch(p->cta_group, p->d == GEMM_BF16, shape, p->maps, kp, stream) !=
+        if (scaled_family(p->family).launch(p->cta_group, p->d == GEMM_BF16, p->narrow, shape, p->maps, kp, stream) !=
             cudaSuccess)
             return GEMM_ERR_CUDA;
     } else {
@@ -643,7 +677,7 @@ gemm_status launch_rows(gemm_plan *p, const void *A, const void *B, const void *
         if (sf_pack(SFA, SFB, p->ws_a, p->ws_b, kp.M, kp.N, sfk, kp.tiles_m * cg, p->tiles_n, p->tile_n, n_wg,
                     unit_scale(p->family), stream) != cudaSuccess)
             return GEMM_ERR_CUDA;
-        return scaled_family(p->family).launch(cg, p->d == GEMM_BF16, shape, maps, kp, stream) == cudaSuccess
+        return scaled_family(p->family).launch(cg, p->d == GEMM_BF16, p->narrow, shape, maps, kp, stream) == cudaSuccess
                    ? GEMM_OK
                    : GEMM_ERR_CUDA;
     }
@@ -1009,6 +1043,14 @@ gemm_status gemm_testing_pair_tile_n(int64_t M, int64_t N, int64_t K, gemm_dtype
     if (!tile_n || M <= 0 || N <= 0 || K <= 0 || units <= 0 || (d != GEMM_F32 && d != GEMM_BF16))
         return GEMM_ERR_INVALID_ARG;
     *tile_n = pair_tile_n(M, N, K, d == GEMM_F32, units);
+    return GEMM_OK;
+}
+
+// Test hook (declared in include/gb300gemm_testing.h): the e4m3 CTA-pair tile-width rule alone.
+gemm_status gemm_testing_e4m3_pair_tile_n(int64_t M, int64_t N, int64_t K, gemm_dtype d, int units, int *tile_n) {
+    if (!tile_n || M <= 0 || N <= 0 || K <= 0 || units <= 0 || (d != GEMM_F32 && d != GEMM_BF16))
+        return GEMM_ERR_INVALID_ARG;
+    *tile_n = e4m3_pair_tile_n(M, N, K, d == GEMM_F32, units);
     return GEMM_OK;
 }
 

@@ -124,14 +124,19 @@ struct ScaledShape {
     int epi_box;     // columns of the epilogue's C / D boxes (32 or 16)
 };
 
-// A block-scaled kernel family: its four instances (CTA group 1 / 2 x D fp32 / bf16)
+// A block-scaled kernel family: its instances (CTA group 1 / 2 x D fp32 / bf16, and for e4m3 a
+// narrow CTA-pair form: 256 x 224 tiles with two accumulators; `narrow` selects it, and
+// families without one (has_narrow false) ignore it)
 struct ScaledFamily {
-    ScaledShape (*shape)(int cta_group);
-    cudaError_t (*prepare)(int cta_group, int out_bf16);      // set the kernel's shared-memory limit
-    cudaError_t (*max_active_clusters)(int cta_group, int out_bf16, int *clusters);
-    cudaError_t (*launch)(int cta_group, int out_bf16, const LaunchShape &shape, const CUtensorMap *maps,
+    ScaledShape (*shape)(int cta_group, bool narrow);
+    cudaError_t (*prepare)(int cta_group, int out_bf16, bool narrow);      // set the kernel's shared-memory limit
+    cudaError_t (*max_active_clusters)(int cta_group, int out_bf16, bool narrow, int *clusters);
+    cudaError_t (*launch)(int cta_group, int out_bf16, bool narrow, const LaunchShape &shape, const CUtensorMap *maps,
                           const KParams &p, cudaStream_t stream);
+    bool has_narrow;
 };
+// the narrow e4m3 pair tile's columns
+constexpr int MXF8_NARROW_N = 224;
 const ScaledFamily &family_mxf8();   // gemm_mxf8.cu
 const ScaledFamily &family_mxf4();   // gemm_mxf4.cu
 const ScaledFamily &family_nvf4();   // gemm_nvf4.cu

@@ -40,6 +40,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 
 
 #include "gemm_internal.h"
@@ -1016,38 +1017,53 @@ cudaError_t max_active_clusters_tc(int *clusters) {
     return cudaOccupancyMaxActiveClusters(clusters, reinterpret_cast<const void *>(&gemm_tc_kernel<Cfg>), &lc);
 }
 
-// The four instances (CTA group 1 / 2, D fp32 / bf16) of a block-scaled family
-template <class C1F, class C1B, class C2F, class C2B>
+// The instances (CTA group 1 / 2, D fp32 / bf16, and optionally a narrow pair form) of a
+// block-scaled family
+template <class C1F, class C1B, class C2F, class C2B, class C2NF = C2F, class C2NB = C2B>
 struct ScaledInstances {
-    static ScaledShape shape(int cta_group) {
-        return cta_group == 1 ? ScaledShape{C1F::BN, C1F::STAGES, C1F::SMEM_BYTES, C1F::BK, C1F::SFA_BYTES, C1F::SFB_BYTES,
-                                            C1F::EPI_BOX}
-                              : ScaledShape{C2F::BN, C2F::STAGES, C2F::SMEM_BYTES, C2F::BK, C2F::SFA_BYTES, C2F::SFB_BYTES,
-                                            C2F::EPI_BOX};
+    static constexpr bool HAS_NARROW = !std::is_same<C2NF, C2F>::value;
+    template <class C>
+    static ScaledShape shape_of() {
+        return ScaledShape{C::BN, C::STAGES, C::SMEM_BYTES, C::BK, C::SFA_BYTES, C::SFB_BYTES, C::EPI_BOX};
     }
-    static cudaError_t prepare(int cta_group, int out_bf16) {
+    static ScaledShape shape(int cta_group, bool narrow) {
+        if (cta_group == 1) return shape_of<C1F>();
+        return narrow ? shape_of<C2NF>() : shape_of<C2F>();
+    }
+    static cudaError_t prepare(int cta_group, int out_bf16, bool narrow) {
         if (cta_group == 1) return out_bf16 ? prepare_tc<C1B>() : prepare_tc<C1F>();
+        if (narrow) return out_bf16 ? prepare_tc<C2NB>() : prepare_tc<C2NF>();
         return out_bf16 ? prepare_tc<C2B>() : prepare_tc<C2F>();
     }
-    static cudaError_t max_active_clusters(int cta_group, int out_bf16, int *clusters) {
+    static cudaError_t max_active_clusters(int cta_group, int out_bf16, bool narrow, int *clusters) {
         if (cta_group == 1)
             return out_bf16 ? max_active_clusters_tc<C1B>(clusters) : max_active_clusters_tc<C1F>(clusters);
+        if (narrow) return out_bf16 ? max_active_clusters_tc<C2NB>(clusters) : max_active_clusters_tc<C2NF>(clusters);
         return out_bf16 ? max_active_clusters_tc<C2B>(clusters) : max_active_clusters_tc<C2F>(clusters);
     }
-    static cudaError_t launch(int cta_group, int out_bf16, const LaunchShape &shape, const CUtensorMap *maps,
-                              const KParams &p, cudaStream_t stream) {
+    static cudaError_t launch(int cta_group, int out_bf16, bool narrow, const LaunchShape &shape,
+                              const CUtensorMap *maps, const KParams &p, cudaStream_t stream) {
         if (cta_group == 1)
             return out_bf16 ? launch_tc<C1B>(shape, maps, p, stream) : launch_tc<C1F>(shape, maps, p, stream);
+        if (narrow)
+            return out_bf16 ? launch_tc<C2NB>(shape, maps, p, stream) : launch_tc<C2NF>(shape, maps, p, stream);
         return out_bf16 ? launch_tc<C2B>(shape, maps, p, stream) : launch_tc<C2F>(shape, maps, p, stream);
     }
     static const ScaledFamily &family() {
-        static const ScaledFamily f{&shape, &prepare, &max_active_clusters, &launch};
+        static const ScaledFamily f{&shape, &prepare, &max_active_clusters, &launch, HAS_NARROW};
         return f;
     }
-    static_assert(C1F::CG == 1 && C1B::CG == 1 && C2F::CG == 2 && C2B::CG == 2, "CTA groups");
-    static_assert(!C1F::OUT_BF16 && C1B::OUT_BF16 && !C2F::OUT_BF16 && C2B::OUT_BF16, "D types");
-    static_assert(C1F::SF_WORDS == C2F::SF_WORDS && C1F::BK == C2F::BK, "one packed scale layout per family");
-    static_assert(C1F::EPI_BOX == C1B::EPI_BOX && C2F::EPI_BOX == C2B::EPI_BOX, "one C / D box per CTA group");
+    static_assert(C1F::CG == 1 && C1B::CG == 1 && C2F::CG == 2 && C2B::CG == 2 && C2NF::CG == 2 && C2NB::CG == 2,
+                  "CTA groups");
+    static_assert(!C1F::OUT_BF16 && C1B::OUT_BF16 && !C2F::OUT_BF16 && C2B::OUT_BF16 && !C2NF::OUT_BF16 &&
+                      C2NB::OUT_BF16,
+                  "D types");
+    static_assert(C1F::SF_WORDS == C2F::SF_WORDS && C1F::BK == C2F::BK && C2NF::SF_WORDS == C2F::SF_WORDS &&
+                      C2NF::BK == C2F::BK,
+                  "one packed scale layout per family");
+    static_assert(C1F::EPI_BOX == C1B::EPI_BOX && C2F::EPI_BOX == C2B::EPI_BOX && C2NF::EPI_BOX == C2NB::EPI_BOX,
+                  "one C / D box per CTA group");
+    static_assert(!HAS_NARROW || C2NF::BN == MXF8_NARROW_N, "narrow pair tile");
 };
 
 }  // namespace gb300

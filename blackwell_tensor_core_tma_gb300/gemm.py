@@ -28,7 +28,7 @@ EXPORTS = ["gemm_plan_create", "gemm_run", "gemm_run_host", "gemm_plan_last_stat
            "gemm_chain_run_host", "gemm_plan_set_stream_k", "gemm_measure_tensor_rate",
            "gemm_testing_pair_tile_n", "gemm_plan_set_clock_meter", "gemm_plan_read_clock_meter",
            "gemm_testing_trace_slots", "gemm_testing_set_trace", "gemm_testing_tmem_ld_probe",
-           "gemm_testing_staging_probe", "gemm_testing_schedule"]
+           "gemm_testing_staging_probe", "gemm_testing_schedule", "gemm_testing_e4m3_pair_tile_n"]
 
 # the per-role trace counters of one CTA, in slot order (a GB300_TRACE=1 library:
 # gemm_testing_set_trace); SM clock cycles unless the name says otherwise
@@ -103,6 +103,8 @@ def lib():
         L.gemm_run_noalloc.restype = st
         L.gemm_testing_pair_tile_n.argtypes = [i64, i64, i64, st, st, ctypes.POINTER(ctypes.c_int)]
         L.gemm_testing_pair_tile_n.restype = st
+        L.gemm_testing_e4m3_pair_tile_n.argtypes = [i64, i64, i64, st, st, ctypes.POINTER(ctypes.c_int)]
+        L.gemm_testing_e4m3_pair_tile_n.restype = st
         ip = ctypes.POINTER(ctypes.c_int)
         L.gemm_testing_schedule.argtypes = [st] * 10 + [ip, st, ip]
         L.gemm_testing_schedule.restype = st

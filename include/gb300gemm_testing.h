@@ -35,6 +35,15 @@ gemm_status gemm_testing_set_fault(gemm_plan_t p, int fault);
 gemm_status gemm_testing_pair_tile_n(int64_t M, int64_t N, int64_t K, gemm_dtype d, int units, int *tile_n);
 
 /*
+ * The e4m3 CTA-pair plans' tile-width rule alone, without a device: 256 (one accumulator) or
+ * 224 (two accumulators, the narrow form) columns for M x N x K with D of type d (GEMM_F32 or
+ * GEMM_BF16) when `units` pairs run at once.  Plans with a row-major (N-contiguous) B keep 256
+ * whatever the rule says.  *tile_n is written on GEMM_OK; GEMM_ERR_INVALID_ARG for NULL
+ * tile_n, non-positive sizes or another d.
+ */
+gemm_status gemm_testing_e4m3_pair_tile_n(int64_t M, int64_t N, int64_t K, gemm_dtype d, int units, int *tile_n);
+
+/*
  * Per-role clock trace of the GEMM kernels, for finding what a kernel waits on.  Only a
  * library compiled with GB300_TRACE=1 (the "trace" build variant, libgb300gemm_trace.so)
  * keeps it; the default build compiles every mark out.  gemm_testing_trace_slots()

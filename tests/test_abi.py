@@ -5,6 +5,7 @@ import re
 
 import pytest
 
+from tests import rules
 from blackwell_tensor_core_tma_gb300 import build, gemm
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -179,6 +180,27 @@ def test_pair_tile_rule_without_device(lib):
     assert lib.gemm_testing_pair_tile_n(0, 1, 1, gemm.GEMM_F32, 76, ctypes.byref(out)) == gemm.GEMM_ERR_INVALID_ARG
     assert lib.gemm_testing_pair_tile_n(1, 1, 1, gemm.GEMM_F16, 76, ctypes.byref(out)) == gemm.GEMM_ERR_INVALID_ARG
     assert lib.gemm_testing_pair_tile_n(1, 1, 1, gemm.GEMM_F32, 76, None) == gemm.GEMM_ERR_INVALID_ARG
+
+
+def test_e4m3_pair_tile_rule_without_device(lib):
+    import ctypes
+    import numpy as np
+    out = ctypes.c_int()
+    # the measured cases: 224 won at 4096^3 (+16 %) and 4096 x 4096 x 8192 (+6 %, against
+    # 256-wide tiles under stream-K) and lost at 8192^3, 6144^3 and 3072 x 3072 x 8192
+    for (M, N, K), want in [((4096, 4096, 4096), 224), ((4096, 4096, 8192), 224), ((8192, 8192, 8192), 256),
+                            ((6144, 6144, 6144), 256), ((3072, 3072, 8192), 256)]:
+        assert lib.gemm_testing_e4m3_pair_tile_n(M, N, K, gemm.GEMM_F32, 76, ctypes.byref(out)) == gemm.GEMM_OK
+        assert out.value == want, (M, N, K)
+    rng = np.random.default_rng(9)
+    for _ in range(2000):
+        M, N, K = (int(v) for v in rng.integers(1, 20000, 3))
+        d = gemm.GEMM_F32 if rng.integers(2) else gemm.GEMM_BF16
+        units = int(rng.integers(1, 160))
+        assert lib.gemm_testing_e4m3_pair_tile_n(M, N, K, d, units, ctypes.byref(out)) == gemm.GEMM_OK
+        assert out.value == rules.e4m3_tile_rule(M, N, K, d == gemm.GEMM_F32, units), (M, N, K, d, units)
+    assert lib.gemm_testing_e4m3_pair_tile_n(0, 1, 1, gemm.GEMM_F32, 76, ctypes.byref(out)) == gemm.GEMM_ERR_INVALID_ARG
+    assert lib.gemm_testing_e4m3_pair_tile_n(1, 1, 1, gemm.GEMM_F32, 76, None) == gemm.GEMM_ERR_INVALID_ARG
 
 
 def test_product_code_does_not_reach_the_oracle():

@@ -6,6 +6,7 @@ corners and edges, a full row and column, and random entries."""
 import numpy as np
 import pytest
 
+from tests import rules
 from blackwell_tensor_core_tma_gb300 import gemm, synth
 from tests import gpucase
 
@@ -105,9 +106,33 @@ def test_block_scaled_small(variant, M, N, K, d, c):
     w = synth.scaled(MXF8, M, N, K, d=d, c=c)
     x, D, info, st, intact = gpucase.run(w, flags=FORCE[variant], guard=512)
     assert st == gemm.GEMM_OK and intact
-    assert info["tile_n"] == (224 if variant == "1cta" else 256) and info["launches_per_run"] == 2
+    # single CTAs: 128 x 224 tiles; pairs: the plan's rule (256, or 224 with two accumulators)
+    assert info["tile_n"] == (224 if variant == "1cta" else rules.e4m3_tile_rule(M, N, K, d == "f32"))
+    assert info["launches_per_run"] == 2
     assert info["cta_group"] == (1 if variant == "1cta" else 2)
     gpucase.check_full(w, x, D)
+
+
+@pytest.mark.parametrize("M,N,K,d,c_none,b_row", [
+    (4096, 4096, 4096, "f32", False, False),   # 304 narrow tiles: four whole rounds (+16 % measured)
+    (1100, 1504, 2080, "bf16", False, False),  # ragged M, N and K, bf16 D
+    (2000, 1300, 1024, "f32", True, False),    # C absent
+    (1536, 2048, 1024, "f32", False, True),    # N-contiguous B: 112 rows are not whole atoms, 256 kept
+])
+def test_e4m3_pair_tile_forms(M, N, K, d, c_none, b_row):
+    """CTA pairs with 256 x 224 tiles and two accumulators (the narrow form), where the plan's
+    rule picks them, against the oracle."""
+    w = synth.scaled(MXF8, M, N, K, d=d, c="normal", b_row_major=b_row)
+    x, D, info, st, intact = gpucase.run(w, c_none=c_none, guard=512)
+    assert st == gemm.GEMM_OK and intact and info["cta_group"] == 2
+    assert info["tile_n"] == (256 if b_row else rules.e4m3_tile_rule(M, N, K, d == "f32"))
+    if not b_row:
+        assert info["tile_n"] == 224
+    if M * N * K > 2 ** 34:                    # sampled entries (C present)
+        rows, cols = gpucase.sample_entries(w.M, w.N, info["tile_m"], info["tile_n"], n_random=4096)
+        gpucase.check_entries(w, x, D, rows, cols)
+    else:
+        gpucase.check_full(w, x, D, c_none=c_none)
 
 
 def test_block_scaled_c_null():
