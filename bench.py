@@ -39,15 +39,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture
 # summarised in profiles/; valid only for the kernel sources the capture ran on
 MEASURED_TRAFFIC = {
-    "bf16_8192x8192x8192_bf16out": {"bytes": 1150125568 + 124247808, "src": "75d80999b0321b76",
+    "bf16_8192x8192x8192_bf16out": {"bytes": 1173044992 + 125537536, "src": "89c72174f571aa96",
                                     "ncu": "profiles/gemm_tc_kernel_bf16_8192x8192x8192_bf16out_launches.md"},
-    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 609625856 + 234899456, "src": "5c4a4907ca02d314",
+    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 605222144 + 235942144, "src": "c3850e7cc6c352d4",
                                           "ncu": "profiles/gemm_tc_kernel_mxf8_8192x8192x8192_launches.md"},
-    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 484349696 + 217867520, "src": "2234cd6b9880b778",
+    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 484580608 + 217747456, "src": "5b3fb74d88415af5",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 496391424 + 219592960, "src": "210fee83283db6a2",
+    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 496498688 + 219558400, "src": "26aa4ebdb229b4af",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312839168 + 11273216, "src": "72a0c97ada588dce",
+    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 313114112 + 11098368, "src": "7d59495d7d8f4082",
                                               "ncu": "profiles/chain_kernel_bf16_32768x4096_256x256_launches.md"},
 }
 
