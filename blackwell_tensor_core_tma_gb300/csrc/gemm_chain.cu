@@ -1,16 +1,16 @@
 // Two chained tensor-core products with the intermediate kept in tensor memory
 // ("Tensor Core 数据布局的演进", section "TMEM 中的累加器": some tcgen05.mma forms
 // read A from TMEM instead of shared memory):
-//     T = A·B        128 x N1 per tile, fp32 accumulator in TMEM columns [0, 256)
+//     T = A·B        128 x N1 per CTA, fp32 accumulator in TMEM columns [0, 256)
 //     P = round(T)   to the operand type, written back over T's first columns: two
 //                    16-bit elements per 32-bit column, the lower K index in the low half
 //     D = C + P·E    tcgen05.mma with A = P read from TMEM and E from shared memory,
 //                    fp32 accumulator in TMEM columns [256, 512)
-// so the intermediate never leaves the SM (except, with stream-K, the partial T of a
-// tile cut between two units, which goes through global memory once).  One CTA (CG = 1) or one CTA pair
-// (CG = 2, cta_group::2: 256 rows, each CTA holding its 128 rows of A, T, P and D
-// and half of B's and E's rows) owns a tile at a time and walks the tiles
-// persistently.  Pairs halve the B and E bytes each SM takes in per row of A: the
+// so the intermediate never leaves the SM (except, with stream-K, which plans take on
+// request only, the partial T of a tile cut between two units, which goes through
+// global memory once).  One CTA (CG = 1) or one CTA pair (CG = 2, cta_group::2: 256
+// rows, each CTA holding its 128 rows of A, T, P and D and half of B's and E's rows)
+// owns a tile at a time and walks the tiles persistently.  Pairs halve the B and E bytes each SM takes in per row of A: the
 // chain's main loop is bound by what one SM can take in (B is re-read by every
 // tile), not by the L2.  Warp roles (192 threads per CTA):
 //   warp 0     TMA producer (each CTA): per tile the K blocks of A and B, then the
