@@ -401,11 +401,14 @@ gemm_status choose_splits(gemm_plan *p) {
     }
     // whole-tile fp16/bf16 pairs with fp32 D and short K: the tile's C-in/D-out epilogue
     // outlasts the next tile's main loop, so twice the epilogue warps (one stage fewer)
-    // pay; with bf16 D or longer K they lose (measured on GB300)
+    // pay; with bf16 D or longer K they lose (measured on GB300).  Single CTAs that take at
+    // most one short tile each: the run is mostly that tile's epilogue, which 8 warps
+    // halve (either D type)
     if (p->family == KIND_F16) {
         F16Config cfg{p->cta_group, p->d == GEMM_BF16, 0, p->tile_n};
-        cfg.wide_epi = p->cta_group == 2 && p->tile_n == TILE_N && p->d == GEMM_F32 && s == 1 && !p->sk &&
-                       p->num_kb <= 40;
+        cfg.wide_epi = (p->cta_group == 2 && p->tile_n == TILE_N && p->d == GEMM_F32 && s == 1 && !p->sk &&
+                        p->num_kb <= 40) ||
+                       (p->cta_group == 1 && s == 1 && !p->sk && p->tiles <= units && p->num_kb <= 40);
         if (cfg.wide_epi && f16_prepare(cfg) != cudaSuccess) return GEMM_ERR_CUDA;
         p->wide_epi = cfg.wide_epi;
         p->stages = f16_stages(cfg);
