@@ -39,15 +39,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu capture
 # summarised in profiles/; valid only for the kernel sources the capture ran on
 MEASURED_TRAFFIC = {
-    "bf16_8192x8192x8192_bf16out": {"bytes": 1173044992 + 125537536, "src": "89c72174f571aa96",
+    "bf16_8192x8192x8192_bf16out": {"bytes": 1139664128 + 124062720, "src": "074331377af61419",
                                     "ncu": "profiles/gemm_tc_kernel_bf16_8192x8192x8192_bf16out_launches.md"},
-    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 605222144 + 235942144, "src": "c3850e7cc6c352d4",
+    "mxf8e4m3_8192x8192x8192_c0_f32out": {"bytes": 609121280 + 235741952, "src": "3a8d4b60a298d33a",
                                           "ncu": "profiles/gemm_tc_kernel_mxf8_8192x8192x8192_launches.md"},
-    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 484580608 + 217747456, "src": "5b3fb74d88415af5",
+    "mxf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 483959040 + 218009856, "src": "7a56a78b84b639d1",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 496498688 + 219558400, "src": "26aa4ebdb229b4af",
+    "nvf4e2m1_8192x8192x8192_c0_f32out": {"bytes": 495177472 + 219982848, "src": "6f369e190bf36c4c",
                                           "ncu": "profiles/gemm_tc_kernel_fp4_8192x8192x8192_launches.md"},
-    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 313114112 + 11098368, "src": "7d59495d7d8f4082",
+    "chain_bf16_32768x4096_256x256_bf16out": {"bytes": 312649216 + 11200512, "src": "fcd2357da88d26b3",
                                               "ncu": "profiles/chain_kernel_bf16_32768x4096_256x256_launches.md"},
 }
 
