@@ -156,8 +156,9 @@ gemm_status gemm_run_host(gemm_plan_t p, const void *A, const void *B, const voi
 
 /*
  * Wait for the stream of the plan's last run, read the plan's device status
- * word (GEMM_OK, or GEMM_ERR_TIMEOUT if a kernel gave up on a wait) and
- * reset it to GEMM_OK.
+ * word (GEMM_OK, GEMM_ERR_TIMEOUT if a kernel gave up on a wait, or, in the
+ * checks build only, GEMM_ERR_CHECK if a copy coordinate failed its check; the
+ * first error a run records stands) and reset it to GEMM_OK.
  */
 gemm_status gemm_plan_last_status(gemm_plan_t p);
 
